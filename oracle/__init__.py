@@ -1,0 +1,228 @@
+"""fp64 CPU oracle for exact attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never calls it and
+shares no code with it.
+
+The numerical work lives in ``attn_oracle.c`` (plain C, fp64, materialised
+score matrices); this module compiles it with gcc and wraps it with ctypes.
+``recurrence.py`` restates the blockwise online-softmax recurrence and the
+split combine for the invariant tests, and ``formulas.py`` holds the closed
+forms the pages print (score bytes, KV-cache bytes, arithmetic intensity,
+softmax operation counts).
+
+Sources (page title, section):
+  auturnal.com "From attention to IO-aware execution" §2 (SDPA), §8 (max
+  subtraction, (m, l, u) statistics), §9 (KV-cache size);
+  papanda925.com "Transformer complexity strategies", standard-attention
+  pseudocode and KV-cache concept;
+  code-journey.com "Attention co-design for long-context inference", Group
+  Size (G);
+  marketmaker.cc "Flash Attention and sequence length", causal masking.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+# element-format codes shared with attn_oracle.c (its own enum)
+F16, BF16, F32, E4M3, F64 = 0, 1, 2, 3, 4
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into liboracle.so (gcc -O2 -fopenmp)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        vp, i32, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        L.oracle_sdpa.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
+                                  i32, f64, i32, vp]
+        L.oracle_sdpa.restype = i32
+        L.oracle_sdpa_rows.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, i32, i32, i32,
+                                       i32, i32, i32, f64, i32]
+        L.oracle_sdpa_rows.restype = i32
+        L.oracle_decode_paged.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp,
+                                          i32, i32, i32, i32, i32, i32, i32, f64, vp, i32,
+                                          i32, vp]
+        L.oracle_decode_paged.restype = i32
+        L.oracle_kv_append.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, i32,
+                                       i32, i32, i32, i32, i32, i32]
+        L.oracle_kv_append.restype = i32
+        L.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_to_f64.restype = f64
+        L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16_to_f64.restype = f64
+        L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_f64.restype = f64
+        L.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------------ helpers
+
+def _as_np(x):
+    """Host array view of a CPU torch tensor or numpy array (no copy of data
+    values: torch half/bfloat16/float8 tensors are viewed as raw bits)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            assert x.device.type == "cpu", "oracle inputs live on the host"
+            x = x.contiguous()
+            if x.dtype in (torch.float16, torch.bfloat16):
+                return x.view(torch.int16).numpy().view(np.uint16)
+            if x.dtype == torch.float8_e4m3fn:
+                return x.view(torch.uint8).numpy()
+            return x.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(x)
+
+
+def dtype_code(x) -> int:
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
+                    torch.float8_e4m3fn: E4M3, torch.float64: F64}[x.dtype]
+    except ImportError:  # pragma: no cover
+        pass
+    return {np.dtype(np.float32): F32, np.dtype(np.float64): F64,
+            np.dtype(np.uint8): E4M3}[np.asarray(x).dtype]
+
+
+def _p(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+# ------------------------------------------------------------- public calls
+
+def sdpa(Q, K, V, causal: bool, scale: float | None = None, nthreads: int = 0,
+         return_counts: bool = False):
+    """Exact attention.  Q [B,Hq,nq,d], K/V [B,Hkv,nkv,d] (same element type).
+    Returns (O [B,Hq,nq,d] fp64, lse [B,Hq,nq] fp64[, (macs, exps)])."""
+    code = dtype_code(Q)
+    assert dtype_code(K) == code and dtype_code(V) == code
+    q, k, v = _as_np(Q), _as_np(K), _as_np(V)
+    B, Hq, nq, d = q.shape
+    _, Hkv, nkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    O = np.zeros((B, Hq, nq, d), np.float64)
+    lse = np.zeros((B, Hq, nq), np.float64)
+    counts = np.zeros(2, np.int64)
+    rc = lib().oracle_sdpa(_p(q), _p(k), _p(v), code, _p(O), _p(lse), B, Hq, Hkv, nq, nkv,
+                           d, int(causal), float(scale), nthreads, _p(counts))
+    if rc != 0:
+        raise ValueError("oracle_sdpa: invalid arguments")
+    if return_counts:
+        return O, lse, (int(counts[0]), int(counts[1]))
+    return O, lse
+
+
+def sdpa_rows(Q, K, V, rows, causal: bool, scale: float | None = None, nthreads: int = 0):
+    """Selected rows (b, h, i) of exact attention; returns (O [r,d], lse [r])."""
+    code = dtype_code(Q)
+    q, k, v = _as_np(Q), _as_np(K), _as_np(V)
+    B, Hq, nq, d = q.shape
+    _, Hkv, nkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows = np.ascontiguousarray(np.asarray(rows, np.int64).reshape(-1, 3))
+    O = np.zeros((rows.shape[0], d), np.float64)
+    lse = np.zeros(rows.shape[0], np.float64)
+    rc = lib().oracle_sdpa_rows(_p(q), _p(k), _p(v), code, _p(rows), rows.shape[0], _p(O),
+                                _p(lse), B, Hq, Hkv, nq, nkv, d, int(causal), float(scale),
+                                nthreads)
+    if rc != 0:
+        raise ValueError("oracle_sdpa_rows: invalid arguments")
+    return O, lse
+
+
+def decode_paged(q, Kc, Vc, block_table, seq_lens, scale: float | None = None,
+                 k_scale=None, v_scale=None, seq_subset=None, nthreads: int = 0,
+                 return_counts: bool = False):
+    """One-token attention over a block-paged cache [num_blocks,Hkv,bs,d].
+    Returns (O [S,Hq,d], lse [S,Hq]) in fp64 (rows outside seq_subset are 0)."""
+    qc, kc = dtype_code(q), dtype_code(Kc)
+    qn, Kn, Vn = _as_np(q), _as_np(Kc), _as_np(Vc)
+    bt = np.ascontiguousarray(_as_np(block_table).astype(np.int32))
+    sl = np.ascontiguousarray(_as_np(seq_lens).astype(np.int32))
+    S, Hq, d = qn.shape
+    num_blocks, Hkv, bs, _ = Kn.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    ks = None if k_scale is None else np.ascontiguousarray(_as_np(k_scale).astype(np.float32))
+    vs = None if v_scale is None else np.ascontiguousarray(_as_np(v_scale).astype(np.float32))
+    sub = None if seq_subset is None else np.ascontiguousarray(np.asarray(seq_subset, np.int32))
+    O = np.zeros((S, Hq, d), np.float64)
+    lse = np.zeros((S, Hq), np.float64)
+    counts = np.zeros(2, np.int64)
+    rc = lib().oracle_decode_paged(_p(qn), qc, _p(Kn), _p(Vn), kc, _p(ks), _p(vs), _p(bt),
+                                   _p(sl), _p(O), _p(lse), S, Hq, Hkv, d, bs, bt.shape[1],
+                                   num_blocks, float(scale), _p(sub),
+                                   0 if sub is None else len(sub), nthreads, _p(counts))
+    if rc != 0:
+        raise ValueError("oracle_decode_paged: invalid arguments")
+    if return_counts:
+        return O, lse, (int(counts[0]), int(counts[1]))
+    return O, lse
+
+
+def kv_append(k_new, v_new, Kc, Vc, block_table, seq_ids, positions, k_scale=None,
+              v_scale=None):
+    """Returns updated copies (numpy, raw bits) of the K and V caches."""
+    sc = dtype_code(k_new)
+    kc = dtype_code(Kc)
+    kn, vn = _as_np(k_new), _as_np(v_new)
+    Kout, Vout = _as_np(Kc).copy(), _as_np(Vc).copy()
+    bt = np.ascontiguousarray(_as_np(block_table).astype(np.int32))
+    sid = np.ascontiguousarray(_as_np(seq_ids).astype(np.int32))
+    pos = np.ascontiguousarray(_as_np(positions).astype(np.int32))
+    ks = None if k_scale is None else np.ascontiguousarray(_as_np(k_scale).astype(np.float32))
+    vs = None if v_scale is None else np.ascontiguousarray(_as_np(v_scale).astype(np.float32))
+    T, Hkv, d = kn.shape
+    num_blocks, _, bs, _ = Kout.shape
+    rc = lib().oracle_kv_append(_p(kn), _p(vn), sc, _p(Kout), _p(Vout), kc, _p(ks), _p(vs),
+                                _p(bt), _p(sid), _p(pos), T, Hkv, d, bs, bt.shape[1],
+                                bt.shape[0], num_blocks)
+    if rc != 0:
+        raise ValueError("oracle_kv_append: invalid arguments")
+    return Kout, Vout
+
+
+def e4m3_decode(code: int) -> float:
+    return float(lib().oracle_e4m3_to_f64(code))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(lib().oracle_f32_to_e4m3(x))
+
+
+def f16_decode(bits: int) -> float:
+    return float(lib().oracle_f16_to_f64(bits))
+
+
+def bf16_decode(bits: int) -> float:
+    return float(lib().oracle_bf16_to_f64(bits))
