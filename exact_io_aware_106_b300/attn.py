@@ -1,0 +1,167 @@
+"""ctypes binding of libattn.so (include/attn.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+checks that tensors live on the GPU, passes their device pointers, sizes and
+the current CUDA stream, and turns non-zero status codes into exceptions.
+There is no fallback: if the library or a GPU is missing, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+_DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.float8_e4m3fn: 3}
+
+EXPORTS = ("attn_prefill", "attn_decode_workspace_bytes", "attn_decode", "attn_kv_append",
+           "attn_last_error", "attn_status_str", "attn_last_launch_count")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_str(status)} ({status})")
+
+
+_lib = None
+
+
+def lib():
+    """Load libattn.so (raises OSError if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"{LIB_PATH} is missing: run `python -m exact_io_aware_106_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                   i32, i32, vp]
+        L.attn_prefill.restype = i32
+        L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.attn_decode_workspace_bytes.restype = sz
+        L.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                  i32, f32, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.attn_decode.restype = i32
+        L.attn_kv_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                     i32, i32, i32, vp, vp, vp]
+        L.attn_kv_append.restype = i32
+        L.attn_last_error.argtypes = [vp]
+        L.attn_last_error.restype = i32
+        L.attn_status_str.argtypes = [i32]
+        L.attn_status_str.restype = ctypes.c_char_p
+        L.attn_last_launch_count.argtypes = []
+        L.attn_last_launch_count.restype = i32
+        _lib = L
+    return _lib
+
+
+def status_str(s: int) -> str:
+    return lib().attn_status_str(s).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("tensor must live on a CUDA device")
+            if not t.is_contiguous():
+                raise ValueError("tensor must be contiguous")
+
+
+def _check(fn, st):
+    if st != OK:
+        raise AttnError(fn, st)
+
+
+def last_launch_count() -> int:
+    return lib().attn_last_launch_count()
+
+
+def last_error(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device error status."""
+    return lib().attn_last_error(_stream(stream))
+
+
+def prefill(Q, K, V, causal: bool, scale: float | None = None, out_dtype=None, O=None,
+            lse=None, want_lse: bool = True, stream=None):
+    """O = softmax(scale Q K^T [causal]) V for Q [B,Hq,n_q,d], K/V [B,Hkv,n_kv,d].
+    Returns (O, lse) with lse [B,Hq,n_q] fp32 (None if want_lse is False)."""
+    _cuda(Q, K, V)
+    B, Hq, nq, d = Q.shape
+    _, Hkv, nkv, _ = K.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out_dtype is None:
+        out_dtype = Q.dtype
+    if O is None:
+        O = torch.empty((B, Hq, nq, d), dtype=out_dtype, device=Q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, nq), dtype=torch.float32, device=Q.device)
+    _cuda(O, lse)
+    st = lib().attn_prefill(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), B, Hq, Hkv, nq, nkv,
+                            d, int(bool(causal)), float(scale), _DT[Q.dtype], _DT[O.dtype],
+                            _stream(stream))
+    _check("attn_prefill", st)
+    return O, lse
+
+
+def decode_workspace_bytes(num_seqs: int, Hq: int, d: int, max_seq_len: int) -> int:
+    return int(lib().attn_decode_workspace_bytes(num_seqs, Hq, d, max_seq_len))
+
+
+def decode(q, Kc, Vc, block_table, seq_lens, max_seq_len: int, scale: float | None = None,
+           k_scale=None, v_scale=None, out_dtype=None, O=None, lse=None, workspace=None,
+           want_lse: bool = True, stream=None):
+    """One query token per sequence against a paged cache [num_blocks,Hkv,bs,d].
+    Returns (O [S,Hq,d], lse [S,Hq])."""
+    _cuda(q, Kc, Vc, block_table, seq_lens, k_scale, v_scale)
+    S, Hq, d = q.shape
+    num_blocks, Hkv, bs, _ = Kc.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out_dtype is None:
+        out_dtype = q.dtype
+    if O is None:
+        O = torch.empty((S, Hq, d), dtype=out_dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((S, Hq), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(S, Hq, d, max_seq_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _cuda(O, lse, workspace)
+    st = lib().attn_decode(_ptr(q), _ptr(Kc), _ptr(Vc), _ptr(block_table), _ptr(seq_lens),
+                           _ptr(O), _ptr(lse), S, Hq, Hkv, d, bs, block_table.shape[1],
+                           num_blocks, int(max_seq_len), float(scale), _DT[q.dtype],
+                           _DT[Kc.dtype], _DT[O.dtype], _ptr(k_scale), _ptr(v_scale),
+                           _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("attn_decode", st)
+    return O, lse
+
+
+def kv_append(k_new, v_new, Kc, Vc, block_table, seq_ids, positions, k_scale=None,
+              v_scale=None, stream=None):
+    """Write k_new/v_new [T,Hkv,d] into the paged caches in place."""
+    _cuda(k_new, v_new, Kc, Vc, block_table, seq_ids, positions, k_scale, v_scale)
+    T, Hkv, d = k_new.shape
+    num_blocks, _, bs, _ = Kc.shape
+    st = lib().attn_kv_append(_ptr(k_new), _ptr(v_new), _ptr(Kc), _ptr(Vc), _ptr(block_table),
+                              _ptr(seq_ids), _ptr(positions), T, block_table.shape[0], Hkv, d,
+                              bs, block_table.shape[1], num_blocks, _DT[k_new.dtype],
+                              _DT[Kc.dtype], _ptr(k_scale), _ptr(v_scale), _stream(stream))
+    _check("attn_kv_append", st)

@@ -1,0 +1,204 @@
+// api.cu -- the extern "C" boundary of libattn.so (declared in attn.h):
+// host-side argument validation, the per-device error word, dispatch to the
+// prefill, decode and KV-append launchers.
+#include <math.h>
+#include <mutex>
+
+#include "attn.h"
+#include "common.cuh"
+#include "launch.h"
+
+
+// The device error word: bit DERR_TIMEOUT / DERR_INDEX, set by kernels with
+// atomicOr, read and cleared by attn_last_error().
+__device__ unsigned int g_attn_err_word;
+
+namespace {
+
+thread_local int t_last_launches = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_err_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the error word on the current device (looked up once
+// per device with that device current).
+unsigned *err_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_attn_err_word) != cudaSuccess)
+            return nullptr;
+        g_err_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool is16(attn_dtype t) { return t == ATTN_F16 || t == ATTN_BF16; }
+bool is_out(attn_dtype t) { return t == ATTN_F16 || t == ATTN_BF16 || t == ATTN_F32; }
+int out_code(attn_dtype t) { return t == ATTN_F16 ? 0 : (t == ATTN_BF16 ? 1 : 2); }
+
+} // namespace
+
+extern "C" {
+
+const char *attn_status_str(attn_status s) {
+    switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID: return "ATTN_ERR_INVALID";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    }
+    return "ATTN_UNKNOWN_STATUS";
+}
+
+int attn_last_launch_count(void) { return t_last_launches; }
+
+attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                         int Hq, int Hkv, int n_q, int n_kv, int d, int causal, float scale,
+                         attn_dtype in_dtype, attn_dtype out_dtype, void *stream) {
+    t_last_launches = 0;
+    if (!Q || !K || !V || !O)
+        return ATTN_ERR_INVALID;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || n_q <= 0 || n_kv <= 0 || d <= 0 || Hq % Hkv != 0)
+        return ATTN_ERR_INVALID;
+    if (causal && n_q > n_kv)
+        return ATTN_ERR_INVALID;
+    if (!isfinite(scale))
+        return ATTN_ERR_INVALID;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+        (lse && !aligned(lse, 4)))
+        return ATTN_ERR_INVALID;
+    if (!is16(in_dtype) || !is_out(out_dtype) || (d != 64 && d != 128))
+        return ATTN_ERR_UNSUPPORTED;
+    const long long nqb = (n_q + 255) / 256;
+    if (nqb * B * Hq > 0x7fffffffLL)
+        return ATTN_ERR_UNSUPPORTED;
+    unsigned *err = err_word();
+    if (!err)
+        return ATTN_ERR_CUDA;
+    attn::PrefillArgs a{Q, K, V, O, lse, B, Hq, Hkv, n_q, n_kv, d, causal ? 1 : 0, scale,
+                        in_dtype == ATTN_BF16, out_code(out_dtype), err};
+    if (attn::prefill_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = 1;
+    return ATTN_OK;
+}
+
+size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int max_seq_len) {
+    if (num_seqs <= 0 || Hq <= 0 || d <= 0 || max_seq_len < 0)
+        return 0;
+    return attn::decode_workspace_bytes(num_seqs, Hq, d, max_seq_len);
+}
+
+attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache,
+                        const int32_t *block_table, const int32_t *seq_lens, void *O, float *lse,
+                        int num_seqs, int Hq, int Hkv, int d, int block_size,
+                        int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
+                        attn_dtype q_dtype, attn_dtype kv_dtype, attn_dtype out_dtype,
+                        const float *k_scale, const float *v_scale, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    t_last_launches = 0;
+    if (!q || !Kcache || !Vcache || !block_table || !seq_lens || !O || !workspace)
+        return ATTN_ERR_INVALID;
+    if (num_seqs <= 0 || num_seqs > 65535 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 ||
+        block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_seq_len < 0)
+        return ATTN_ERR_INVALID;
+    if (static_cast<long long>(max_seq_len) >
+        static_cast<long long>(max_blocks_per_seq) * block_size)
+        return ATTN_ERR_INVALID;
+    if (!isfinite(scale))
+        return ATTN_ERR_INVALID;
+    if (!is16(q_dtype) || !is_out(out_dtype))
+        return ATTN_ERR_UNSUPPORTED;
+    const bool e4 = kv_dtype == ATTN_E4M3;
+    if (!(kv_dtype == q_dtype || (e4 && q_dtype == ATTN_BF16)))
+        return ATTN_ERR_UNSUPPORTED;
+    if (e4 && (!k_scale || !v_scale))
+        return ATTN_ERR_INVALID;
+    if ((d != 64 && d != 128 && d != 256) ||
+        (block_size != 16 && block_size != 32 && block_size != 64) || Hq / Hkv > 16)
+        return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(q, 2) || !aligned(O, 4) ||
+        !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return ATTN_ERR_INVALID;
+    if (workspace_bytes < attn::decode_workspace_bytes(num_seqs, Hq, d, max_seq_len))
+        return ATTN_ERR_INVALID;
+    unsigned *err = err_word();
+    if (!err)
+        return ATTN_ERR_CUDA;
+    attn::DecodeArgs a{q, Kcache, Vcache, block_table, seq_lens, O, lse, num_seqs, Hq, Hkv, d,
+                       block_size, max_blocks_per_seq, num_blocks, max_seq_len, scale,
+                       q_dtype == ATTN_BF16, e4, out_code(out_dtype), k_scale, v_scale,
+                       workspace, err};
+    if (attn::decode_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = 2;
+    return ATTN_OK;
+}
+
+attn_status attn_kv_append(const void *k_new, const void *v_new, void *Kcache, void *Vcache,
+                           const int32_t *block_table, const int32_t *seq_ids,
+                           const int32_t *positions, int T, int num_seqs, int Hkv, int d,
+                           int block_size, int max_blocks_per_seq, int num_blocks,
+                           attn_dtype src_dtype, attn_dtype kv_dtype, const float *k_scale,
+                           const float *v_scale, void *stream) {
+    t_last_launches = 0;
+    if (T < 0 || num_seqs <= 0 || Hkv <= 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
+        num_blocks <= 0)
+        return ATTN_ERR_INVALID;
+    if (T == 0)
+        return ATTN_OK;
+    if (!k_new || !v_new || !Kcache || !Vcache || !block_table || !seq_ids || !positions)
+        return ATTN_ERR_INVALID;
+    if (!is16(src_dtype))
+        return ATTN_ERR_UNSUPPORTED;
+    const bool e4 = kv_dtype == ATTN_E4M3;
+    if (!(kv_dtype == src_dtype || e4))
+        return ATTN_ERR_UNSUPPORTED;
+    if (e4 && (!k_scale || !v_scale))
+        return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128 && d != 256)
+        return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(Kcache, 16) ||
+        !aligned(Vcache, 16))
+        return ATTN_ERR_INVALID;
+    if (static_cast<long long>(T) * Hkv > 0x7fffffffLL)
+        return ATTN_ERR_UNSUPPORTED;
+    unsigned *err = err_word();
+    if (!err)
+        return ATTN_ERR_CUDA;
+    attn::AppendArgs a{k_new, v_new, Kcache, Vcache, block_table, seq_ids, positions, T,
+                       num_seqs, Hkv, d, block_size, max_blocks_per_seq, num_blocks,
+                       src_dtype == ATTN_BF16, e4, k_scale, v_scale, err};
+    if (attn::kv_append_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = 1;
+    return ATTN_OK;
+}
+
+attn_status attn_last_error(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    unsigned w = 0;
+    if (cudaMemcpyFromSymbol(&w, g_attn_err_word, sizeof w) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (w != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_attn_err_word, &zero, sizeof zero) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    if (w & attn::DERR_TIMEOUT)
+        return ATTN_ERR_TIMEOUT;
+    if (w & attn::DERR_INDEX)
+        return ATTN_ERR_INVALID;
+    return ATTN_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,64 @@
+// launch.h -- host-side launcher interfaces shared by api.cu and the kernel
+// translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace attn {
+
+struct PrefillArgs {
+    const void *Q;
+    const void *K;
+    const void *V;
+    void *O;
+    float *lse;
+    int B, Hq, Hkv, n_q, n_kv, d, causal;
+    float scale;
+    bool bf16;
+    int out_dtype; // 0 f16, 1 bf16, 2 f32
+    unsigned *err;
+};
+
+struct DecodeArgs {
+    const void *q;
+    const void *Kc;
+    const void *Vc;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    void *O;
+    float *lse;
+    int num_seqs, Hq, Hkv, d, block_size, max_blocks, num_blocks, max_seq_len;
+    float scale;
+    bool q_bf16, kv_e4m3;
+    int out_dtype; // 0 f16, 1 bf16, 2 f32
+    const float *k_scale;
+    const float *v_scale;
+    void *workspace;
+    unsigned *err;
+};
+
+struct AppendArgs {
+    const void *k_new;
+    const void *v_new;
+    void *Kc;
+    void *Vc;
+    const int32_t *block_table;
+    const int32_t *seq_ids;
+    const int32_t *positions;
+    int T, num_seqs, Hkv, d, block_size, max_blocks, num_blocks;
+    bool bf16, to_e4m3;
+    const float *k_scale;
+    const float *v_scale;
+    unsigned *err;
+};
+
+cudaError_t prefill_launch(const PrefillArgs &a, cudaStream_t st);
+cudaError_t decode_launch(const DecodeArgs &a, cudaStream_t st);
+cudaError_t kv_append_launch(const AppendArgs &a, cudaStream_t st);
+size_t decode_workspace_bytes(int num_seqs, int Hq, int d, int max_seq_len);
+int decode_tokens_per_split(int max_seq_len);
+int decode_max_splits(int max_seq_len);
+
+} // namespace attn

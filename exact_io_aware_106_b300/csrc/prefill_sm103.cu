@@ -1,0 +1,556 @@
+// prefill_sm103.cu -- exact attention forward on sm_103a tensor cores.
+//
+// The method (auturnal.com "From attention to IO-aware execution" §8;
+// marketmaker.cc "Flash Attention and sequence length", "The Flash Attention
+// algorithm" and "The online softmax recurrence"): Q is cut into row blocks
+// and K, V into column blocks; for every (row block, column block) the score
+// tile S = Q K^T is formed on chip, the running row max m, denominator l and
+// un-normalised output u are rescaled by exp(m - m') when the block raises
+// the max, u += P V, and u / l is written once at the end.  The full score
+// matrix never leaves the SM.  Normalisation is deferred to the end of the
+// loop (the FA2 scheduling on the same page), causal tiles entirely in the
+// future are skipped (page 5, causal masking), and query head h reads KV
+// head h / G (code-journey.com "Attention co-design", Group Size).
+//
+// B300 mapping (one CTA = 2 query tiles of 128 rows = 256 rows of one head):
+//   warp 8      TMA producer: Q tiles once, then K_j / V_j through rings of
+//               shared-memory stages (128-byte swizzle, one 3-D tensor map
+//               per operand so tails read zeros).
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory
+//               (tcgen05.mma, A and B from shared memory), then
+//               O_t += P_t V_j with P_t read from tensor memory.
+//   warps 0-7   softmax, one warpgroup per query tile, one thread per row:
+//               tcgen05.ld the 128 scores of its row, row max, p = 2^(s*c-m)
+//               on the SFU, row sum, P packed to 16-bit back into tensor
+//               memory over the consumed scores, O rescaled in tensor memory
+//               when the reference max moves, final O / l and lse.
+// The two tiles ping-pong: while warpgroup 0 turns S_0 into P_0, the tensor
+// core computes O_1 += P_1 V_j and S_1 for the next block, and vice versa.
+//
+// Tensor memory (512 columns x 128 lanes): S_0 [0,128), S_1 [128,256),
+// O_0 [256, 256+D), O_1 [256+D, 256+2D).  P_t (16-bit, two per column)
+// overwrites the first 64 columns of S_t; for rows with few visible keys
+// the rounding residual P - P_hi is stored in the next 64 columns and
+// multiplied in as a second MMA, so that the 16-bit rounding of P does not
+// reach the output where too few terms average it out.
+//
+// Scores are in the log2 domain (c = scale * log2 e).  The reference max
+// m is only moved when a block's max exceeds it by more than 8, so p stays
+// <= 2^8.  u / l does not depend on which reference value is subtracted
+// (the max-subtraction invariance of §8); keeping a slightly stale one
+// avoids most O rescales.
+#include "common.cuh"
+#include "launch.h"
+
+namespace attn {
+
+namespace pf {
+
+constexpr int BM = 128;      // query rows per tile
+constexpr int NT = 2;        // query tiles per CTA
+constexpr int BN = 128;      // keys per block
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kSplitKeys = 512; // rows seeing fewer keys carry the P residual
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct Cfg {
+    static constexpr int PANELS = D / 64;                // 128-byte column panels
+    static constexpr int Q_TILE_BYTES = BM * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int NK = D == 64 ? 3 : 2;           // K stages
+    static constexpr int NV = D == 64 ? 3 : 2;           // V stages
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + NT * Q_TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
+    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 * NT + 2;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 64 + 1024; // + alignment slack
+    __host__ __device__ static constexpr int S_COL(int t) { return t * BN; }
+    __host__ __device__ static constexpr int O_COL(int t) { return NT * BN + t * D; }
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(NT * BN + NT * D <= 512, "tensor memory budget");
+};
+
+struct Shape {
+    int B, Hq, Hkv, G, n_q, n_kv, causal, nqb;
+    float c;     // scale * log2(e)
+    float scale; // for reference only
+};
+
+__device__ __forceinline__ int tile_blocks(const Shape &sh, int q0, int t) {
+    const int r0 = q0 + t * BM;
+    if (r0 >= sh.n_q)
+        return 0;
+    const int nkb = (sh.n_kv + BN - 1) / BN;
+    if (!sh.causal)
+        return nkb;
+    const int r_last = min(r0 + BM - 1, sh.n_q - 1);
+    const int k_last = r_last + (sh.n_kv - sh.n_q);
+    return min(nkb, k_last / BN + 1);
+}
+
+__device__ __forceinline__ bool tile_split(const Shape &sh, int q0, int t) {
+    const int r0 = q0 + t * BM;
+    const int keys = sh.causal ? (r0 + (sh.n_kv - sh.n_q) + 1) : sh.n_kv;
+    return keys < kSplitKeys;
+}
+
+template <int D, bool BF16, int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, void *__restrict__ O,
+                   float *__restrict__ lse, const Shape sh, unsigned *err) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned base (128-byte swizzle atoms repeat every 1 KB)
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+
+    const uint32_t sQ = base_s + C::OFF_Q;
+    const uint32_t sK = base_s + C::OFF_K;
+    const uint32_t sV = base_s + C::OFF_V;
+    const uint32_t bar0 = base_s + C::OFF_BAR;
+    const uint32_t b_qfull = bar0;
+    auto b_kfull = [&](int i) { return bar0 + 8u * (1 + i); };
+    auto b_kempty = [&](int i) { return bar0 + 8u * (1 + C::NK + i); };
+    auto b_vfull = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + i); };
+    auto b_vempty = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + C::NV + i); };
+    auto b_sfull = [&](int t) { return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + t); };
+    auto b_pfull = [&](int t) { return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + NT + t); };
+    const uint32_t b_ofull = bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + 2 * NT);
+    const uint32_t b_drain = b_ofull + 8u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- work item: heaviest query blocks first (causal work grows with q)
+    const int BH = sh.B * sh.Hq;
+    const int qb = sh.nqb - 1 - static_cast<int>(blockIdx.x) / BH;
+    const int bh = static_cast<int>(blockIdx.x) % BH;
+    const int b = bh / sh.Hq, h = bh % sh.Hq;
+    const int bkv = b * sh.Hkv + h / sh.G;
+    const int q0 = qb * (NT * BM);
+    int nb[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+        nb[t] = tile_blocks(sh, q0, t);
+    const int nb_max = max(nb[0], nb[1]);
+
+    // ---- set-up: barriers, tensor memory
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(b_qfull, 1);
+        for (int i = 0; i < C::NK; ++i) {
+            mbar_init(b_kfull(i), 1);
+            mbar_init(b_kempty(i), 1);
+        }
+        for (int i = 0; i < C::NV; ++i) {
+            mbar_init(b_vfull(i), 1);
+            mbar_init(b_vempty(i), 1);
+        }
+        for (int t = 0; t < NT; ++t) {
+            mbar_init(b_sfull(t), 1);
+            mbar_init(b_pfull(t), 4);
+        }
+        mbar_init(b_ofull, 1);
+        mbar_init(b_drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ================================================= TMA producer
+        if (lane == 0) {
+            int ntiles = 0;
+            for (int t = 0; t < NT; ++t)
+                ntiles += nb[t] > 0;
+            mbar_arrive_expect_tx(b_qfull, ntiles * C::Q_TILE_BYTES);
+            for (int t = 0; t < NT; ++t)
+                if (nb[t] > 0)
+                    for (int p = 0; p < C::PANELS; ++p)
+                        tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * 128, &tm_q, b_qfull,
+                                    p * 64, q0 + t * BM, bh);
+            int k_issued = 0, v_issued = 0;
+            for (int j = 0; j < nb_max; ++j) {
+                const int ks = j % C::NK;
+                if (j >= C::NK &&
+                    !mbar_wait(b_kempty(ks), ((j / C::NK) - 1) & 1, abort_flag, err))
+                    break;
+                mbar_arrive_expect_tx(b_kfull(ks), C::KV_BYTES);
+                for (int p = 0; p < C::PANELS; ++p)
+                    tma_load_3d(sK + ks * C::KV_BYTES + p * BN * 128, &tm_k, b_kfull(ks), p * 64,
+                                j * BN, bkv);
+                k_issued = j + 1;
+                const int vs = j % C::NV;
+                if (j >= C::NV &&
+                    !mbar_wait(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
+                    break;
+                mbar_arrive_expect_tx(b_vfull(vs), C::KV_BYTES);
+                for (int p = 0; p < C::PANELS; ++p)
+                    tma_load_3d(sV + vs * C::KV_BYTES + p * BN * 128, &tm_v, b_vfull(vs), p * 64,
+                                j * BN, bkv);
+                v_issued = j + 1;
+            }
+            if (*abort_flag) { // let in-flight copies land before the CTA exits
+                mbar_wait_drain(b_qfull, 0);
+                for (int u = max(0, k_issued - C::NK); u < k_issued; ++u)
+                    mbar_wait_drain(b_kfull(u % C::NK), (u / C::NK) & 1);
+                for (int u = max(0, v_issued - C::NV); u < v_issued; ++u)
+                    mbar_wait_drain(b_vfull(u % C::NV), (u / C::NV) & 1);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_f16(BM, BN, BF16, false, false);
+            constexpr uint32_t idesc_pv = idesc_f16(BM, D, BF16, false, true);
+            bool split[NT];
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                split[t] = tile_split(sh, q0, t);
+
+            auto issue_qk = [&](int t, int ks) {
+                const uint32_t qa = sQ + t * C::Q_TILE_BYTES;
+                const uint32_t kb = sK + ks * C::KV_BYTES;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k / 4) * (BM * 128) + (k % 4) * 32;
+                    const uint32_t offb = (k / 4) * (BN * 128) + (k % 4) * 32;
+                    mma_ss(tmem + C::S_COL(t), sdesc_sw128(qa + off, 16, 1024),
+                           sdesc_sw128(kb + offb, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int vs, bool first) {
+                const uint32_t vb = sV + vs * C::KV_BYTES;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+                    mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, bd, idesc_pv,
+                           (first && k == 0) ? 0u : 1u);
+                }
+                if (split[t]) {
+#pragma unroll
+                    for (int k = 0; k < BN / 16; ++k) {
+                        const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+                        mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + 64 + k * 8, bd, idesc_pv,
+                               1u);
+                    }
+                }
+            };
+
+            bool ok = mbar_wait(b_qfull, 0, abort_flag, err);
+            if (ok && nb_max > 0) {
+                ok = mbar_wait(b_kfull(0), 0, abort_flag, err);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < NT; ++t)
+                        if (nb[t] > 0) {
+                            issue_qk(t, 0);
+                            tc_commit(b_sfull(t));
+                        }
+                    tc_commit(b_kempty(0));
+                }
+            }
+            for (int j = 0; ok && j < nb_max; ++j) {
+                const int vs = j % C::NV;
+                const int kn = j + 1, ks = kn % C::NK;
+                const bool need_k = kn < nb_max;
+                if (!mbar_wait(b_vfull(vs), (j / C::NV) & 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                if (need_k && !mbar_wait(b_kfull(ks), (kn / C::NK) & 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (j < nb[0]) {
+                    if (!mbar_wait(b_pfull(0), j & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(0, vs, j == 0);
+                    if (kn < nb[0]) {
+                        issue_qk(0, ks);
+                        tc_commit(b_sfull(0));
+                    }
+                }
+                if (j < nb[1]) {
+                    if (!mbar_wait(b_pfull(1), j & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(1, vs, j == 0);
+                }
+                tc_commit(b_vempty(vs));
+                if (j < nb[1] && kn < nb[1]) {
+                    issue_qk(1, ks);
+                    tc_commit(b_sfull(1));
+                }
+                if (need_k)
+                    tc_commit(b_kempty(ks));
+            }
+            if (ok)
+                tc_commit(b_ofull);
+            // every MMA this thread issued must finish before tensor memory
+            // is released
+            tc_commit(b_drain);
+            mbar_wait_drain(b_drain, 0);
+        }
+    } else {
+        // ================================================= softmax warps
+        const int t = warp >> 2;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int row_g = q0 + t * BM + r;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::S_COL(t);
+        const uint32_t tO = tmem + lane_off + C::O_COL(t);
+        const int off = sh.n_kv - sh.n_q;
+        const bool split = tile_split(sh, q0, t);
+        const int r0 = q0 + t * BM;
+        const float c = sh.c;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+
+        for (int j = 0; j < nb[t]; ++j) {
+            if (!mbar_wait(b_sfull(t), j & 1, abort_flag, err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[BN];
+#pragma unroll
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t u[32];
+                tmem_ld32(tS + ch * 32, u);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    s[ch * 32 + i] = __uint_as_float(u[i]);
+            }
+            const int kbase = j * BN;
+            const bool need_mask =
+                (sh.causal && kbase + BN - 1 > r0 + off) || (kbase + BN > sh.n_kv);
+            if (need_mask) {
+                int lim = sh.causal ? row_g + off : sh.n_kv - 1;
+                lim = min(lim, sh.n_kv - 1) - kbase;
+#pragma unroll
+                for (int k = 0; k < BN; ++k)
+                    if (k > lim)
+                        s[k] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int k = 1; k < BN; ++k)
+                mx = fmaxf(mx, s[k]);
+            const float m_blk = mx * c;
+            float m_use = m;
+            if (m_blk > m + kRescaleThreshold || m == -INFINITY)
+                m_use = fmaxf(m_blk, m);
+            const float alpha =
+                (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
+            const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
+            float sum = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2(fmaf(s[ch * 32 + 2 * i], c, neg));
+                    const float p1 = ex2(fmaf(s[ch * 32 + 2 * i + 1], c, neg));
+                    sum += p0 + p1;
+                    hi[i] = pack2<BF16>(p0, p1);
+                    if (split)
+                        lo[i] = pack2<BF16>(p0 - lo16<BF16>(hi[i]), p1 - hi16<BF16>(hi[i]));
+                }
+                tmem_st16(tS + ch * 16, hi);
+                if (split)
+                    tmem_st16(tS + 64 + ch * 16, lo);
+            }
+            // O_t holds the sum over earlier blocks (their MMAs completed
+            // before S_t of this block was produced); rescale it in place.
+            if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t u[32];
+                    tmem_ld32(tO + ch * 32, u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                    tmem_st32(tO + ch * 32, u);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b_pfull(t));
+            l = l * alpha + sum;
+            m = m_use;
+        }
+        if (ok && nb[t] > 0)
+            ok = mbar_wait(b_ofull, 0, abort_flag, err);
+        tc_fence_after();
+        if (nb[t] > 0) {
+            // ---- epilogue: O = u / l, lse = ln(sum exp(scale * s))
+            const bool row_ok = row_g < sh.n_q;
+            const float inv = (ok && l > 0.f) ? 1.0f / l : 0.f;
+            const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row_g) * D;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t u[32];
+                tmem_ld32(tO + ch * 32, u);
+                if (row_ok) {
+                    float o[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = ok ? __uint_as_float(u[i]) * inv : 0.f;
+                    if constexpr (OUT == 2) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(O) + orow +
+                                                                 ch * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2],
+                                                 o[4 * i + 3]);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(O) + orow +
+                                                               ch * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack2<OUT == 1>(o[8 * i], o[8 * i + 1]),
+                                                pack2<OUT == 1>(o[8 * i + 2], o[8 * i + 3]),
+                                                pack2<OUT == 1>(o[8 * i + 4], o[8 * i + 5]),
+                                                pack2<OUT == 1>(o[8 * i + 6], o[8 * i + 7]));
+                    }
+                }
+            }
+            if (lse != nullptr && row_ok)
+                lse[static_cast<size_t>(bh) * sh.n_q + row_g] =
+                    ok ? (m + __log2f(l)) * 0.69314718055994530942f
+                       : __int_as_float(0x7fc00000);
+        }
+    }
+
+    // ---- teardown: every tensor-memory access is done before release
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+} // namespace pf
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// [d, n, bh] bf16/f16 tensor, box {64, 128, 1}, 128-byte swizzle, zero fill.
+static bool make_map(CUtensorMap *m, const void *ptr, int d, int n, int bh, bool bf16) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+                          static_cast<cuuint64_t>(bh)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(n)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     3, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool BF16, int OUT>
+static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
+    using C = pf::Cfg<D>;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.Q, D, a.n_q, a.B * a.Hq, BF16) ||
+        !make_map(&mk, a.K, D, a.n_kv, a.B * a.Hkv, BF16) ||
+        !make_map(&mv, a.V, D, a.n_kv, a.B * a.Hkv, BF16))
+        return cudaErrorInvalidValue;
+    pf::Shape sh;
+    sh.B = a.B;
+    sh.Hq = a.Hq;
+    sh.Hkv = a.Hkv;
+    sh.G = a.Hq / a.Hkv;
+    sh.n_q = a.n_q;
+    sh.n_kv = a.n_kv;
+    sh.causal = a.causal;
+    sh.nqb = (a.n_q + pf::NT * pf::BM - 1) / (pf::NT * pf::BM);
+    sh.c = a.scale * 1.4426950408889634f;
+    sh.scale = a.scale;
+    auto kern = pf::prefill_kernel<D, BF16, OUT>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    const long long grid = static_cast<long long>(sh.nqb) * a.B * a.Hq;
+    if (grid > 0x7fffffffLL)
+        return cudaErrorInvalidValue;
+    kern<<<static_cast<unsigned>(grid), pf::kThreads, C::SMEM, st>>>(mq, mk, mv, a.O, a.lse, sh,
+                                                                     a.err);
+    return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+static cudaError_t launch_prefill_out(const PrefillArgs &a, cudaStream_t st) {
+    switch (a.out_dtype) {
+    case 0: return launch_prefill_t<D, BF16, 0>(a, st);
+    case 1: return launch_prefill_t<D, BF16, 1>(a, st);
+    default: return launch_prefill_t<D, BF16, 2>(a, st);
+    }
+}
+
+cudaError_t prefill_launch(const PrefillArgs &a, cudaStream_t st) {
+    if (a.d == 64)
+        return a.bf16 ? launch_prefill_out<64, true>(a, st) : launch_prefill_out<64, false>(a, st);
+    if (a.d == 128)
+        return a.bf16 ? launch_prefill_out<128, true>(a, st)
+                      : launch_prefill_out<128, false>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+} // namespace attn

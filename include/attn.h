@@ -1,0 +1,155 @@
+/*
+ * attn.h -- C ABI of libattn.so: exact IO-aware attention on B300 (sm_103a).
+ *
+ * What is computed (all entry points): scaled dot-product attention
+ *     O = softmax(scale * Q K^T [masked]) V
+ * (auturnal.com, "From attention to IO-aware execution", §2; papanda925.com,
+ * "Transformer complexity strategies", standard-attention pseudocode),
+ * evaluated tile by tile with the online-softmax statistics of §8 of the
+ * first page: a running max m, denominator l and un-normalised sum u per
+ * query row, rescaled by exp(m - m') whenever a block raises the max, u / l
+ * emitted at the end.  The n_q x n_kv score matrix never reaches device
+ * memory.
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *    caller owns every buffer.  The library keeps no allocation of its own
+ *    beyond one 4-byte device error word per device.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous on that stream; results are valid once
+ *    the stream has reached the call.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns ATTN_ERR_INVALID (or ATTN_ERR_UNSUPPORTED for a valid
+ *    but unimplemented combination) and launches nothing.  A launch failure
+ *    returns ATTN_ERR_CUDA.
+ *  - Errors that only the device can see (a block-table entry out of range,
+ *    a sequence longer than the table, a bounded wait that expired) are
+ *    recorded in the device error word and the affected output is written
+ *    as zeros; attn_last_error() reports and clears them.
+ *  - Tensors are contiguous, innermost dimension last, 16-byte aligned.
+ *  - GQA: query head h reads KV head h / (Hq / Hkv)
+ *    (code-journey.com, "Attention co-design", Group Size: G query heads
+ *    share one KV head; G = 1 is MHA).
+ *  - Causal masks are aligned bottom-right: query i sees key j iff
+ *    j <= i + (n_kv - n_q) (marketmaker.cc, "Flash Attention and sequence
+ *    length", causal masking; the pages do not fix the alignment for
+ *    n_q != n_kv, this reading makes a decode query see the whole cache).
+ *  - lse, when requested, is the natural log-sum-exp of the row's scaled
+ *    scores, ln sum_j exp(scale * q.k_j), in fp32.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = 1,     /* bad argument (host check) or bad index (device) */
+    ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head size) */
+    ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    ATTN_ERR_TIMEOUT = 4      /* a bounded device-side wait expired */
+} attn_status;
+
+typedef enum {
+    ATTN_F16 = 0,
+    ATTN_BF16 = 1,
+    ATTN_F32 = 2,
+    ATTN_E4M3 = 3 /* OCP FP8 E4M3 ("fn"), one fp32 scale per KV head */
+} attn_dtype;
+
+/* Prefill / full attention.
+ *   Q   [B, Hq,  n_q,  d]   in_dtype (F16 or BF16)
+ *   K,V [B, Hkv, n_kv, d]   in_dtype
+ *   O   [B, Hq,  n_q,  d]   out_dtype (F16, BF16 or F32)
+ *   lse [B, Hq,  n_q]       fp32, or NULL
+ * d in {64, 128}; Hq % Hkv == 0; causal requires n_q <= n_kv.
+ * scale is the factor applied to q.k (1/sqrt(d) for the textbook form).
+ * Host-side errors: ATTN_ERR_INVALID for null pointers, non-positive sizes,
+ * misalignment, Hq % Hkv != 0, causal with n_q > n_kv; ATTN_ERR_UNSUPPORTED
+ * for other d or dtype combinations.  One kernel launch. */
+ATTN_API attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O,
+                         float *lse, int B, int Hq, int Hkv, int n_q, int n_kv,
+                         int d, int causal, float scale, attn_dtype in_dtype,
+                         attn_dtype out_dtype, void *stream);
+
+/* Bytes of caller-provided device workspace attn_decode needs for these
+ * sizes (split-KV partial states).  max_seq_len bounds every seq_lens[s]. */
+ATTN_API size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d,
+                                   int max_seq_len);
+
+/* Single-token decode over a block-paged KV cache
+ * (papanda925.com, block-wise KV cache; code-journey.com, prefill vs
+ * decode: one query token against the whole cache).
+ *   q        [num_seqs, Hq, d]                        q_dtype (F16 / BF16)
+ *   Kcache,
+ *   Vcache   [num_blocks, Hkv, block_size, d]          kv_dtype: same as
+ *            q_dtype, or E4M3 with k_scale/v_scale [Hkv] fp32 (dequantised
+ *            value = code * scale)
+ *   block_table [num_seqs, max_blocks_per_seq] int32: token t of sequence s
+ *            is slot t % block_size of block block_table[s][t / block_size]
+ *   seq_lens [num_seqs] int32, each in [0, max_seq_len]
+ *   O        [num_seqs, Hq, d] out_dtype;  lse [num_seqs, Hq] fp32 or NULL
+ *   workspace: >= attn_decode_workspace_bytes(...) bytes, 256-byte aligned;
+ *            its contents on entry do not matter and are overwritten.
+ * block_size in {16, 32, 64}; d in {64, 128, 256}; Hq / Hkv <= 16.
+ * A sequence of length 0 yields O = 0 and lse = -inf.  Two kernel launches
+ * (split kernel, then combine).  The workspace must not be shared by
+ * overlapping calls. */
+ATTN_API attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache,
+                        const int32_t *block_table, const int32_t *seq_lens,
+                        void *O, float *lse, int num_seqs, int Hq, int Hkv,
+                        int d, int block_size, int max_blocks_per_seq,
+                        int num_blocks, int max_seq_len, float scale,
+                        attn_dtype q_dtype, attn_dtype kv_dtype,
+                        attn_dtype out_dtype, const float *k_scale,
+                        const float *v_scale, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* KV-cache append (papanda925.com, KV-cache management concept: the K/V of
+ * each new token is added to the cache).
+ *   k_new, v_new [T, Hkv, d] src_dtype (F16 / BF16)
+ *   token r goes to sequence seq_ids[r], position positions[r]: block
+ *   block_table[seq][pos / block_size], slot pos % block_size.
+ * kv_dtype == src_dtype copies the bits; kv_dtype == E4M3 stores
+ * e4m3_rn_satfinite(x / scale[h]) with the division in fp32.
+ * seq_lens are NOT updated: the caller owns them.  Out-of-range ids,
+ * positions or block entries are skipped and recorded in the device error
+ * word.  One kernel launch (none when T == 0). */
+ATTN_API attn_status attn_kv_append(const void *k_new, const void *v_new, void *Kcache,
+                           void *Vcache, const int32_t *block_table,
+                           const int32_t *seq_ids, const int32_t *positions,
+                           int T, int num_seqs, int Hkv, int d, int block_size,
+                           int max_blocks_per_seq, int num_blocks,
+                           attn_dtype src_dtype, attn_dtype kv_dtype,
+                           const float *k_scale, const float *v_scale,
+                           void *stream);
+
+/* Synchronises `stream`, then returns and clears the current device's error
+ * word: ATTN_ERR_TIMEOUT if a bounded wait expired, ATTN_ERR_INVALID if a
+ * device-side index check failed, ATTN_ERR_CUDA if the stream reports a
+ * CUDA error, else ATTN_OK. */
+ATTN_API attn_status attn_last_error(void *stream);
+
+/* Static string naming a status code (never NULL). */
+ATTN_API const char *attn_status_str(attn_status s);
+
+/* Number of kernel launches the most recent successful call of each entry
+ * point made on this host thread (0 after a host-side error). */
+ATTN_API int attn_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -1,0 +1,110 @@
+"""The C-ABI library loads, exports every symbol include/attn.h declares, and
+rejects bad arguments on the host before launching anything (no GPU needed:
+these paths return before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_io_aware_106_b300 import attn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from exact_io_aware_106_b300 import build
+    build.build()
+    return attn.lib()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("attn_prefill", "attn_decode", "attn_kv_append", "attn_decode_workspace_bytes",
+              "attn_last_error", "attn_status_str"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    for s in declared_symbols():
+        assert hasattr(L, s), s
+        assert s in attn.EXPORTS
+
+
+def test_status_strings(L):
+    assert attn.status_str(0) == "ATTN_OK"
+    assert attn.status_str(4) == "ATTN_ERR_TIMEOUT"
+    assert attn.status_str(99) == "ATTN_UNKNOWN_STATUS"
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced by the host checks
+
+
+def _prefill(L, **kw):
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, lse=None, B=1, Hq=4, Hkv=2, nq=128, nkv=128, d=128,
+             causal=1, scale=0.1, ind=1, outd=1)
+    a.update(kw)
+    return L.attn_prefill(a["Q"], a["K"], a["V"], a["O"], a["lse"], a["B"], a["Hq"], a["Hkv"],
+                          a["nq"], a["nkv"], a["d"], a["causal"], a["scale"], a["ind"], a["outd"],
+                          None)
+
+
+def test_prefill_host_validation(L):
+    assert _prefill(L, Q=None) == attn.ERR_INVALID
+    assert _prefill(L, Hq=3, Hkv=2) == attn.ERR_INVALID
+    assert _prefill(L, nq=0) == attn.ERR_INVALID
+    assert _prefill(L, nq=200, nkv=100) == attn.ERR_INVALID           # causal, n_q > n_kv
+    assert _prefill(L, Q=ctypes.c_void_p((1 << 20) + 8)) == attn.ERR_INVALID  # alignment
+    assert _prefill(L, scale=float("nan")) == attn.ERR_INVALID
+    assert _prefill(L, d=96) == attn.ERR_UNSUPPORTED
+    assert _prefill(L, ind=2) == attn.ERR_UNSUPPORTED                 # fp32 inputs
+    assert _prefill(L, outd=3) == attn.ERR_UNSUPPORTED
+    assert L.attn_last_launch_count() == 0
+
+
+def _decode(L, **kw):
+    a = dict(S=4, Hq=8, Hkv=2, d=128, bs=16, mb=8, nb=32, msl=128, scale=0.1, qd=1, kvd=1,
+             od=1, ks=None, vs=None, ws=FAKE, wsb=1 << 30, bt=FAKE)
+    a.update(kw)
+    return L.attn_decode(FAKE, FAKE, FAKE, a["bt"], FAKE, FAKE, None, a["S"], a["Hq"], a["Hkv"],
+                         a["d"], a["bs"], a["mb"], a["nb"], a["msl"], a["scale"], a["qd"],
+                         a["kvd"], a["od"], a["ks"], a["vs"], a["ws"], a["wsb"], None)
+
+
+def test_decode_host_validation(L):
+    assert _decode(L, bt=None) == attn.ERR_INVALID
+    assert _decode(L, Hq=6, Hkv=4) == attn.ERR_INVALID
+    assert _decode(L, msl=8 * 16 + 1) == attn.ERR_INVALID              # longer than the table
+    assert _decode(L, wsb=16) == attn.ERR_INVALID                      # workspace too small
+    assert _decode(L, kvd=3, ks=None) == attn.ERR_INVALID              # fp8 without scales
+    assert _decode(L, d=80) == attn.ERR_UNSUPPORTED
+    assert _decode(L, bs=8, msl=64) == attn.ERR_UNSUPPORTED
+    assert _decode(L, Hq=34, Hkv=2) == attn.ERR_UNSUPPORTED            # G > 16
+    assert _decode(L, kvd=0) == attn.ERR_UNSUPPORTED                   # f16 cache, bf16 query
+    assert _decode(L, ws=ctypes.c_void_p((1 << 20) + 16)) == attn.ERR_INVALID
+
+
+def test_decode_workspace_size_is_monotone(L):
+    a = attn.decode_workspace_bytes(64, 32, 128, 32768)
+    b = attn.decode_workspace_bytes(64, 32, 128, 1024)
+    assert a >= b > 0
+    assert attn.decode_workspace_bytes(0, 32, 128, 1024) == 0
+
+
+def test_kv_append_host_validation(L):
+    f = L.attn_kv_append
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 2, 128, 16, 4, 8, 1, 1, None, None,
+             None) == attn.OK                                          # nothing to do
+    assert f(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3, 2, 2, 128, 16, 4, 8, 1, 1, None, None,
+             None) == attn.ERR_INVALID
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3, 2, 2, 128, 16, 4, 8, 1, 3, None, None,
+             None) == attn.ERR_INVALID                                 # fp8 without scales
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3, 2, 2, 100, 16, 4, 8, 1, 1, None, None,
+             None) == attn.ERR_UNSUPPORTED

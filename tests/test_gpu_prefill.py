@@ -1,0 +1,117 @@
+"""Prefill parity: the tcgen05 kernel against the fp64 oracle.
+
+Small shapes are compared element by element over every output; they span
+several 128-row tiles and 128-key blocks with ragged tails, both causal
+alignments, MHA/GQA/MQA and every output format.  The full-size workloads
+are compared on sampled rows (first/last/tile-boundary rows of sampled heads,
+computed row by row by the oracle) in the launch configuration the benchmark
+times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_io_aware_106_b300 import attn, workloads as W
+from tests.parity import assert_lse, assert_out
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+SMALL = [
+    # B, Hq, Hkv, n_q, n_kv, d, causal, in, out
+    (1, 1, 1, 128, 128, 64, False, "f16", "f32"),
+    (1, 1, 1, 512, 512, 64, False, "f16", "f32"),      # single-head workload, whole
+    (1, 2, 1, 300, 300, 128, True, "bf16", "bf16"),
+    (2, 4, 2, 640, 640, 128, True, "bf16", "f32"),
+    (1, 4, 1, 200, 700, 64, True, "bf16", "bf16"),     # n_q < n_kv, bottom-right mask
+    (1, 2, 2, 1, 1, 128, False, "bf16", "bf16"),       # one query, one key
+    (1, 8, 1, 77, 333, 128, False, "f16", "f16"),      # MQA, ragged both ways
+    (1, 1, 1, 1000, 1000, 64, True, "f16", "f32"),
+    (1, 2, 1, 129, 129, 128, True, "bf16", "f32"),     # one row past a tile
+    (3, 3, 3, 257, 511, 128, False, "bf16", "bf16"),   # tile 1 holds one row
+    (1, 16, 1, 256, 256, 64, True, "f16", "bf16"),     # G = 16
+]
+
+
+def _run(spec_t, seed):
+    B, Hq, Hkv, nq, nkv, d, causal, ind, outd = spec_t
+    spec = W.PrefillSpec(B, Hq, Hkv, nq, nkv, d, causal, ind, outd)
+    t = W.make_prefill(spec, seed=seed)
+    O_ref, lse_ref = oracle.sdpa(t["Q"], t["K"], t["V"], causal)
+    Q, K, V = (x.cuda() for x in (t["Q"], t["K"], t["V"]))
+    O, lse = attn.prefill(Q, K, V, causal, out_dtype=DT[outd])
+    assert attn.last_launch_count() == 1
+    assert attn.last_error() == attn.OK
+    return O, lse, O_ref, lse_ref
+
+
+@pytest.mark.parametrize("spec_t", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_prefill_small_all_outputs(spec_t):
+    O, lse, O_ref, lse_ref = _run(spec_t, seed=0)
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_prefill_other_seeds(seed):
+    O, lse, O_ref, lse_ref = _run((1, 4, 2, 384, 384, 128, True, "bf16", "f32"), seed)
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
+def test_prefill_fp32_output_matches_16bit_output():
+    """The 16-bit output is the fp32 output rounded once."""
+    spec = W.PrefillSpec(1, 4, 2, 333, 333, 128, True, "bf16", "bf16")
+    t = W.make_prefill(spec, seed=3)
+    Q, K, V = (x.cuda() for x in (t["Q"], t["K"], t["V"]))
+    O32, _ = attn.prefill(Q, K, V, True, out_dtype=torch.float32)
+    O16, _ = attn.prefill(Q, K, V, True, out_dtype=torch.bfloat16)
+    assert torch.equal(O32.to(torch.bfloat16), O16)
+
+
+def test_prefill_large_scores_do_not_overflow():
+    """Scores far beyond exp's range (|s| ~ 1e3) stay finite: the row max is
+    subtracted before exponentiation."""
+    spec = W.PrefillSpec(1, 2, 1, 200, 200, 64, True, "bf16", "f32")
+    t = W.make_prefill(spec, seed=4)
+    Q = (t["Q"].float() * 30).to(torch.bfloat16)
+    O_ref, lse_ref = oracle.sdpa(Q, t["K"], t["V"], True)
+    O, lse = attn.prefill(Q.cuda(), t["K"].cuda(), t["V"].cuda(), True,
+                          out_dtype=torch.float32)
+    assert torch.isfinite(O).all()
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
+def _sample_rows(n_q, rng, k=6):
+    base = [0, 1, 127, 128, 255, 256, n_q - 1, n_q - 2]
+    base += [int(x) for x in rng.integers(0, n_q, size=k)]
+    return sorted({r for r in base if 0 <= r < n_q})
+
+
+@pytest.mark.parametrize("name", ["gqa-4k", "long-23k", "long-32k"])
+def test_prefill_full_size_sampled_rows(name):
+    spec = W.PREFILL_WORKLOADS[name]
+    t = W.make_prefill(spec, seed=0, device="cuda")
+    O, lse = attn.prefill(t["Q"], t["K"], t["V"], spec.causal,
+                          out_dtype=W.DTYPES[spec.out_dtype])
+    assert attn.last_error() == attn.OK
+    rng = np.random.default_rng(0)
+    heads = sorted({0, spec.Hq - 1} | {int(h) for h in rng.integers(0, spec.Hq, size=2)})
+    bs = sorted({0, spec.B - 1})
+    G = spec.Hq // spec.Hkv
+    for b in bs:
+        for h in heads:
+            rows = _sample_rows(spec.n_q, rng)
+            hk = h // G
+            Qh = t["Q"][b:b + 1, h:h + 1].cpu()
+            Kh = t["K"][b:b + 1, hk:hk + 1].cpu()
+            Vh = t["V"][b:b + 1, hk:hk + 1].cpu()
+            Or, lr = oracle.sdpa_rows(Qh, Kh, Vh, [(0, 0, r) for r in rows], spec.causal,
+                                      nthreads=0)
+            assert_out(O[b, h, rows], Or, what=f"{name} b{b} h{h}")
+            assert_lse(lse[b, h, rows], lr, what=f"{name} b{b} h{h}")
+    # the output is finite everywhere
+    assert torch.isfinite(O.float()).all() and torch.isfinite(lse).all()
