@@ -107,7 +107,8 @@ def make_seq_structure(num_seqs, len_lo, len_hi, block_size, seed, extra_blocks=
                        lens=None):
     """Sequence lengths ~ U{len_lo..len_hi} and a block table dealing a
     seeded random permutation of the physical blocks to the sequences in
-    order.  Unused table entries are -1.  Always drawn on the host."""
+    order.  The table is wide enough for len_hi tokens per sequence; unused
+    entries are -1.  Always drawn on the host."""
     g = _gen("cpu", seed + 7919)
     if lens is None:
         lens = torch.randint(len_lo, len_hi + 1, (num_seqs,), generator=g, dtype=torch.int64)
@@ -115,7 +116,8 @@ def make_seq_structure(num_seqs, len_lo, len_hi, block_size, seed, extra_blocks=
         lens = torch.as_tensor(lens, dtype=torch.int64)
     nblk = (lens + block_size - 1) // block_size
     num_blocks = int(nblk.sum()) + extra_blocks
-    max_blocks = max(1, int(nblk.max()) if num_seqs else 1)
+    max_blocks = max(1, (len_hi + block_size - 1) // block_size,
+                     int(nblk.max()) if num_seqs else 1)
     perm = torch.randperm(max(num_blocks, 1), generator=g, dtype=torch.int64)[:num_blocks]
     table = torch.full((num_seqs, max_blocks), -1, dtype=torch.int32)
     off = 0
