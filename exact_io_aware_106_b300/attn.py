@@ -20,7 +20,11 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 _DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.float8_e4m3fn: 3}
 
 EXPORTS = ("attn_prefill", "attn_decode_workspace_bytes", "attn_decode", "attn_kv_append",
-           "attn_last_error", "attn_status_str", "attn_last_launch_count")
+           "attn_last_error", "attn_status_str", "attn_last_launch_count",
+           "attn_decode_static_ws")
+
+# Scratch size compiled into the library for attn_decode_static_ws.
+DECODE_STATIC_WS_BYTES = 16 << 20
 
 
 class AttnError(RuntimeError):
@@ -55,6 +59,9 @@ def lib():
         L.attn_last_error.restype = i32
         L.attn_status_str.argtypes = [i32]
         L.attn_status_str.restype = ctypes.c_char_p
+        L.attn_decode_static_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                            i32, i32, i32, i32, f32, i32, i32, i32, vp, vp, vp]
+        L.attn_decode_static_ws.restype = i32
         L.attn_last_launch_count.argtypes = []
         L.attn_last_launch_count.restype = i32
         _lib = L

@@ -202,3 +202,56 @@ attn_status attn_last_error(void *stream) {
 }
 
 } // extern "C"
+
+// ------------------------------------------------ decode without allocation
+
+// Split-KV scratch for attn_decode_static_ws, compiled into the library so
+// that callers who may not allocate device memory can still decode.  In
+// host code this name is only a stand-in for the symbol: the device address
+// comes from cudaGetSymbolAddress, per device.
+static __device__ __align__(256) unsigned char g_decode_scratch[ATTN_DECODE_STATIC_WS_BYTES];
+
+namespace {
+
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_decode_scratch on the current device, looked up once
+// per device with that device current; nullptr if the lookup fails.
+void *decode_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
+            return nullptr;
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+
+} // namespace
+
+extern "C" attn_status attn_decode_static_ws(
+    const void *q, const void *Kcache, const void *Vcache, const int32_t *block_table,
+    const int32_t *seq_lens, void *O, float *lse, int num_seqs, int Hq, int Hkv, int d,
+    int block_size, int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
+    attn_dtype q_dtype, attn_dtype kv_dtype, attn_dtype out_dtype, const float *k_scale,
+    const float *v_scale, void *stream) {
+    t_last_launches = 0;
+    if (num_seqs <= 0 || Hq <= 0 || d <= 0 || max_seq_len < 0)
+        return ATTN_ERR_INVALID;
+    // the scratch must hold every split's partial state for these sizes
+    if (attn::decode_workspace_bytes(num_seqs, Hq, d, max_seq_len) >
+        static_cast<size_t>(ATTN_DECODE_STATIC_WS_BYTES))
+        return ATTN_ERR_UNSUPPORTED;
+    void *ws = decode_scratch();
+    if (!ws)
+        return ATTN_ERR_CUDA;
+    return attn_decode(q, Kcache, Vcache, block_table, seq_lens, O, lse, num_seqs, Hq, Hkv, d,
+                       block_size, max_blocks_per_seq, num_blocks, max_seq_len, scale, q_dtype,
+                       kv_dtype, out_dtype, k_scale, v_scale, ws, ATTN_DECODE_STATIC_WS_BYTES,
+                       stream);
+}

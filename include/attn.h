@@ -148,6 +148,38 @@ ATTN_API const char *attn_status_str(attn_status s);
  * point made on this host thread (0 after a host-side error). */
 ATTN_API int attn_last_launch_count(void);
 
+/* Largest scratch attn_decode_static_ws can use: 16 MiB per device. */
+#define ATTN_DECODE_STATIC_WS_BYTES (16u << 20)
+
+/* attn_decode without a caller-provided workspace, for callers that may not
+ * allocate device memory themselves: code running inside a host framework
+ * that owns every device allocation, or latency-critical threads that cannot
+ * afford cudaMalloc (it may synchronise the whole device).  There is no
+ * counterpart of this call on the source pages; it only changes where the
+ * split-KV scratch lives.
+ *
+ * Arguments, results and errors are those of attn_decode, minus the
+ * workspace.  The scratch is a 16 MiB array compiled into the library
+ * (ATTN_DECODE_STATIC_WS_BYTES), held by every GPU that loads the library
+ * until the process exits.  Sizes whose scratch need
+ * (attn_decode_workspace_bytes) exceeds it return ATTN_ERR_UNSUPPORTED before
+ * anything runs.  Nothing is allocated: no cudaMalloc, no cudaFree.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (current device at call time); make that first call before any
+ * stream capture.  Every call on a device shares the one array: calls whose
+ * kernels may overlap on the GPU (other streams, other host threads) race on
+ * it and must be serialised by the caller.  The kernels write every scratch
+ * entry before reading it, so the contents a previous call left behind do
+ * not matter and nothing needs clearing. */
+ATTN_API attn_status attn_decode_static_ws(
+    const void *q, const void *Kcache, const void *Vcache,
+    const int32_t *block_table, const int32_t *seq_lens, void *O, float *lse,
+    int num_seqs, int Hq, int Hkv, int d, int block_size,
+    int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
+    attn_dtype q_dtype, attn_dtype kv_dtype, attn_dtype out_dtype,
+    const float *k_scale, const float *v_scale, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
