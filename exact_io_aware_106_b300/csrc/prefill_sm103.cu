@@ -99,6 +99,37 @@ __device__ __forceinline__ bool tile_split(const Shape &sh, int q0, int t) {
     return keys < kSplitKeys;
 }
 
+// p = 2^(s*c - m) for the 128 scores of this thread's row, packed to 16 bits
+// and stored over the consumed scores (P_hi in columns [0,64) of the S
+// tile; with SPLIT, the rounding residual p - P_hi in columns [64,128)).
+// Returns the row sum of p (fp32, eight independent partial sums).
+template <bool BF16, bool SPLIT>
+__device__ __forceinline__ float exp_pack_store(const float (&s)[BN], float c, float neg,
+                                                uint32_t tS) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        acc[i] = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(s[ch * 32 + 2 * i], c, neg));
+            const float p1 = ex2(fmaf(s[ch * 32 + 2 * i + 1], c, neg));
+            acc[(2 * i) & 7] += p0;
+            acc[(2 * i + 1) & 7] += p1;
+            hi[i] = pack2<BF16>(p0, p1);
+            if constexpr (SPLIT)
+                lo[i] = pack2<BF16>(p0 - lo16<BF16>(hi[i]), p1 - hi16<BF16>(hi[i]));
+        }
+        tmem_st16(tS + ch * 16, hi);
+        if constexpr (SPLIT)
+            tmem_st16(tS + 64 + ch * 16, lo);
+    }
+    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+}
+
 template <int D, bool BF16, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -341,13 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             float s[BN];
+            {
+                uint32_t u[BN];
+                tmem_ld128(tS, u);
 #pragma unroll
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t u[32];
-                tmem_ld32(tS + ch * 32, u);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    s[ch * 32 + i] = __uint_as_float(u[i]);
+                for (int i = 0; i < BN; ++i)
+                    s[i] = __uint_as_float(u[i]);
             }
             const int kbase = j * BN;
             const bool need_mask =
@@ -360,10 +390,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (k > lim)
                         s[k] = -INFINITY;
             }
-            float mx = s[0];
+            // row max as a tree: eight independent chains, then 8 -> 1
+            float mx8[8];
 #pragma unroll
-            for (int k = 1; k < BN; ++k)
-                mx = fmaxf(mx, s[k]);
+            for (int i = 0; i < 8; ++i)
+                mx8[i] = s[i];
+#pragma unroll
+            for (int k = 8; k < BN; ++k)
+                mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_blk = mx * c;
             float m_use = m;
             if (m_blk > m + kRescaleThreshold || m == -INFINITY)
@@ -371,23 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float alpha =
                 (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
             const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
-            float sum = 0.f;
-#pragma unroll
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t hi[16], lo[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(s[ch * 32 + 2 * i], c, neg));
-                    const float p1 = ex2(fmaf(s[ch * 32 + 2 * i + 1], c, neg));
-                    sum += p0 + p1;
-                    hi[i] = pack2<BF16>(p0, p1);
-                    if (split)
-                        lo[i] = pack2<BF16>(p0 - lo16<BF16>(hi[i]), p1 - hi16<BF16>(hi[i]));
-                }
-                tmem_st16(tS + ch * 16, hi);
-                if (split)
-                    tmem_st16(tS + 64 + ch * 16, lo);
-            }
+            const float sum = split ? exp_pack_store<BF16, true>(s, c, neg, tS)
+                                    : exp_pack_store<BF16, false>(s, c, neg, tS);
             // O_t holds the sum over earlier blocks (their MMAs completed
             // before S_t of this block was produced); rescale it in place.
             if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
