@@ -124,7 +124,7 @@ attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache,
     if ((d != 64 && d != 128 && d != 256) ||
         (block_size != 16 && block_size != 32 && block_size != 64) || Hq / Hkv > 16)
         return ATTN_ERR_UNSUPPORTED;
-    if (!aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(q, 2) || !aligned(O, 4) ||
+    if (!aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(q, 16) || !aligned(O, 4) ||
         !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return ATTN_ERR_INVALID;
     if (workspace_bytes < attn::decode_workspace_bytes(num_seqs, Hq, d, max_seq_len))

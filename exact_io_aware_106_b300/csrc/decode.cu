@@ -517,6 +517,340 @@ __global__ void __launch_bounds__(D)
 
 } // namespace dec
 
+// ---------------------------------------------------------------------------
+// 16-bit cache: the two small products on the warp-level tensor cores.
+//
+// Per CTA: (split, KV head hk, sequence s).  The G <= 16 query heads of the
+// group are the rows of one 16-row MMA tile (rows G..15 are zero), so a
+// 16-token unit costs D/8 MMAs for S = q K^T and D/8 (2 D/8 with the P
+// residual) for u += P V, instead of ~G * 16 * D * 2 scalar FMAs.  K and V
+// units arrive by TMA into 128-byte-swizzled shared memory (one 3-D tensor
+// map per cache, box 64 x 16), which makes the ldmatrix reads of both the
+// K operand and the transposed V operand free of bank conflicts.  A producer
+// warp keeps NST units in flight; consumer warp w takes units w, w + 4, ...
+// with its own (m, l, u) per row, and the four states are merged at the end.
+// The online-softmax statistics follow the same rules as the scalar path:
+// log2-domain scores, a reference max moved only when a unit's max exceeds
+// it by more than 8, alpha = 2^(m - m') applied to l and u.
+namespace dm {
+
+constexpr int kUnit = 16;     // tokens per unit (one TMA box row count)
+constexpr int kNC = 4;        // consumer warps
+constexpr int kThreads = (kNC + 1) * 32;
+constexpr int kMaxUnits = 256; // units per CTA (tps <= 4096)
+constexpr int kSplitKeys = 512; // sequences shorter than this carry the P residual
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct Lay {
+    static constexpr int PANELS = D / 64;               // 128-byte column panels
+    static constexpr int PANEL_BYTES = kUnit * 128;     // one TMA box
+    static constexpr int HALF = PANELS * PANEL_BYTES;   // K (or V) of one unit
+    static constexpr int STAGE = 2 * HALF;
+    static constexpr int NST = D == 64 ? 12 : (D == 128 ? 8 : 5);
+    static constexpr int MIN_CTAS = D == 64 ? 4 : (D == 128 ? 3 : 2);
+    static constexpr int QROW = 2 * D + 16;             // padded q row (conflict-free ldmatrix)
+    static constexpr int RING = NST * STAGE;
+    static constexpr int MERGE_U = kNC * 16 * D * 4;
+    static constexpr int MERGE = MERGE_U + kNC * 16 * 8;
+    static constexpr int OFF_Q = RING > MERGE ? RING : MERGE;
+    static constexpr int OFF_BLK = OFF_Q + 16 * QROW;
+    static constexpr int OFF_BAR = OFF_BLK + kMaxUnits * 4;
+    static constexpr int SMEM = OFF_BAR + 2 * NST * 8 + 16 + 1024; // + alignment slack
+};
+
+__device__ __forceinline__ float max4(float a, float b, float c, float d) {
+    return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, Lay<D>::MIN_CTAS)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const void *__restrict__ q_,
+                      const int32_t *__restrict__ block_table,
+                      const int32_t *__restrict__ seq_lens, float2 *__restrict__ ws_ml,
+                      float *__restrict__ ws_u, int Hq, int G, int block_size, int max_blocks,
+                      int num_blocks, int max_seq_len, int tps, int max_splits, float c,
+                      unsigned *err) {
+    using Ly = Lay<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u; // swizzle atoms repeat every 1 KB
+    uint8_t *base = smem_raw + (base_s - raw_s);
+    int32_t *blk_ids = reinterpret_cast<int32_t *>(base + Ly::OFF_BLK);
+    const uint32_t sQ = base_s + Ly::OFF_Q;
+    const uint32_t bar0 = base_s + Ly::OFF_BAR;
+    auto b_full = [&](int i) { return bar0 + 8u * i; };
+    auto b_empty = [&](int i) { return bar0 + 8u * (Ly::NST + i); };
+    __shared__ int s_flag; // 1 = bad index, 2 = aborted
+    __shared__ int s_abort;
+
+    const int split = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int len = seq_lens[s];
+    const bool len_ok = len >= 0 && len <= max_seq_len &&
+                        (len + block_size - 1) / block_size <= max_blocks;
+    if (!len_ok) { // the combine kernel zeroes this sequence's output
+        if (split == 0 && hk == 0 && threadIdx.x == 0)
+            atomicOr(err, DERR_INDEX);
+        return;
+    }
+    const int t0 = split * tps;
+    if (t0 >= len)
+        return; // past the end of this sequence: no partial for this split
+    const int t1 = min(len, t0 + tps);
+    const int nunits = (t1 - t0 + kUnit - 1) / kUnit;
+    const int head0 = hk * G;
+
+    if (threadIdx.x == 0) {
+        s_flag = 0;
+        s_abort = 0;
+    }
+    __syncthreads();
+    for (int u = threadIdx.x; u < nunits; u += kThreads) {
+        const int phys =
+            block_table[static_cast<size_t>(s) * max_blocks + (t0 + u * kUnit) / block_size];
+        if (phys < 0 || phys >= num_blocks)
+            s_flag = 1;
+        blk_ids[u] = phys;
+    }
+    // the group's query rows, zero rows up to 16
+    for (int i = threadIdx.x; i < 16 * (D / 8); i += kThreads) {
+        const int r = i / (D / 8), c8 = i % (D / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < G)
+            v = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(q_) +
+                                                 (static_cast<size_t>(s) * Hq + head0 + r) * D +
+                                                 c8 * 8);
+        *reinterpret_cast<uint4 *>(base + Ly::OFF_Q + r * Ly::QROW + c8 * 16) = v;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Ly::NST; ++i) {
+            mbar_init(b_full(i), 1);  // producer arrive + tx bytes
+            mbar_init(b_empty(i), 1); // the consuming warp
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (s_flag) {
+        if (threadIdx.x == 0)
+            atomicOr(err, DERR_INDEX);
+        for (int r = threadIdx.x; r < G; r += kThreads)
+            ws_ml[(static_cast<size_t>(s) * Hq + head0 + r) * max_splits + split] =
+                make_float2(0.f, -1.f); // l < 0 marks an unusable partial
+        return;
+    }
+    volatile int *abort_flag = &s_abort;
+
+    if (warp == kNC) {
+        // ------------------------------------------------ producer warp
+        if (lane == 0) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            int issued = 0;
+            for (int u = 0; u < nunits; ++u) {
+                const int st = u % Ly::NST;
+                if (u >= Ly::NST &&
+                    !mbar_wait(b_empty(st), ((u / Ly::NST) - 1) & 1, abort_flag, err))
+                    break;
+                const int y = hk * block_size + (t0 + u * kUnit) % block_size;
+                const uint32_t dst = base_s + st * Ly::STAGE;
+                mbar_arrive_expect_tx(b_full(st), Ly::STAGE);
+#pragma unroll
+                for (int p = 0; p < Ly::PANELS; ++p) {
+                    tma_load_3d(dst + p * Ly::PANEL_BYTES, &tm_k, b_full(st), p * 64, y,
+                                blk_ids[u]);
+                    tma_load_3d(dst + Ly::HALF + p * Ly::PANEL_BYTES, &tm_v, b_full(st), p * 64,
+                                y, blk_ids[u]);
+                }
+                issued = u + 1;
+            }
+            if (*abort_flag) {
+                // let copies already in flight land before the CTA exits
+                for (int u = max(0, issued - Ly::NST); u < issued; ++u)
+                    mbar_wait_drain(b_full(u % Ly::NST), (u / Ly::NST) & 1);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    const int g = lane >> 2, t = lane & 3;
+    const int mj = lane >> 3, mr = lane & 7; // ldmatrix: matrix index, row
+    const uint32_t q_lane = sQ + (mr + (mj & 1) * 8) * Ly::QROW + (mj >> 1) * 16;
+    const int k_tok = mr + (mj >> 1) * 8; // K rows: matrices {t0-7,d0-7},{t0-7,d8-15},{t8-15,..}
+    const int v_tok = mr + (mj & 1) * 8;  // V rows: matrices {t0-7,d0-7},{t8-15,d0-7},{t0-7,d8-15},..
+    const bool split_p = len < kSplitKeys;
+
+    float o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n)
+        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    bool ok = true;
+
+    for (int u = warp; u < nunits; u += kNC) {
+        const int st = u % Ly::NST;
+        if (!mbar_wait(b_full(st), (u / Ly::NST) & 1, abort_flag, err)) {
+            ok = false;
+            break;
+        }
+        const uint32_t Ks = base_s + st * Ly::STAGE;
+        const uint32_t Vs = Ks + Ly::HALF;
+        const int nvalid = min(kUnit, t1 - (t0 + u * kUnit));
+        if (nvalid < kUnit) {
+            // V rows past the sequence end get p = 0; zero them so that stale
+            // non-finite cache contents cannot reach u through 0 * x
+            uint8_t *vg = base + (Vs - base_s);
+            const int nz = (kUnit - nvalid) * 8; // 16-byte chunks per panel
+            for (int i = lane; i < Ly::PANELS * nz; i += 32) {
+                const int p = i / nz, r = nvalid + (i % nz) / 8, ch = i % 8;
+                *reinterpret_cast<uint4 *>(vg + p * Ly::PANEL_BYTES + r * 128 + ch * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+
+        // S = q K^T: 16 rows x 16 tokens as two 8-token column tiles
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kc = 0; kc < D / 16; ++kc) {
+            uint32_t a[4], b[4];
+            ldsm_x4(a, q_lane + kc * 32);
+            const int dcol = kc * 16 + (mj & 1) * 8;
+            ldsm_x4(b, Ks + (dcol >> 6) * Ly::PANEL_BYTES + k_tok * 128 +
+                           ((((dcol & 63) >> 3) ^ (k_tok & 7)) << 4));
+            mma16816<BF16>(s0, a, b[0], b[1]);
+            mma16816<BF16>(s1, a, b[2], b[3]);
+        }
+        // log2-domain scores; row g: tokens 2t, 2t+1, 8+2t, 9+2t; row g+8 the same
+        float sc[8] = {s0[0] * c, s0[1] * c, s1[0] * c, s1[1] * c,
+                       s0[2] * c, s0[3] * c, s1[2] * c, s1[3] * c};
+        if (nvalid < kUnit) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int tok = (i >> 1) * 8 + 2 * t + (i & 1);
+                if (tok >= nvalid)
+                    sc[i] = sc[4 + i] = -INFINITY;
+            }
+        }
+        float mx[2] = {max4(sc[0], sc[1], sc[2], sc[3]), max4(sc[4], sc[5], sc[6], sc[7])};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        }
+        float alpha[2], neg[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float mu = m[r];
+            if (mx[r] > m[r] + kRescaleThreshold || m[r] == -INFINITY)
+                mu = fmaxf(mx[r], m[r]);
+            alpha[r] = (mu == m[r]) ? 1.0f : ((m[r] == -INFINITY) ? 0.f : ex2(m[r] - mu));
+            neg[r] = (mu == -INFINITY) ? 0.f : -mu;
+            m[r] = mu;
+        }
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            p[i] = ex2(sc[i] + neg[i >> 2]);
+        l[0] = l[0] * alpha[0] + ((p[0] + p[1]) + (p[2] + p[3]));
+        l[1] = l[1] * alpha[1] + ((p[4] + p[5]) + (p[6] + p[7]));
+        if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                o[n][0] *= alpha[0];
+                o[n][1] *= alpha[0];
+                o[n][2] *= alpha[1];
+                o[n][3] *= alpha[1];
+            }
+        }
+        // P as the A operand: {(g, 2t..), (g+8, 2t..), (g, 8+2t..), (g+8, 8+2t..)}
+        uint32_t pa[4] = {pack2<BF16>(p[0], p[1]), pack2<BF16>(p[4], p[5]),
+                          pack2<BF16>(p[2], p[3]), pack2<BF16>(p[6], p[7])};
+        uint32_t pl[4];
+        if (split_p) {
+            // rounding residual of the 16-bit P, multiplied in as a second
+            // product so that short sequences do not see P's rounding
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int lo_i = (i & 1) * 4 + (i >> 1) * 2;
+                pl[i] = pack2<BF16>(p[lo_i] - lo16<BF16>(pa[i]), p[lo_i + 1] - hi16<BF16>(pa[i]));
+            }
+        }
+        // u += P V: V^T fragments by transposed ldmatrix, two d-tiles per load
+#pragma unroll
+        for (int np = 0; np < D / 16; ++np) {
+            uint32_t b[4];
+            const int dcol = np * 16 + (mj >> 1) * 8;
+            ldsm_x4_t(b, Vs + (dcol >> 6) * Ly::PANEL_BYTES + v_tok * 128 +
+                             ((((dcol & 63) >> 3) ^ (v_tok & 7)) << 4));
+            mma16816<BF16>(o[2 * np], pa, b[0], b[1]);
+            mma16816<BF16>(o[2 * np + 1], pa, b[2], b[3]);
+            if (split_p) {
+                mma16816<BF16>(o[2 * np], pl, b[0], b[1]);
+                mma16816<BF16>(o[2 * np + 1], pl, b[2], b[3]);
+            }
+        }
+        __syncwarp();
+        if (nvalid < kUnit)
+            fence_proxy_async_smem(); // the zeroing stores precede the next copy into this stage
+        if (lane == 0)
+            mbar_arrive(b_empty(st));
+    }
+    // the four lanes of a quad hold partial row sums of the same rows
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+    }
+    if (!ok)
+        s_flag = 2;
+
+    // ---- merge the consumer warps' states (the ring is drained: every
+    // issued unit was consumed before its consumer reached this barrier)
+    asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
+    float *mrg_u = reinterpret_cast<float *>(base);                      // [kNC][16][D]
+    float2 *mrg_ml = reinterpret_cast<float2 *>(base + Ly::MERGE_U);     // [kNC][16]
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+        const int col = n * 8 + 2 * t;
+        if (g < G)
+            *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g) * D + col) =
+                make_float2(o[n][0], o[n][1]);
+        if (g + 8 < G)
+            *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g + 8) * D + col) =
+                make_float2(o[n][2], o[n][3]);
+    }
+    if (t == 0) {
+        mrg_ml[warp * 16 + g] = make_float2(m[0], l[0]);
+        mrg_ml[warp * 16 + g + 8] = make_float2(m[1], l[1]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
+    const bool bad = s_flag != 0;
+    for (int idx = threadIdx.x; idx < G * D; idx += kNC * 32) {
+        const int r = idx / D, e = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kNC; ++w)
+            M = fmaxf(M, mrg_ml[w * 16 + r].x);
+        float Lsum = 0.f, U = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNC; ++w) {
+            const float2 ml = mrg_ml[w * 16 + r];
+            const float sc = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+            Lsum += sc * ml.y;
+            U += sc * mrg_u[(w * 16 + r) * D + e];
+        }
+        const size_t o_idx = (static_cast<size_t>(s) * Hq + head0 + r) * max_splits + split;
+        ws_u[o_idx * D + e] = U;
+        if (e == 0)
+            ws_ml[o_idx] = bad ? make_float2(0.f, -1.f) : make_float2(M, Lsum);
+    }
+}
+
+} // namespace dm
+
 // ------------------------------------------------------------------ host
 
 // Tokens per split: a function of max_seq_len only, so that the workspace
@@ -599,6 +933,34 @@ static cudaError_t launch_combine(const DecodeArgs &a, const float2 *ws_ml, cons
     return cudaGetLastError();
 }
 
+template <int D, bool BF16>
+static cudaError_t launch_mma(const DecodeArgs &a, float2 *ws_ml, float *ws_u, int tps,
+                              int max_splits, cudaStream_t st) {
+    using Ly = dm::Lay<D>;
+    // cache [num_blocks, Hkv, block_size, D] viewed as {D, Hkv * block_size, num_blocks}
+    const uint64_t dims[3] = {static_cast<uint64_t>(D),
+                              static_cast<uint64_t>(a.Hkv) * a.block_size,
+                              static_cast<uint64_t>(a.num_blocks)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(a.Hkv) * a.block_size * D * 2};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(dm::kUnit), 1};
+    CUtensorMap mk, mv;
+    if (!make_tmap_3d_16bit(&mk, a.Kc, BF16, dims, strides, box) ||
+        !make_tmap_3d_16bit(&mv, a.Vc, BF16, dims, strides, box))
+        return cudaErrorInvalidValue;
+    auto kern = dm::decode_mma_kernel<D, BF16>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    dim3 grid(max_splits, a.Hkv, a.num_seqs);
+    kern<<<grid, dm::kThreads, Ly::SMEM, st>>>(
+        mk, mv, a.q, a.block_table, a.seq_lens, ws_ml, ws_u, a.Hq, a.Hq / a.Hkv, a.block_size,
+        a.max_blocks, a.num_blocks, a.max_seq_len, tps, max_splits,
+        a.scale * 1.4426950408889634f, a.err);
+    return cudaGetLastError();
+}
+
 template <int D>
 static cudaError_t decode_d(const DecodeArgs &a, cudaStream_t st) {
     const int tps = decode_tokens_per_split(a.max_seq_len);
@@ -611,9 +973,9 @@ static cudaError_t decode_d(const DecodeArgs &a, cudaStream_t st) {
     if (a.kv_e4m3)
         e = dispatch_hpw<D, true, true>(a, ws_ml, ws_u, tps, max_splits, st);
     else if (a.q_bf16)
-        e = dispatch_hpw<D, true, false>(a, ws_ml, ws_u, tps, max_splits, st);
+        e = launch_mma<D, true>(a, ws_ml, ws_u, tps, max_splits, st);
     else
-        e = dispatch_hpw<D, false, false>(a, ws_ml, ws_u, tps, max_splits, st);
+        e = launch_mma<D, false>(a, ws_ml, ws_u, tps, max_splits, st);
     if (e != cudaSuccess)
         return e;
     switch (a.out_dtype) {

@@ -2,6 +2,7 @@
 // translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -53,6 +54,11 @@ struct AppendArgs {
     const float *v_scale;
     unsigned *err;
 };
+
+// 3-D tensor map over a 16-bit tensor with 128-byte swizzle and zero fill
+// outside the bounds (dims innermost first, strides in bytes for dims 1, 2).
+bool make_tmap_3d_16bit(CUtensorMap *m, const void *ptr, bool bf16, const uint64_t dims[3],
+                        const uint64_t strides_bytes[2], const uint32_t box[3]);
 
 cudaError_t prefill_launch(const PrefillArgs &a, cudaStream_t st);
 cudaError_t decode_launch(const DecodeArgs &a, cudaStream_t st);

@@ -486,42 +486,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn get_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
 // [d, n, bh] bf16/f16 tensor, box {64, 128, 1}, 128-byte swizzle, zero fill.
 static bool make_map(CUtensorMap *m, const void *ptr, int d, int n, int bh, bool bf16) {
-    EncodeTiledFn enc = get_encode_fn();
-    if (!enc)
-        return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
-                          static_cast<cuuint64_t>(bh)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                             static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(n)};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                     3, const_cast<void *>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(n),
+                              static_cast<uint64_t>(bh)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2,
+                                 static_cast<uint64_t>(d) * 2 * static_cast<uint64_t>(n)};
+    const uint32_t box[3] = {64, 128, 1};
+    return make_tmap_3d_16bit(m, ptr, bf16, dims, strides, box);
 }
 
 template <int D, bool BF16, int OUT>

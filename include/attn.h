@@ -102,7 +102,8 @@ ATTN_API size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d,
  *   O        [num_seqs, Hq, d] out_dtype;  lse [num_seqs, Hq] fp32 or NULL
  *   workspace: >= attn_decode_workspace_bytes(...) bytes, 256-byte aligned;
  *            its contents on entry do not matter and are overwritten.
- * block_size in {16, 32, 64}; d in {64, 128, 256}; Hq / Hkv <= 16.
+ * block_size in {16, 32, 64}; d in {64, 128, 256}; Hq / Hkv <= 16; q, the
+ * caches and the workspace 16-byte aligned (the workspace 256-byte).
  * A sequence of length 0 yields O = 0 and lse = -inf.  Two kernel launches
  * (split kernel, then combine).  The workspace must not be shared by
  * overlapping calls. */
