@@ -168,18 +168,21 @@ def _src_sha(path):
 
 
 def measured_traffic(kernel_file: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel
-    source is unchanged since the counters were taken; else None."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes (read + write) per launch from the committed ncu summary
+    table profiles/traffic.txt, if the kernel source is unchanged since the
+    counters were taken; else None.  Each line of the table:
+    `<workload> <kernel source file> <source sha256[:16]> <bytes per launch>`."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(workload)
-    if not d:
-        return None
     src = os.path.join(ROOT, "exact_io_aware_106_b300", "csrc", kernel_file)
-    if d.get("source_sha") != _src_sha(src):
-        return None
-    return d.get("dram_bytes_per_launch")
+    sha = _src_sha(src)
+    for ln in open(p):
+        f = ln.split()
+        if len(f) == 4 and not ln.startswith("#") and f[0] == workload and f[1] == kernel_file \
+                and f[2] == sha:
+            return float(f[3])
+    return None
 
 
 def run_ours(args, rank, world):
@@ -294,6 +297,7 @@ def run_ours(args, rank, world):
     }
 
     res["traffic"] = measured_traffic("prefill_sm103.cu", PREFILL.name)
+    res["traffic_dec"] = measured_traffic("decode.cu", DECODE.name)
     if args.no_e2e or args.only != "step":
         res["t_e2e"], res["h2d"], res["d2h"] = None, 0, 0
         return res
@@ -473,8 +477,8 @@ def main():
     pk = res["peaks"]
     if rank == 0:
         value = 100.0 * roof_total / t_step
-        pre_tflops = res["F"] / res["t_pre"] / 1e12 if res["t_pre"] > 0 else None
-        dec_gbs = res["Bd"] / res["t_dec"] / 1e9 if res["t_dec"] > 0 else None
+        pre_tflops = res["F"] / res["t_pre"] / 1e12 if args.only != "decode" else None
+        dec_gbs = res["Bd"] / res["t_dec"] / 1e9 if args.only != "prefill" else None
         r2 = lambda x, n: None if x is None or x != x else round(x, n)  # noqa: E731
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "% of roofline",
@@ -513,12 +517,15 @@ def main():
                 "pct_roofline": round(100 * res["roof_dec"] / res["t_dec"], 2),
                 "frac_of_8tbs_spec": round(dec_gbs / 8000.0, 4), "bytes": res["Bd"]}
             line["append"] = {"ms": round(res["t_app"] * 1e3, 4)}
+            dec_roof = {
+                "bound": "hbm", "kernel": "decode_mma_kernel<128,bf16> + decode_combine_kernel",
+                "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(dec_gbs / pk["hbm_gbs"], 4),
+                "peak_kind": f"{pk['source']} HBM copy", "traffic": res["traffic_dec"]}
             if pre_tflops is None:
-                line["roofline"] = {
-                    "bound": "hbm", "kernel": "decode_split_kernel<128,4,bf16,bf16>",
-                    "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(dec_gbs / pk["hbm_gbs"], 4),
-                    "peak_kind": f"{pk['source']} HBM copy", "traffic": None}
+                line["roofline"] = dec_roof
+            else:
+                line["decode_roofline"] = dec_roof
         line["e2e"] = {"value": r2(100.0 * roof_total / t_e2e, 3), "unit": "% of roofline",
                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                        "ms_per_step": r2(t_e2e * 1e3, 3)}
