@@ -353,6 +353,104 @@ def run_ours(args, rank, world):
     return res
 
 
+# ------------------------------------------------- single named workloads
+
+def _time_kernel(fn, stream, warmup, steps, flush):
+    """Median and best device time of fn() over `steps` runs, L2 flushed
+    (a 256 MiB write) before every run, outside the timed events."""
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) / 1e3)
+    return statistics.median(ts), min(ts)
+
+
+def workload_lines(name: str, steps: int, warmup: int):
+    """Time one named workload (or every cell of the G x d x dtype sweep) by
+    itself and yield one JSON-ready dict per measurement."""
+    from exact_io_aware_106_b300 import attn
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    jobs = []
+    if name in W.PREFILL_WORKLOADS:
+        jobs.append(("prefill", W.PREFILL_WORKLOADS[name]))
+    elif name in W.DECODE_WORKLOADS:
+        jobs.append(("decode", W.DECODE_WORKLOADS[name]))
+    elif name == "sweep":
+        for kv in ("bf16", "e4m3"):
+            for G in (1, 4, 8, 16):
+                for d in (64, 128, 256):
+                    jobs.append(("decode", W.sweep_decode(G, d, kv)))
+                    jobs.append(("prefill", W.sweep_prefill(G, d, kv)))
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    for kind, spec in jobs:
+        line = {"workload": spec.name, "kind": kind}
+        try:
+            if kind == "prefill":
+                t = W.make_prefill(spec, seed=0, device=dev)
+                kw = {}
+                if spec.dtype == "e4m3":
+                    kw = W.quantize_prefill_e4m3(t)
+                Q, K, V = kw.pop("Q", t["Q"]), kw.pop("K", t["K"]), kw.pop("V", t["V"])
+                O = torch.empty(t["Q"].shape, dtype=W.DTYPES[spec.out_dtype], device=dev)
+                lse = torch.empty(t["Q"].shape[:3], dtype=torch.float32, device=dev)
+
+                def fn():
+                    attn.prefill(Q, K, V, spec.causal, O=O, lse=lse, stream=stream, **kw)
+                med, best = _time_kernel(fn, stream, warmup, steps, flush)
+                F = prefill_flops(spec)
+                peak = pk["bf16_tflops"] * (2.0 if spec.dtype == "e4m3" else 1.0)
+                Bp = prefill_bytes(spec)
+                roof = max(F / (peak * 1e12), Bp / (pk["hbm_gbs"] * 1e9))
+                line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            tflops=round(F / med / 1e12, 2),
+                            pct_roofline=round(100 * roof / med, 2),
+                            peak_tflops=peak,
+                            peak_kind="measured burst bf16" + (
+                                " x 2 (nominal fp8/bf16 ratio)" if spec.dtype == "e4m3" else ""))
+            else:
+                dd = W.make_decode(spec, seed=0, device=dev)
+                lens = dd["seq_lens"].cpu()
+                S = spec.num_seqs
+                Od = torch.empty((S, spec.Hq, spec.d), dtype=W.DTYPES[spec.out_dtype], device=dev)
+                lsed = torch.empty((S, spec.Hq), dtype=torch.float32, device=dev)
+                ws = torch.empty(attn.decode_workspace_bytes(S, spec.Hq, spec.d, spec.len_hi),
+                                 dtype=torch.uint8, device=dev)
+
+                def fn():
+                    attn.decode(dd["q"], dd["Kc"], dd["Vc"], dd["block_table"], dd["seq_lens"],
+                                max_seq_len=spec.len_hi, k_scale=dd["k_scale"],
+                                v_scale=dd["v_scale"], O=Od, lse=lsed, workspace=ws,
+                                stream=stream)
+                med, best = _time_kernel(fn, stream, warmup, steps, flush)
+                Bd = decode_bytes(spec, lens)
+                roof = max(decode_flops(spec, lens) / (pk["bf16_tflops"] * 1e12),
+                           Bd / (pk["hbm_gbs"] * 1e9))
+                line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            gbs=round(Bd / med / 1e9, 1), bytes=Bd,
+                            pct_roofline=round(100 * roof / med, 2),
+                            peak_gbs=pk["hbm_gbs"], peak_kind="measured HBM copy")
+            if attn.last_error(stream) != attn.OK:
+                line["device_error"] = True
+        except Exception as e:  # an unsupported cell is reported, not hidden
+            line["unsupported"] = str(e).splitlines()[0][:160]
+        yield line
+
+
 # ------------------------------------------------------------- CPU oracle
 
 def oracle_sample(threads: int, rows: int, seqs: int, seed: int = 0):
@@ -451,9 +549,19 @@ def main():
                     help="override the prefill length (smaller profiling case)")
     ap.add_argument("--decode-seqs", type=int, default=0,
                     help="override the number of decode sequences (profiling case)")
+    ap.add_argument("--workload", default="",
+                    help="time one named workload alone (single-head, gqa-4k, long-23k, "
+                         "long-32k, paged-decode) or every cell of 'sweep'; one line each")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+
+    if args.workload:
+        for line in workload_lines(args.workload, args.steps, args.warmup):
+            line.update(metric=METRIC, unit="% of roofline", n_gpus=1, impl="ours",
+                        data="synthetic", l2="flushed before every timed run")
+            print(json.dumps(line), flush=True)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -74,9 +74,9 @@ attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, f
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
         (lse && !aligned(lse, 4)))
         return ATTN_ERR_INVALID;
-    if (!is16(in_dtype) || !is_out(out_dtype) || (d != 64 && d != 128))
+    if (!is16(in_dtype) || !is_out(out_dtype) || (d != 64 && d != 128 && d != 256))
         return ATTN_ERR_UNSUPPORTED;
-    const long long nqb = (n_q + 255) / 256;
+    const long long nqb = (n_q + 127) / 128;
     if (nqb * B * Hq > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
     unsigned *err = err_word();

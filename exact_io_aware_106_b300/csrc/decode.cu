@@ -45,6 +45,9 @@ struct Layout {
     static constexpr int NST0 = 65536 / (2 * UNIT_BYTES);
     static constexpr int NST = NST0 < 4 ? 4 : (NST0 > 16 ? 16 : NST0);
     static_assert(NCHUNK * CH == EPL, "lane element split");
+    // block groups (1, 2 or 4) take units round-robin: a stage must always
+    // belong to the same group for the parity waits to be exact
+    static_assert(NST % kCW == 0, "each stage must belong to one block group");
 };
 
 // Element index of chunk c, element i of lane column dc.
@@ -547,7 +550,14 @@ struct Lay {
     static constexpr int PANEL_BYTES = kUnit * 128;     // one TMA box
     static constexpr int HALF = PANELS * PANEL_BYTES;   // K (or V) of one unit
     static constexpr int STAGE = 2 * HALF;
-    static constexpr int NST = D == 64 ? 12 : (D == 128 ? 8 : 5);
+    // Unit u lives in stage u % NST and is consumed by warp u % kNC.  With
+    // NST a multiple of kNC a stage is only ever consumed by one warp, so
+    // that warp has itself waited for the stage's previous phase before it
+    // waits (by parity) for the next one; otherwise a warp could wait on a
+    // stage whose previous fill, for another warp, has not landed yet, and
+    // the parity test would pass one phase early.
+    static constexpr int NST = D == 64 ? 12 : (D == 128 ? 8 : 4);
+    static_assert(NST % kNC == 0, "each stage must belong to one consumer warp");
     static constexpr int MIN_CTAS = D == 64 ? 4 : (D == 128 ? 3 : 2);
     static constexpr int QROW = 2 * D + 16;             // padded q row (conflict-free ldmatrix)
     static constexpr int RING = NST * STAGE;

@@ -484,15 +484,389 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 } // namespace pf
 
+// ---------------------------------------------------------------------------
+// Head size 256.  Two 128-row tiles would need 2 x (128 + 256) tensor-memory
+// columns, more than the 512 an SM has, so one CTA owns one query tile and
+// the overlap comes from double-buffering S over consecutive key blocks:
+// while the softmax warpgroup turns S_(j mod 2) into P, the tensor core
+// computes O += P_(j-1) V_(j-1) and S_(j+1).  Key blocks are 64 wide so that
+// two K and two V stages fit next to the 64 KB Q tile.
+//   warp 4      TMA producer (Q once, K / V rings of 2 stages)
+//   warp 5      MMA issuer (one thread)
+//   warps 0-3   softmax, one thread per row; the epilogue
+// Tensor memory: S_0 [0,64), S_1 [64,128), O [128, 384).  A block that moves
+// the reference max rescales O only after the previous block's P V product
+// has completed (barrier o_done, one phase per product).
+namespace pfw {
+
+constexpr int D = 256;
+constexpr int BM = 128;
+constexpr int BN = 64;
+constexpr int PANELS = D / 64;
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int NK = 2, NV = 2;
+constexpr int Q_BYTES = BM * D * 2;     // 64 KB
+constexpr int KV_BYTES = BN * D * 2;    // 32 KB
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_V = OFF_K + NK * KV_BYTES;
+constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
+// qfull, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], pfull[2], odone, ofull, drain
+constexpr int NBAR = 1 + 2 * NK + 2 * NV + 4 + 3;
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int SMEM = OFF_MISC + 64 + 1024;
+constexpr int S_COL0 = 0, O_COL = 2 * BN;
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(O_COL + D <= 512, "tensor memory budget");
+
+__device__ __forceinline__ int tile_blocks(const pf::Shape &sh, int r0) {
+    const int nkb = (sh.n_kv + BN - 1) / BN;
+    if (!sh.causal)
+        return nkb;
+    const int r_last = min(r0 + BM - 1, sh.n_q - 1);
+    return min(nkb, (r_last + (sh.n_kv - sh.n_q)) / BN + 1);
+}
+
+template <bool BF16, bool SPLIT>
+__device__ __forceinline__ float exp_pack_store64(const float (&s)[BN], float c, float neg,
+                                                  uint32_t tS) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        acc[i] = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(s[ch * 32 + 2 * i], c, neg));
+            const float p1 = ex2(fmaf(s[ch * 32 + 2 * i + 1], c, neg));
+            acc[(2 * i) & 7] += p0;
+            acc[(2 * i + 1) & 7] += p1;
+            hi[i] = pack2<BF16>(p0, p1);
+            if constexpr (SPLIT)
+                lo[i] = pack2<BF16>(p0 - lo16<BF16>(hi[i]), p1 - hi16<BF16>(hi[i]));
+        }
+        tmem_st16(tS + ch * 16, hi);
+        if constexpr (SPLIT)
+            tmem_st16(tS + BN / 2 + ch * 16, lo);
+    }
+    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+}
+
+template <bool BF16, int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, void *__restrict__ O,
+                        float *__restrict__ lse, const pf::Shape sh, unsigned *err) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+    const uint32_t sQ = base_s + OFF_Q, sK = base_s + OFF_K, sV = base_s + OFF_V;
+    const uint32_t bar0 = base_s + OFF_BAR;
+    const uint32_t b_qfull = bar0;
+    auto b_kfull = [&](int i) { return bar0 + 8u * (1 + i); };
+    auto b_kempty = [&](int i) { return bar0 + 8u * (1 + NK + i); };
+    auto b_vfull = [&](int i) { return bar0 + 8u * (1 + 2 * NK + i); };
+    auto b_vempty = [&](int i) { return bar0 + 8u * (1 + 2 * NK + NV + i); };
+    auto b_sfull = [&](int b) { return bar0 + 8u * (1 + 2 * NK + 2 * NV + b); };
+    auto b_pfull = [&](int b) { return bar0 + 8u * (1 + 2 * NK + 2 * NV + 2 + b); };
+    const uint32_t b_odone = bar0 + 8u * (1 + 2 * NK + 2 * NV + 4);
+    const uint32_t b_ofull = b_odone + 8u;
+    const uint32_t b_drain = b_ofull + 8u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + OFF_MISC + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = sh.B * sh.Hq;
+    const int qb = sh.nqb - 1 - static_cast<int>(blockIdx.x) / BH; // heaviest first
+    const int bh = static_cast<int>(blockIdx.x) % BH;
+    const int b = bh / sh.Hq, h = bh % sh.Hq;
+    const int bkv = b * sh.Hkv + h / sh.G;
+    const int r0 = qb * BM;
+    const int nb = tile_blocks(sh, r0);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(b_qfull, 1);
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(b_kfull(i), 1);
+            mbar_init(b_kempty(i), 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(b_vfull(i), 1);
+            mbar_init(b_vempty(i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(b_sfull(i), 1);
+            mbar_init(b_pfull(i), 4);
+        }
+        mbar_init(b_odone, 1);
+        mbar_init(b_ofull, 1);
+        mbar_init(b_drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ================================================= TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(b_qfull, Q_BYTES);
+            for (int p = 0; p < PANELS; ++p)
+                tma_load_3d(sQ + p * BM * 128, &tm_q, b_qfull, p * 64, r0, bh);
+            int k_issued = 0, v_issued = 0;
+            for (int j = 0; j < nb; ++j) {
+                const int ks = j % NK;
+                if (j >= NK && !mbar_wait(b_kempty(ks), ((j / NK) - 1) & 1, abort_flag, err))
+                    break;
+                mbar_arrive_expect_tx(b_kfull(ks), KV_BYTES);
+                for (int p = 0; p < PANELS; ++p)
+                    tma_load_3d(sK + ks * KV_BYTES + p * BN * 128, &tm_k, b_kfull(ks), p * 64,
+                                j * BN, bkv);
+                k_issued = j + 1;
+                const int vs = j % NV;
+                if (j >= NV && !mbar_wait(b_vempty(vs), ((j / NV) - 1) & 1, abort_flag, err))
+                    break;
+                mbar_arrive_expect_tx(b_vfull(vs), KV_BYTES);
+                for (int p = 0; p < PANELS; ++p)
+                    tma_load_3d(sV + vs * KV_BYTES + p * BN * 128, &tm_v, b_vfull(vs), p * 64,
+                                j * BN, bkv);
+                v_issued = j + 1;
+            }
+            if (*abort_flag) { // let in-flight copies land before the CTA exits
+                mbar_wait_drain(b_qfull, 0);
+                for (int u = max(0, k_issued - NK); u < k_issued; ++u)
+                    mbar_wait_drain(b_kfull(u % NK), (u / NK) & 1);
+                for (int u = max(0, v_issued - NV); u < v_issued; ++u)
+                    mbar_wait_drain(b_vfull(u % NV), (u / NV) & 1);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_f16(BM, BN, BF16, false, false);
+            constexpr uint32_t idesc_pv = idesc_f16(BM, D, BF16, false, true);
+            const bool split = (sh.causal ? (r0 + (sh.n_kv - sh.n_q) + 1) : sh.n_kv) <
+                               pf::kSplitKeys;
+            auto issue_qk = [&](int buf, int ks) {
+                const uint32_t kb = sK + ks * KV_BYTES;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t offa = (k / 4) * (BM * 128) + (k % 4) * 32;
+                    const uint32_t offb = (k / 4) * (BN * 128) + (k % 4) * 32;
+                    mma_ss(tmem + S_COL0 + buf * BN, sdesc_sw128(sQ + offa, 16, 1024),
+                           sdesc_sw128(kb + offb, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int buf, int vs, bool first) {
+                const uint32_t vb = sV + vs * KV_BYTES;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+                    mma_ts(tmem + O_COL, tmem + S_COL0 + buf * BN + k * 8, bd, idesc_pv,
+                           (first && k == 0) ? 0u : 1u);
+                }
+                if (split) {
+#pragma unroll
+                    for (int k = 0; k < BN / 16; ++k) {
+                        const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+                        mma_ts(tmem + O_COL, tmem + S_COL0 + buf * BN + BN / 2 + k * 8, bd,
+                               idesc_pv, 1u);
+                    }
+                }
+            };
+            bool ok = mbar_wait(b_qfull, 0, abort_flag, err);
+            // S for the first two blocks
+            for (int j = 0; ok && j < min(2, nb); ++j) {
+                ok = mbar_wait(b_kfull(j % NK), (j / NK) & 1, abort_flag, err);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                issue_qk(j & 1, j % NK);
+                tc_commit(b_sfull(j & 1));
+                tc_commit(b_kempty(j % NK));
+            }
+            for (int j = 0; ok && j < nb; ++j) {
+                const int buf = j & 1, vs = j % NV;
+                if (!mbar_wait(b_vfull(vs), (j / NV) & 1, abort_flag, err) ||
+                    !mbar_wait(b_pfull(buf), (j >> 1) & 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_pv(buf, vs, j == 0);
+                tc_commit(b_vempty(vs));
+                tc_commit(b_odone);
+                const int jn = j + 2;
+                if (jn < nb) {
+                    if (!mbar_wait(b_kfull(jn % NK), (jn / NK) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_qk(buf, jn % NK);
+                    tc_commit(b_sfull(buf));
+                    tc_commit(b_kempty(jn % NK));
+                }
+            }
+            if (ok)
+                tc_commit(b_ofull);
+            tc_commit(b_drain);
+            mbar_wait_drain(b_drain, 0);
+        }
+    } else {
+        // ================================================= softmax warps
+        const int r = warp * 32 + lane;
+        const int row_g = r0 + r;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tO = tmem + lane_off + O_COL;
+        const int off = sh.n_kv - sh.n_q;
+        const bool split = (sh.causal ? (r0 + off + 1) : sh.n_kv) < pf::kSplitKeys;
+        const float c = sh.c;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nb; ++j) {
+            const int buf = j & 1;
+            const uint32_t tS = tmem + lane_off + S_COL0 + buf * BN;
+            if (!mbar_wait(b_sfull(buf), (j >> 1) & 1, abort_flag, err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[BN];
+            {
+                uint32_t u[BN];
+                tmem_ld64(tS, u);
+#pragma unroll
+                for (int i = 0; i < BN; ++i)
+                    s[i] = __uint_as_float(u[i]);
+            }
+            const int kbase = j * BN;
+            if ((sh.causal && kbase + BN - 1 > r0 + off) || (kbase + BN > sh.n_kv)) {
+                int lim = sh.causal ? row_g + off : sh.n_kv - 1;
+                lim = min(lim, sh.n_kv - 1) - kbase;
+#pragma unroll
+                for (int k = 0; k < BN; ++k)
+                    if (k > lim)
+                        s[k] = -INFINITY;
+            }
+            float mx8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                mx8[i] = s[i];
+#pragma unroll
+            for (int k = 8; k < BN; ++k)
+                mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float m_blk = mx * c;
+            float m_use = m;
+            if (m_blk > m + pf::kRescaleThreshold || m == -INFINITY)
+                m_use = fmaxf(m_blk, m);
+            const float alpha =
+                (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
+            const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
+            if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
+                // O must hold exactly the blocks before j: wait for P_(j-1) V_(j-1)
+                if (!mbar_wait(b_odone, (j - 1) & 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t u[32];
+                    tmem_ld32(tO + ch * 32, u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                    tmem_st32(tO + ch * 32, u);
+                }
+            }
+            const float sum = split ? exp_pack_store64<BF16, true>(s, c, neg, tS)
+                                    : exp_pack_store64<BF16, false>(s, c, neg, tS);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b_pfull(buf));
+            l = l * alpha + sum;
+            m = m_use;
+        }
+        if (ok && nb > 0)
+            ok = mbar_wait(b_ofull, 0, abort_flag, err);
+        tc_fence_after();
+        const bool row_ok = row_g < sh.n_q;
+        const float inv = (ok && l > 0.f) ? 1.0f / l : 0.f;
+        const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row_g) * D;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t u[32];
+            tmem_ld32(tO + ch * 32, u);
+            if (row_ok) {
+                float o[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    o[i] = ok ? __uint_as_float(u[i]) * inv : 0.f;
+                if constexpr (OUT == 2) {
+                    float4 *dst =
+                        reinterpret_cast<float4 *>(static_cast<float *>(O) + orow + ch * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                } else {
+                    uint4 *dst =
+                        reinterpret_cast<uint4 *>(static_cast<uint16_t *>(O) + orow + ch * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pack2<OUT == 1>(o[8 * i], o[8 * i + 1]),
+                                            pack2<OUT == 1>(o[8 * i + 2], o[8 * i + 3]),
+                                            pack2<OUT == 1>(o[8 * i + 4], o[8 * i + 5]),
+                                            pack2<OUT == 1>(o[8 * i + 6], o[8 * i + 7]));
+                }
+            }
+        }
+        if (lse != nullptr && row_ok)
+            lse[static_cast<size_t>(bh) * sh.n_q + row_g] =
+                ok ? (m + __log2f(l)) * 0.69314718055994530942f : __int_as_float(0x7fc00000);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+} // namespace pfw
+
 // ------------------------------------------------------------------ host
 
-// [d, n, bh] bf16/f16 tensor, box {64, 128, 1}, 128-byte swizzle, zero fill.
-static bool make_map(CUtensorMap *m, const void *ptr, int d, int n, int bh, bool bf16) {
+// [d, n, bh] bf16/f16 tensor, box {64, rows, 1}, 128-byte swizzle, zero fill.
+static bool make_map(CUtensorMap *m, const void *ptr, int d, int n, int bh, bool bf16,
+                     int rows = 128) {
     const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(n),
                               static_cast<uint64_t>(bh)};
     const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2,
                                  static_cast<uint64_t>(d) * 2 * static_cast<uint64_t>(n)};
-    const uint32_t box[3] = {64, 128, 1};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(rows), 1};
     return make_tmap_3d_16bit(m, ptr, bf16, dims, strides, box);
 }
 
@@ -537,7 +911,49 @@ static cudaError_t launch_prefill_out(const PrefillArgs &a, cudaStream_t st) {
     }
 }
 
+template <bool BF16, int OUT>
+static cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.Q, pfw::D, a.n_q, a.B * a.Hq, BF16, pfw::BM) ||
+        !make_map(&mk, a.K, pfw::D, a.n_kv, a.B * a.Hkv, BF16, pfw::BN) ||
+        !make_map(&mv, a.V, pfw::D, a.n_kv, a.B * a.Hkv, BF16, pfw::BN))
+        return cudaErrorInvalidValue;
+    pf::Shape sh;
+    sh.B = a.B;
+    sh.Hq = a.Hq;
+    sh.Hkv = a.Hkv;
+    sh.G = a.Hq / a.Hkv;
+    sh.n_q = a.n_q;
+    sh.n_kv = a.n_kv;
+    sh.causal = a.causal;
+    sh.nqb = (a.n_q + pfw::BM - 1) / pfw::BM;
+    sh.c = a.scale * 1.4426950408889634f;
+    sh.scale = a.scale;
+    auto kern = pfw::prefill_wide_kernel<BF16, OUT>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pfw::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    const long long grid = static_cast<long long>(sh.nqb) * a.B * a.Hq;
+    if (grid > 0x7fffffffLL)
+        return cudaErrorInvalidValue;
+    kern<<<static_cast<unsigned>(grid), pfw::kThreads, pfw::SMEM, st>>>(mq, mk, mv, a.O, a.lse,
+                                                                        sh, a.err);
+    return cudaGetLastError();
+}
+
+template <bool BF16>
+static cudaError_t launch_prefill_wide_out(const PrefillArgs &a, cudaStream_t st) {
+    switch (a.out_dtype) {
+    case 0: return launch_prefill_wide<BF16, 0>(a, st);
+    case 1: return launch_prefill_wide<BF16, 1>(a, st);
+    default: return launch_prefill_wide<BF16, 2>(a, st);
+    }
+}
+
 cudaError_t prefill_launch(const PrefillArgs &a, cudaStream_t st) {
+    if (a.d == 256)
+        return a.bf16 ? launch_prefill_wide_out<true>(a, st) : launch_prefill_wide_out<false>(a, st);
     if (a.d == 64)
         return a.bf16 ? launch_prefill_out<64, true>(a, st) : launch_prefill_out<64, false>(a, st);
     if (a.d == 128)

@@ -172,3 +172,18 @@ def make_append(T: int, Hkv: int, d: int, dtype: str, seed: int = 0, device="cpu
     g = _gen(device, seed + 31)
     dt = DTYPES[dtype]
     return _randn((T, Hkv, d), dt, g, device), _randn((T, Hkv, d), dt, g, device)
+
+
+def quantize_prefill_e4m3(t: dict) -> dict:
+    """Storage conversion of prefill inputs to fp8-E4M3 with one fp32 scale
+    per head of each tensor (amax/448, the same rule as the cache): returns
+    Q, K, V codes and q_scale [B*Hq], k_scale, v_scale [B*Hkv].  Input
+    preparation only."""
+    out = {}
+    for name in ("Q", "K", "V"):
+        x = t[name]
+        B, H = x.shape[:2]
+        codes, scale = quantize_e4m3_per_head(x.reshape(B * H, *x.shape[2:]), 0)
+        out[name] = codes.reshape(x.shape)
+        out[name.lower() + "_scale"] = scale
+    return out

@@ -73,7 +73,7 @@ typedef enum {
  *   K,V [B, Hkv, n_kv, d]   in_dtype
  *   O   [B, Hq,  n_q,  d]   out_dtype (F16, BF16 or F32)
  *   lse [B, Hq,  n_q]       fp32, or NULL
- * d in {64, 128}; Hq % Hkv == 0; causal requires n_q <= n_kv.
+ * d in {64, 128, 256}; Hq % Hkv == 0; causal requires n_q <= n_kv.
  * scale is the factor applied to q.k (1/sqrt(d) for the textbook form).
  * Host-side errors: ATTN_ERR_INVALID for null pointers, non-positive sizes,
  * misalignment, Hq % Hkv != 0, causal with n_q > n_kv; ATTN_ERR_UNSUPPORTED

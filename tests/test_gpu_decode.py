@@ -130,6 +130,35 @@ def test_decode_full_size_sampled_sequences():
     assert torch.isfinite(O).all()
 
 
+SWEEP_DECODE = [W.sweep_decode(G, d, kv) for G, d, kv in
+                ((1, 256, "bf16"), (16, 256, "bf16"), (4, 64, "bf16"), (8, 128, "bf16"),
+                 (1, 256, "e4m3"), (16, 128, "e4m3"))]
+
+
+@pytest.mark.parametrize("spec", SWEEP_DECODE, ids=lambda s: s.name)
+def test_decode_sweep_full_size_sampled_sequences(spec):
+    """The G x d sweep at full size (32 sequences x 8192 tokens, every split
+    busy, several CTAs per SM), checked on sampled sequences."""
+    t = W.make_decode(spec, seed=0, device="cuda")
+    O, lse = attn.decode(t["q"], t["Kc"], t["Vc"], t["block_table"], t["seq_lens"],
+                         max_seq_len=spec.len_hi, k_scale=t["k_scale"], v_scale=t["v_scale"],
+                         out_dtype=torch.float32)
+    assert attn.last_error() == attn.OK
+    pick = [0, 13, spec.num_seqs - 1]
+    bt = t["block_table"].cpu()
+    nblk = (spec.len_hi + spec.block_size - 1) // spec.block_size
+    phys = torch.cat([bt[s, :nblk] for s in pick]).long()
+    Kc, Vc = t["Kc"][phys.cuda()].cpu(), t["Vc"][phys.cuda()].cpu()
+    table = torch.arange(len(pick) * nblk, dtype=torch.int32).view(len(pick), nblk)
+    ks = None if t["k_scale"] is None else t["k_scale"].cpu()
+    vs = None if t["v_scale"] is None else t["v_scale"].cpu()
+    O_ref, lse_ref = oracle.decode_paged(t["q"][pick].cpu(), Kc, Vc, table,
+                                         t["seq_lens"][pick].cpu(), k_scale=ks, v_scale=vs)
+    assert_out(O[pick], O_ref)
+    assert_lse(lse[pick], lse_ref)
+    assert torch.isfinite(O).all()
+
+
 # ----------------------------------------------------------------- append
 
 @pytest.mark.parametrize("kv,d", [("bf16", 128), ("f16", 64), ("e4m3", 128), ("e4m3", 256)])

@@ -32,6 +32,13 @@ SMALL = [
     (1, 2, 1, 129, 129, 128, True, "bf16", "f32"),     # one row past a tile
     (3, 3, 3, 257, 511, 128, False, "bf16", "bf16"),   # tile 1 holds one row
     (1, 16, 1, 256, 256, 64, True, "f16", "bf16"),     # G = 16
+    # head size 256 (one query tile per CTA, 64-key blocks)
+    (1, 1, 1, 64, 64, 256, False, "f16", "f32"),
+    (1, 2, 1, 300, 300, 256, True, "bf16", "f32"),
+    (1, 4, 2, 200, 700, 256, True, "f16", "bf16"),     # n_q < n_kv, bottom-right mask
+    (2, 2, 2, 129, 129, 256, False, "bf16", "bf16"),
+    (1, 2, 2, 1, 1, 256, False, "bf16", "f16"),
+    (1, 8, 1, 1000, 1000, 256, True, "bf16", "f32"),   # MQA, G = 8
 ]
 
 
@@ -91,9 +98,14 @@ def _sample_rows(n_q, rng, k=6):
     return sorted({r for r in base if 0 <= r < n_q})
 
 
-@pytest.mark.parametrize("name", ["gqa-4k", "long-23k", "long-32k"])
+SWEEP_PREFILL = [W.sweep_prefill(G, d) for G, d in ((1, 64), (16, 64), (4, 128), (16, 128),
+                                                   (1, 256), (8, 256), (16, 256))]
+
+
+@pytest.mark.parametrize("name", ["gqa-4k", "long-23k", "long-32k"] +
+                         [s.name for s in SWEEP_PREFILL])
 def test_prefill_full_size_sampled_rows(name):
-    spec = W.PREFILL_WORKLOADS[name]
+    spec = W.PREFILL_WORKLOADS.get(name) or {s.name: s for s in SWEEP_PREFILL}[name]
     t = W.make_prefill(spec, seed=0, device="cuda")
     O, lse = attn.prefill(t["Q"], t["K"], t["V"], spec.causal,
                           out_dtype=W.DTYPES[spec.out_dtype])
