@@ -117,7 +117,7 @@ attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache,
     if (!is16(q_dtype) || !is_out(out_dtype))
         return ATTN_ERR_UNSUPPORTED;
     const bool e4 = kv_dtype == ATTN_E4M3;
-    if (!(kv_dtype == q_dtype || (e4 && q_dtype == ATTN_BF16)))
+    if (!(kv_dtype == q_dtype || e4))
         return ATTN_ERR_UNSUPPORTED;
     if (e4 && (!k_scale || !v_scale))
         return ATTN_ERR_INVALID;

@@ -55,6 +55,16 @@ struct AppendArgs {
     unsigned *err;
 };
 
+enum class TmapElem { BF16, F16, U8 };
+
+// 3-D tensor map (dims innermost first, strides in bytes for dims 1, 2) with
+// the given swizzle span (128, 64 or 0 bytes) and zero fill outside bounds.
+bool make_tmap_3d(CUtensorMap *m, const void *ptr, TmapElem elem, const uint64_t dims[3],
+                  const uint64_t strides_bytes[2], const uint32_t box[3], int swizzle_bytes);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
 // 3-D tensor map over a 16-bit tensor with 128-byte swizzle and zero fill
 // outside the bounds (dims innermost first, strides in bytes for dims 1, 2).
 bool make_tmap_3d_16bit(CUtensorMap *m, const void *ptr, bool bf16, const uint64_t dims[3],

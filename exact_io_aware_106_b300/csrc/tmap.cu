@@ -24,8 +24,8 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-bool make_tmap_3d_16bit(CUtensorMap *m, const void *ptr, bool bf16, const uint64_t dims[3],
-                        const uint64_t strides_bytes[2], const uint32_t box[3]) {
+bool make_tmap_3d(CUtensorMap *m, const void *ptr, TmapElem elem, const uint64_t dims[3],
+                  const uint64_t strides_bytes[2], const uint32_t box[3], int swizzle_bytes) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc)
         return false;
@@ -33,11 +33,37 @@ bool make_tmap_3d_16bit(CUtensorMap *m, const void *ptr, bool bf16, const uint64
     cuuint64_t s[2] = {strides_bytes[0], strides_bytes[1]};
     cuuint32_t b[3] = {box[0], box[1], box[2]};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                     3, const_cast<void *>(ptr), d, s, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUtensorMapDataType dt = elem == TmapElem::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : elem == TmapElem::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
+    CUresult r = enc(m, dt, 3, const_cast<void *>(ptr), d, s, b, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_3d_16bit(CUtensorMap *m, const void *ptr, bool bf16, const uint64_t dims[3],
+                        const uint64_t strides_bytes[2], const uint32_t box[3]) {
+    return make_tmap_3d(m, ptr, bf16 ? TmapElem::BF16 : TmapElem::F16, dims, strides_bytes, box,
+                        128);
+}
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
 }
 
 } // namespace attn

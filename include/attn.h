@@ -95,7 +95,7 @@ ATTN_API size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d,
  *   Kcache,
  *   Vcache   [num_blocks, Hkv, block_size, d]          kv_dtype: same as
  *            q_dtype, or E4M3 with k_scale/v_scale [Hkv] fp32 (dequantised
- *            value = code * scale)
+ *            value = code * scale; q may then be F16 or BF16)
  *   block_table [num_seqs, max_blocks_per_seq] int32: token t of sequence s
  *            is slot t % block_size of block block_table[s][t / block_size]
  *   seq_lens [num_seqs] int32, each in [0, max_seq_len]
