@@ -45,7 +45,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
-                                   i32, i32, vp]
+                                   i32, i32, vp, vp, vp, vp]
         L.attn_prefill.restype = i32
         L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.attn_decode_workspace_bytes.restype = sz
@@ -106,16 +106,19 @@ def last_error(stream=None) -> int:
 
 
 def prefill(Q, K, V, causal: bool, scale: float | None = None, out_dtype=None, O=None,
-            lse=None, want_lse: bool = True, stream=None):
+            lse=None, want_lse: bool = True, q_scale=None, k_scale=None, v_scale=None,
+            stream=None):
     """O = softmax(scale Q K^T [causal]) V for Q [B,Hq,n_q,d], K/V [B,Hkv,n_kv,d].
-    Returns (O, lse) with lse [B,Hq,n_q] fp32 (None if want_lse is False)."""
-    _cuda(Q, K, V)
+    E4M3 inputs take per-head fp32 scales q_scale [B*Hq], k_scale/v_scale
+    [B*Hkv] (value = code * scale).  Returns (O, lse) with lse [B,Hq,n_q]
+    fp32 (None if want_lse is False)."""
+    _cuda(Q, K, V, q_scale, k_scale, v_scale)
     B, Hq, nq, d = Q.shape
     _, Hkv, nkv, _ = K.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out_dtype is None:
-        out_dtype = Q.dtype
+        out_dtype = torch.bfloat16 if Q.dtype == torch.float8_e4m3fn else Q.dtype
     if O is None:
         O = torch.empty((B, Hq, nq, d), dtype=out_dtype, device=Q.device)
     if lse is None and want_lse:
@@ -123,7 +126,7 @@ def prefill(Q, K, V, causal: bool, scale: float | None = None, out_dtype=None, O
     _cuda(O, lse)
     st = lib().attn_prefill(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), B, Hq, Hkv, nq, nkv,
                             d, int(bool(causal)), float(scale), _DT[Q.dtype], _DT[O.dtype],
-                            _stream(stream))
+                            _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _stream(stream))
     _check("attn_prefill", st)
     return O, lse
 

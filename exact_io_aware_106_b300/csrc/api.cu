@@ -61,7 +61,8 @@ int attn_last_launch_count(void) { return t_last_launches; }
 
 attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
                          int Hq, int Hkv, int n_q, int n_kv, int d, int causal, float scale,
-                         attn_dtype in_dtype, attn_dtype out_dtype, void *stream) {
+                         attn_dtype in_dtype, attn_dtype out_dtype, const float *q_scale,
+                         const float *k_scale, const float *v_scale, void *stream) {
     t_last_launches = 0;
     if (!Q || !K || !V || !O)
         return ATTN_ERR_INVALID;
@@ -74,8 +75,12 @@ attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, f
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
         (lse && !aligned(lse, 4)))
         return ATTN_ERR_INVALID;
-    if (!is16(in_dtype) || !is_out(out_dtype) || (d != 64 && d != 128 && d != 256))
+    const bool e4 = in_dtype == ATTN_E4M3;
+    if ((!is16(in_dtype) && !e4) || !is_out(out_dtype) || (d != 64 && d != 128 && d != 256))
         return ATTN_ERR_UNSUPPORTED;
+    if (e4 && (!q_scale || !k_scale || !v_scale || !aligned(q_scale, 4) ||
+               !aligned(k_scale, 4) || !aligned(v_scale, 4)))
+        return ATTN_ERR_INVALID;
     const long long nqb = (n_q + 127) / 128;
     if (nqb * B * Hq > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
@@ -83,7 +88,9 @@ attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, f
     if (!err)
         return ATTN_ERR_CUDA;
     attn::PrefillArgs a{Q, K, V, O, lse, B, Hq, Hkv, n_q, n_kv, d, causal ? 1 : 0, scale,
-                        in_dtype == ATTN_BF16, out_code(out_dtype), err};
+                        in_dtype == ATTN_BF16, e4, out_code(out_dtype),
+                        e4 ? q_scale : nullptr, e4 ? k_scale : nullptr,
+                        e4 ? v_scale : nullptr, err};
     if (attn::prefill_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     t_last_launches = 1;

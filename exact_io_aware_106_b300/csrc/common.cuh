@@ -168,6 +168,17 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc], 8-bit operands (kind::f8f6f4;
+// the instruction descriptor's A/B format fields are 0 for E4M3).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor, kind::f16 with fp32 accumulation.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 f16,
 //   1 bf16), 15/16 A/B major (0 = K-major, 1 = MN-major), 17-22 N>>3,
@@ -193,6 +204,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Shared-memory matrix descriptor for a K-major operand whose rows are
+// `row_bytes` (128 or 64) long and swizzled over that span by TMA: 8-row
+// atoms SBO = 8 * row_bytes apart; layout 2 = 128-byte, 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr, int row_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1) << 16; // leading byte offset (unused when swizzled)
+    d |= static_cast<uint64_t>(((8u * row_bytes) >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(row_bytes == 128 ? 2 : 4) << 61;
     return d;
 }
 
@@ -341,6 +365,37 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
                      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
                      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of 16-byte chunk `ch` of row `row` in a TMA-swizzled panel
+// whose rows are PW bytes (128: chunk ^= row mod 8; 64: chunk ^= row/2 mod 4).
+template <int PW>
+__device__ __forceinline__ uint32_t swz_offset(int row, int ch) {
+    if constexpr (PW == 128)
+        return static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
+    else
+        return static_cast<uint32_t>(row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Two E4M3 codes (low byte first) widened exactly to f16x2.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(v & 0xFFFFu)));
+    return r;
 }
 
 // ------------------------------------------------------------- numerics

@@ -18,7 +18,11 @@ struct PrefillArgs {
     int B, Hq, Hkv, n_q, n_kv, d, causal;
     float scale;
     bool bf16;
+    bool e4m3;     // E4M3 inputs with per-head scales
     int out_dtype; // 0 f16, 1 bf16, 2 f32
+    const float *q_scale;
+    const float *k_scale;
+    const float *v_scale;
     unsigned *err;
 };
 

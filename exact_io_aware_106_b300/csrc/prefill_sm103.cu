@@ -14,8 +14,8 @@
 //
 // B300 mapping (one CTA = 2 query tiles of 128 rows = 256 rows of one head):
 //   warp 8      TMA producer: Q tiles once, then K_j / V_j through rings of
-//               shared-memory stages (128-byte swizzle, one 3-D tensor map
-//               per operand so tails read zeros).
+//               shared-memory stages (swizzled, one 3-D tensor map per
+//               operand so tails read zeros).
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory
 //               (tcgen05.mma, A and B from shared memory), then
 //               O_t += P_t V_j with P_t read from tensor memory.
@@ -24,6 +24,7 @@
 //               on the SFU, row sum, P packed to 16-bit back into tensor
 //               memory over the consumed scores, O rescaled in tensor memory
 //               when the reference max moves, final O / l and lse.
+//   warp 10     (E4M3 inputs only) widens each V tile to f16 on chip.
 // The two tiles ping-pong: while warpgroup 0 turns S_0 into P_0, the tensor
 // core computes O_1 += P_1 V_j and S_1 for the next block, and vice versa.
 //
@@ -33,6 +34,12 @@
 // the rounding residual P - P_hi is stored in the next 64 columns and
 // multiplied in as a second MMA, so that the 16-bit rounding of P does not
 // reach the output where too few terms average it out.
+//
+// E4M3 inputs (one fp32 scale per head of Q, K and V): S = Q K^T runs on the
+// 8-bit tensor cores (kind::f8f6f4, both operands K-major as TMA lands them);
+// P V runs in f16 -- the converter warp widens the E4M3 V tile exactly into
+// the same swizzled f16 layout that 16-bit inputs arrive in.  The scales
+// fold into the score factor (q_scale * k_scale) and the epilogue (v_scale).
 //
 // Scores are in the log2 domain (c = scale * log2 e).  The reference max
 // m is only moved when a block's max exceeds it by more than 8, so p stays
@@ -49,36 +56,51 @@ namespace pf {
 constexpr int BM = 128;      // query rows per tile
 constexpr int NT = 2;        // query tiles per CTA
 constexpr int BN = 128;      // keys per block
-constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kConvWarp = 10;
 constexpr int kSplitKeys = 512; // rows seeing fewer keys carry the P residual
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+template <int D, bool F8>
 struct Cfg {
-    static constexpr int PANELS = D / 64;                // 128-byte column panels
-    static constexpr int Q_TILE_BYTES = BM * D * 2;
-    static constexpr int KV_BYTES = BN * D * 2;
-    static constexpr int NK = D == 64 ? 3 : 2;           // K stages
-    static constexpr int NV = D == 64 ? 3 : 2;           // V stages
+    static constexpr int EB = F8 ? 1 : 2;                   // bytes per Q/K element
+    static constexpr int PW = D * EB < 128 ? D * EB : 128;  // Q/K row bytes per panel = swizzle span
+    static constexpr int QK_PANELS = D * EB / PW;
+    static constexpr int Q_TILE_BYTES = BM * D * EB;
+    static constexpr int K_BYTES = BN * D * EB;
+    static constexpr int V_BYTES = BN * D * 2;              // 16-bit V operand stage
+    static constexpr int VS_BYTES = BN * D;                 // E4M3 V staging
+    static constexpr int NK = (F8 || D == 64) ? 3 : 2;      // K stages
+    static constexpr int NV = D == 64 ? 3 : 2;              // V stages
+    static constexpr int NVS = F8 ? 2 : 0;                  // E4M3 V staging buffers
+    static constexpr int THREADS = F8 ? 352 : 320;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NT * Q_TILE_BYTES;
-    static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
-    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 * NT + 2;
+    static constexpr int OFF_V = OFF_K + NK * K_BYTES;
+    static constexpr int OFF_VS = OFF_V + NV * V_BYTES;
+    static constexpr int OFF_BAR = OFF_VS + NVS * VS_BYTES;
+    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 * NVS + 2 * NT + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024; // + alignment slack
     __host__ __device__ static constexpr int S_COL(int t) { return t * BN; }
     __host__ __device__ static constexpr int O_COL(int t) { return NT * BN + t * D; }
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(NT * BN + NT * D <= 512, "tensor memory budget");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
 struct Shape {
     int B, Hq, Hkv, G, n_q, n_kv, causal, nqb;
     float c;     // scale * log2(e)
     float scale; // for reference only
+};
+
+// Per-head scales of E4M3 inputs (null for 16-bit inputs).
+struct Scales {
+    const float *q;
+    const float *k;
+    const float *v;
 };
 
 __device__ __forceinline__ int tile_blocks(const Shape &sh, int q0, int t) {
@@ -99,19 +121,19 @@ __device__ __forceinline__ bool tile_split(const Shape &sh, int q0, int t) {
     return keys < kSplitKeys;
 }
 
-// p = 2^(s*c - m) for the 128 scores of this thread's row, packed to 16 bits
-// and stored over the consumed scores (P_hi in columns [0,64) of the S
-// tile; with SPLIT, the rounding residual p - P_hi in columns [64,128)).
+// p = 2^(s*c - m) for the NB scores of this thread's row, packed to 16 bits
+// and stored over the consumed scores (P_hi in columns [0, NB/2) of the S
+// tile; with SPLIT, the rounding residual p - P_hi in columns [NB/2, NB)).
 // Returns the row sum of p (fp32, eight independent partial sums).
-template <bool BF16, bool SPLIT>
-__device__ __forceinline__ float exp_pack_store(const float (&s)[BN], float c, float neg,
+template <int NB, bool BF16, bool SPLIT>
+__device__ __forceinline__ float exp_pack_store(const float (&s)[NB], float c, float neg,
                                                 uint32_t tS) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         acc[i] = 0.f;
 #pragma unroll
-    for (int ch = 0; ch < BN / 32; ++ch) {
+    for (int ch = 0; ch < NB / 32; ++ch) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -125,18 +147,38 @@ __device__ __forceinline__ float exp_pack_store(const float (&s)[BN], float c, f
         }
         tmem_st16(tS + ch * 16, hi);
         if constexpr (SPLIT)
-            tmem_st16(tS + 64 + ch * 16, lo);
+            tmem_st16(tS + NB / 2 + ch * 16, lo);
     }
     return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
-template <int D, bool BF16, int OUT>
-__global__ void __launch_bounds__(kThreads, 1)
+// Widen one E4M3 V tile [ROWS][D] (panels of PW-byte rows, PW-byte swizzle)
+// into the f16 operand layout (panels of 64 elements = 128-byte rows,
+// 128-byte swizzle) -- the layout 16-bit V tiles arrive in by TMA.
+template <int D, int ROWS, int PW>
+__device__ __forceinline__ void widen_v_tile(uint32_t src, uint32_t dst, int lane) {
+    constexpr int CPR = D / 16; // 16-byte source chunks per row
+#pragma unroll 4
+    for (int i = lane; i < ROWS * CPR; i += 32) {
+        const int r = i / CPR, c = i % CPR;
+        const uint4 v = lds_v4(src + (c * 16 / PW) * (ROWS * PW) +
+                               swz_offset<PW>(r, (c * 16 % PW) >> 4));
+        const uint32_t pb = dst + (c / 4) * (ROWS * 128);
+        sts_v4(pb + swz_offset<128>(r, 2 * (c % 4)), e4m3x2_to_f16x2(v.x),
+               e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y), e4m3x2_to_f16x2(v.y >> 16));
+        sts_v4(pb + swz_offset<128>(r, 2 * (c % 4) + 1), e4m3x2_to_f16x2(v.z),
+               e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w), e4m3x2_to_f16x2(v.w >> 16));
+    }
+}
+
+template <int D, bool BF16, bool F8, int OUT>
+__global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, void *__restrict__ O,
-                   float *__restrict__ lse, const Shape sh, unsigned *err) {
-    using C = Cfg<D>;
+                   float *__restrict__ lse, const Shape sh, const Scales sc, unsigned *err) {
+    using C = Cfg<D, F8>;
+    constexpr bool PB = F8 ? false : BF16; // format of P and of the V operand
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (128-byte swizzle atoms repeat every 1 KB)
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -146,15 +188,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = base_s + C::OFF_Q;
     const uint32_t sK = base_s + C::OFF_K;
     const uint32_t sV = base_s + C::OFF_V;
+    const uint32_t sVS = base_s + C::OFF_VS;
     const uint32_t bar0 = base_s + C::OFF_BAR;
     const uint32_t b_qfull = bar0;
     auto b_kfull = [&](int i) { return bar0 + 8u * (1 + i); };
     auto b_kempty = [&](int i) { return bar0 + 8u * (1 + C::NK + i); };
     auto b_vfull = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + i); };
     auto b_vempty = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + C::NV + i); };
-    auto b_sfull = [&](int t) { return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + t); };
-    auto b_pfull = [&](int t) { return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + NT + t); };
-    const uint32_t b_ofull = bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + 2 * NT);
+    auto b_vsfull = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + i); };
+    auto b_vsempty = [&](int i) {
+        return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + C::NVS + i);
+    };
+    constexpr int SB = 1 + 2 * C::NK + 2 * C::NV + 2 * C::NVS;
+    auto b_sfull = [&](int t) { return bar0 + 8u * (SB + t); };
+    auto b_pfull = [&](int t) { return bar0 + 8u * (SB + NT + t); };
+    const uint32_t b_ofull = bar0 + 8u * (SB + 2 * NT);
     const uint32_t b_drain = b_ofull + 8u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
@@ -186,6 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_vfull(i), 1);
             mbar_init(b_vempty(i), 1);
         }
+        for (int i = 0; i < C::NVS; ++i) {
+            mbar_init(b_vsfull(i), 1);
+            mbar_init(b_vsempty(i), 1);
+        }
         for (int t = 0; t < NT; ++t) {
             mbar_init(b_sfull(t), 1);
             mbar_init(b_pfull(t), 4);
@@ -211,49 +263,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ================================================= TMA producer
         if (lane == 0) {
+            constexpr int XP = C::PW / C::EB; // elements per Q/K panel row
             int ntiles = 0;
             for (int t = 0; t < NT; ++t)
                 ntiles += nb[t] > 0;
             mbar_arrive_expect_tx(b_qfull, ntiles * C::Q_TILE_BYTES);
             for (int t = 0; t < NT; ++t)
                 if (nb[t] > 0)
-                    for (int p = 0; p < C::PANELS; ++p)
-                        tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * 128, &tm_q, b_qfull,
-                                    p * 64, q0 + t * BM, bh);
+                    for (int p = 0; p < C::QK_PANELS; ++p)
+                        tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q, b_qfull,
+                                    p * XP, q0 + t * BM, bh);
             int k_issued = 0, v_issued = 0;
             for (int j = 0; j < nb_max; ++j) {
                 const int ks = j % C::NK;
                 if (j >= C::NK &&
                     !mbar_wait(b_kempty(ks), ((j / C::NK) - 1) & 1, abort_flag, err))
                     break;
-                mbar_arrive_expect_tx(b_kfull(ks), C::KV_BYTES);
-                for (int p = 0; p < C::PANELS; ++p)
-                    tma_load_3d(sK + ks * C::KV_BYTES + p * BN * 128, &tm_k, b_kfull(ks), p * 64,
-                                j * BN, bkv);
+                mbar_arrive_expect_tx(b_kfull(ks), C::K_BYTES);
+                for (int p = 0; p < C::QK_PANELS; ++p)
+                    tma_load_3d(sK + ks * C::K_BYTES + p * BN * C::PW, &tm_k, b_kfull(ks),
+                                p * XP, j * BN, bkv);
                 k_issued = j + 1;
-                const int vs = j % C::NV;
-                if (j >= C::NV &&
-                    !mbar_wait(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
-                    break;
-                mbar_arrive_expect_tx(b_vfull(vs), C::KV_BYTES);
-                for (int p = 0; p < C::PANELS; ++p)
-                    tma_load_3d(sV + vs * C::KV_BYTES + p * BN * 128, &tm_v, b_vfull(vs), p * 64,
-                                j * BN, bkv);
+                if constexpr (F8) {
+                    // E4M3 V into staging; the converter warp fills the V stage
+                    const int vs = j % C::NVS;
+                    if (j >= C::NVS &&
+                        !mbar_wait(b_vsempty(vs), ((j / C::NVS) - 1) & 1, abort_flag, err))
+                        break;
+                    mbar_arrive_expect_tx(b_vsfull(vs), C::VS_BYTES);
+                    for (int p = 0; p < C::QK_PANELS; ++p)
+                        tma_load_3d(sVS + vs * C::VS_BYTES + p * BN * C::PW, &tm_v,
+                                    b_vsfull(vs), p * XP, j * BN, bkv);
+                } else {
+                    const int vs = j % C::NV;
+                    if (j >= C::NV &&
+                        !mbar_wait(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
+                        break;
+                    mbar_arrive_expect_tx(b_vfull(vs), C::V_BYTES);
+                    for (int p = 0; p < D / 64; ++p)
+                        tma_load_3d(sV + vs * C::V_BYTES + p * BN * 128, &tm_v, b_vfull(vs),
+                                    p * 64, j * BN, bkv);
+                }
                 v_issued = j + 1;
             }
             if (*abort_flag) { // let in-flight copies land before the CTA exits
                 mbar_wait_drain(b_qfull, 0);
                 for (int u = max(0, k_issued - C::NK); u < k_issued; ++u)
                     mbar_wait_drain(b_kfull(u % C::NK), (u / C::NK) & 1);
-                for (int u = max(0, v_issued - C::NV); u < v_issued; ++u)
-                    mbar_wait_drain(b_vfull(u % C::NV), (u / C::NV) & 1);
+                if constexpr (F8) {
+                    for (int u = max(0, v_issued - C::NVS); u < v_issued; ++u)
+                        mbar_wait_drain(b_vsfull(u % C::NVS), (u / C::NVS) & 1);
+                } else {
+                    for (int u = max(0, v_issued - C::NV); u < v_issued; ++u)
+                        mbar_wait_drain(b_vfull(u % C::NV), (u / C::NV) & 1);
+                }
+            }
+        }
+    } else if (warp == kConvWarp) {
+        // ================================================= V widening (E4M3)
+        if constexpr (F8) {
+            for (int j = 0; j < nb_max; ++j) {
+                const int ss = j % C::NVS, vs = j % C::NV;
+                if (!mbar_wait(b_vsfull(ss), (j / C::NVS) & 1, abort_flag, err))
+                    break;
+                if (j >= C::NV && !mbar_wait(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
+                    break;
+                widen_v_tile<D, BN, C::PW>(sVS + ss * C::VS_BYTES, sV + vs * C::V_BYTES, lane);
+                fence_proxy_async_smem(); // generic writes -> tensor-core reads
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(b_vsempty(ss));
+                    mbar_arrive(b_vfull(vs));
+                }
             }
         }
     } else if (warp == kMmaWarp) {
         // ================================================= MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_f16(BM, BN, BF16, false, false);
-            constexpr uint32_t idesc_pv = idesc_f16(BM, D, BF16, false, true);
+            constexpr uint32_t idesc_qk = idesc_f16(BM, BN, F8 ? false : BF16, false, false);
+            constexpr uint32_t idesc_pv = idesc_f16(BM, D, PB, false, true);
             bool split[NT];
 #pragma unroll
             for (int t = 0; t < NT; ++t)
@@ -261,17 +349,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             auto issue_qk = [&](int t, int ks) {
                 const uint32_t qa = sQ + t * C::Q_TILE_BYTES;
-                const uint32_t kb = sK + ks * C::KV_BYTES;
+                const uint32_t kb = sK + ks * C::K_BYTES;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * (BM * 128) + (k % 4) * 32;
-                    const uint32_t offb = (k / 4) * (BN * 128) + (k % 4) * 32;
-                    mma_ss(tmem + C::S_COL(t), sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(kb + offb, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+                for (int k = 0; k < D * C::EB / 32; ++k) { // 32-byte K steps
+                    const uint32_t byte = k * 32;
+                    const uint32_t offa = (byte / C::PW) * (BM * C::PW) + byte % C::PW;
+                    const uint32_t offb = (byte / C::PW) * (BN * C::PW) + byte % C::PW;
+                    const uint64_t ad = sdesc_kmajor(qa + offa, C::PW);
+                    const uint64_t bd = sdesc_kmajor(kb + offb, C::PW);
+                    if constexpr (F8)
+                        mma_ss_f8(tmem + C::S_COL(t), ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+                    else
+                        mma_ss(tmem + C::S_COL(t), ad, bd, idesc_qk, k > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int vs, bool first) {
-                const uint32_t vb = sV + vs * C::KV_BYTES;
+                const uint32_t vb = sV + vs * C::V_BYTES;
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
@@ -361,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int off = sh.n_kv - sh.n_q;
         const bool split = tile_split(sh, q0, t);
         const int r0 = q0 + t * BM;
-        const float c = sh.c;
+        const float c = F8 ? sh.c * sc.q[bh] * sc.k[bkv] : sh.c;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
 
@@ -407,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float alpha =
                 (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
             const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
-            const float sum = split ? exp_pack_store<BF16, true>(s, c, neg, tS)
-                                    : exp_pack_store<BF16, false>(s, c, neg, tS);
+            const float sum = split ? exp_pack_store<BN, PB, true>(s, c, neg, tS)
+                                    : exp_pack_store<BN, PB, false>(s, c, neg, tS);
             // O_t holds the sum over earlier blocks (their MMAs completed
             // before S_t of this block was produced); rescale it in place.
             if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
@@ -436,7 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nb[t] > 0) {
             // ---- epilogue: O = u / l, lse = ln(sum exp(scale * s))
             const bool row_ok = row_g < sh.n_q;
-            const float inv = (ok && l > 0.f) ? 1.0f / l : 0.f;
+            const float vsc = F8 ? sc.v[bkv] : 1.0f;
+            const float inv = (ok && l > 0.f) ? vsc / l : 0.f;
             const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row_g) * D;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
@@ -490,9 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the overlap comes from double-buffering S over consecutive key blocks:
 // while the softmax warpgroup turns S_(j mod 2) into P, the tensor core
 // computes O += P_(j-1) V_(j-1) and S_(j+1).  Key blocks are 64 wide so that
-// two K and two V stages fit next to the 64 KB Q tile.
+// two K and two V stages fit next to the Q tile.
 //   warp 4      TMA producer (Q once, K / V rings of 2 stages)
 //   warp 5      MMA issuer (one thread)
+//   warp 6      (E4M3 inputs only) widens each V tile to f16
 //   warps 0-3   softmax, one thread per row; the epilogue
 // Tensor memory: S_0 [0,64), S_1 [64,128), O [128, 384).  A block that moves
 // the reference max rescales O only after the previous block's P V product
@@ -502,21 +597,34 @@ namespace pfw {
 constexpr int D = 256;
 constexpr int BM = 128;
 constexpr int BN = 64;
-constexpr int PANELS = D / 64;
-constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
+constexpr int kConvWarp = 6;
 constexpr int NK = 2, NV = 2;
-constexpr int Q_BYTES = BM * D * 2;     // 64 KB
-constexpr int KV_BYTES = BN * D * 2;    // 32 KB
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_BYTES;
-constexpr int OFF_V = OFF_K + NK * KV_BYTES;
-constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
-// qfull, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], pfull[2], odone, ofull, drain
-constexpr int NBAR = 1 + 2 * NK + 2 * NV + 4 + 3;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int SMEM = OFF_MISC + 64 + 1024;
+
+template <bool F8>
+struct Cfg {
+    static constexpr int EB = F8 ? 1 : 2;
+    static constexpr int PW = 128;
+    static constexpr int QK_PANELS = D * EB / PW;
+    static constexpr int Q_BYTES = BM * D * EB;
+    static constexpr int K_BYTES = BN * D * EB;
+    static constexpr int V_BYTES = BN * D * 2;
+    static constexpr int VS_BYTES = BN * D;
+    static constexpr int NVS = F8 ? 2 : 0;
+    static constexpr int THREADS = F8 ? 224 : 192;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + NK * K_BYTES;
+    static constexpr int OFF_VS = OFF_V + NV * V_BYTES;
+    static constexpr int OFF_BAR = OFF_VS + NVS * VS_BYTES;
+    // qfull, kfull/kempty, vfull/vempty, vsfull/vsempty, sfull[2], pfull[2],
+    // odone, ofull, drain
+    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 * NVS + 4 + 3;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 64 + 1024;
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
 constexpr int S_COL0 = 0, O_COL = 2 * BN;
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(O_COL + D <= 512, "tensor memory budget");
@@ -529,57 +637,37 @@ __device__ __forceinline__ int tile_blocks(const pf::Shape &sh, int r0) {
     return min(nkb, (r_last + (sh.n_kv - sh.n_q)) / BN + 1);
 }
 
-template <bool BF16, bool SPLIT>
-__device__ __forceinline__ float exp_pack_store64(const float (&s)[BN], float c, float neg,
-                                                  uint32_t tS) {
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        acc[i] = 0.f;
-#pragma unroll
-    for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(s[ch * 32 + 2 * i], c, neg));
-            const float p1 = ex2(fmaf(s[ch * 32 + 2 * i + 1], c, neg));
-            acc[(2 * i) & 7] += p0;
-            acc[(2 * i + 1) & 7] += p1;
-            hi[i] = pack2<BF16>(p0, p1);
-            if constexpr (SPLIT)
-                lo[i] = pack2<BF16>(p0 - lo16<BF16>(hi[i]), p1 - hi16<BF16>(hi[i]));
-        }
-        tmem_st16(tS + ch * 16, hi);
-        if constexpr (SPLIT)
-            tmem_st16(tS + BN / 2 + ch * 16, lo);
-    }
-    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-}
-
-template <bool BF16, int OUT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool BF16, bool F8, int OUT>
+__global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
     prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, void *__restrict__ O,
-                        float *__restrict__ lse, const pf::Shape sh, unsigned *err) {
+                        float *__restrict__ lse, const pf::Shape sh, const pf::Scales sc,
+                        unsigned *err) {
+    using C = Cfg<F8>;
+    constexpr bool PB = F8 ? false : BF16;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_s - raw_s);
-    const uint32_t sQ = base_s + OFF_Q, sK = base_s + OFF_K, sV = base_s + OFF_V;
-    const uint32_t bar0 = base_s + OFF_BAR;
+    const uint32_t sQ = base_s + C::OFF_Q, sK = base_s + C::OFF_K, sV = base_s + C::OFF_V;
+    const uint32_t sVS = base_s + C::OFF_VS;
+    const uint32_t bar0 = base_s + C::OFF_BAR;
     const uint32_t b_qfull = bar0;
     auto b_kfull = [&](int i) { return bar0 + 8u * (1 + i); };
     auto b_kempty = [&](int i) { return bar0 + 8u * (1 + NK + i); };
     auto b_vfull = [&](int i) { return bar0 + 8u * (1 + 2 * NK + i); };
     auto b_vempty = [&](int i) { return bar0 + 8u * (1 + 2 * NK + NV + i); };
-    auto b_sfull = [&](int b) { return bar0 + 8u * (1 + 2 * NK + 2 * NV + b); };
-    auto b_pfull = [&](int b) { return bar0 + 8u * (1 + 2 * NK + 2 * NV + 2 + b); };
-    const uint32_t b_odone = bar0 + 8u * (1 + 2 * NK + 2 * NV + 4);
+    auto b_vsfull = [&](int i) { return bar0 + 8u * (1 + 2 * NK + 2 * NV + i); };
+    auto b_vsempty = [&](int i) { return bar0 + 8u * (1 + 2 * NK + 2 * NV + C::NVS + i); };
+    constexpr int SB = 1 + 2 * NK + 2 * NV + 2 * C::NVS;
+    auto b_sfull = [&](int b) { return bar0 + 8u * (SB + b); };
+    auto b_pfull = [&](int b) { return bar0 + 8u * (SB + 2 + b); };
+    const uint32_t b_odone = bar0 + 8u * (SB + 4);
     const uint32_t b_ofull = b_odone + 8u;
     const uint32_t b_drain = b_ofull + 8u;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + OFF_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + OFF_MISC + 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = sh.B * sh.Hq;
@@ -600,6 +688,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < NV; ++i) {
             mbar_init(b_vfull(i), 1);
             mbar_init(b_vempty(i), 1);
+        }
+        for (int i = 0; i < C::NVS; ++i) {
+            mbar_init(b_vsfull(i), 1);
+            mbar_init(b_vsempty(i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_sfull(i), 1);
@@ -627,55 +719,96 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ================================================= TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(b_qfull, Q_BYTES);
-            for (int p = 0; p < PANELS; ++p)
-                tma_load_3d(sQ + p * BM * 128, &tm_q, b_qfull, p * 64, r0, bh);
+            constexpr int XP = C::PW / C::EB;
+            mbar_arrive_expect_tx(b_qfull, C::Q_BYTES);
+            for (int p = 0; p < C::QK_PANELS; ++p)
+                tma_load_3d(sQ + p * BM * C::PW, &tm_q, b_qfull, p * XP, r0, bh);
             int k_issued = 0, v_issued = 0;
             for (int j = 0; j < nb; ++j) {
                 const int ks = j % NK;
                 if (j >= NK && !mbar_wait(b_kempty(ks), ((j / NK) - 1) & 1, abort_flag, err))
                     break;
-                mbar_arrive_expect_tx(b_kfull(ks), KV_BYTES);
-                for (int p = 0; p < PANELS; ++p)
-                    tma_load_3d(sK + ks * KV_BYTES + p * BN * 128, &tm_k, b_kfull(ks), p * 64,
-                                j * BN, bkv);
+                mbar_arrive_expect_tx(b_kfull(ks), C::K_BYTES);
+                for (int p = 0; p < C::QK_PANELS; ++p)
+                    tma_load_3d(sK + ks * C::K_BYTES + p * BN * C::PW, &tm_k, b_kfull(ks),
+                                p * XP, j * BN, bkv);
                 k_issued = j + 1;
-                const int vs = j % NV;
-                if (j >= NV && !mbar_wait(b_vempty(vs), ((j / NV) - 1) & 1, abort_flag, err))
-                    break;
-                mbar_arrive_expect_tx(b_vfull(vs), KV_BYTES);
-                for (int p = 0; p < PANELS; ++p)
-                    tma_load_3d(sV + vs * KV_BYTES + p * BN * 128, &tm_v, b_vfull(vs), p * 64,
-                                j * BN, bkv);
+                if constexpr (F8) {
+                    const int vs = j % C::NVS;
+                    if (j >= C::NVS &&
+                        !mbar_wait(b_vsempty(vs), ((j / C::NVS) - 1) & 1, abort_flag, err))
+                        break;
+                    mbar_arrive_expect_tx(b_vsfull(vs), C::VS_BYTES);
+                    for (int p = 0; p < C::QK_PANELS; ++p)
+                        tma_load_3d(sVS + vs * C::VS_BYTES + p * BN * C::PW, &tm_v,
+                                    b_vsfull(vs), p * XP, j * BN, bkv);
+                } else {
+                    const int vs = j % NV;
+                    if (j >= NV && !mbar_wait(b_vempty(vs), ((j / NV) - 1) & 1, abort_flag, err))
+                        break;
+                    mbar_arrive_expect_tx(b_vfull(vs), C::V_BYTES);
+                    for (int p = 0; p < D / 64; ++p)
+                        tma_load_3d(sV + vs * C::V_BYTES + p * BN * 128, &tm_v, b_vfull(vs),
+                                    p * 64, j * BN, bkv);
+                }
                 v_issued = j + 1;
             }
             if (*abort_flag) { // let in-flight copies land before the CTA exits
                 mbar_wait_drain(b_qfull, 0);
                 for (int u = max(0, k_issued - NK); u < k_issued; ++u)
                     mbar_wait_drain(b_kfull(u % NK), (u / NK) & 1);
-                for (int u = max(0, v_issued - NV); u < v_issued; ++u)
-                    mbar_wait_drain(b_vfull(u % NV), (u / NV) & 1);
+                if constexpr (F8) {
+                    for (int u = max(0, v_issued - C::NVS); u < v_issued; ++u)
+                        mbar_wait_drain(b_vsfull(u % C::NVS), (u / C::NVS) & 1);
+                } else {
+                    for (int u = max(0, v_issued - NV); u < v_issued; ++u)
+                        mbar_wait_drain(b_vfull(u % NV), (u / NV) & 1);
+                }
+            }
+        }
+    } else if (warp == kConvWarp) {
+        // ================================================= V widening (E4M3)
+        if constexpr (F8) {
+            for (int j = 0; j < nb; ++j) {
+                const int ss = j % C::NVS, vs = j % NV;
+                if (!mbar_wait(b_vsfull(ss), (j / C::NVS) & 1, abort_flag, err))
+                    break;
+                if (j >= NV && !mbar_wait(b_vempty(vs), ((j / NV) - 1) & 1, abort_flag, err))
+                    break;
+                pf::widen_v_tile<D, BN, C::PW>(sVS + ss * C::VS_BYTES, sV + vs * C::V_BYTES,
+                                               lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(b_vsempty(ss));
+                    mbar_arrive(b_vfull(vs));
+                }
             }
         }
     } else if (warp == kMmaWarp) {
         // ================================================= MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_f16(BM, BN, BF16, false, false);
-            constexpr uint32_t idesc_pv = idesc_f16(BM, D, BF16, false, true);
+            constexpr uint32_t idesc_qk = idesc_f16(BM, BN, F8 ? false : BF16, false, false);
+            constexpr uint32_t idesc_pv = idesc_f16(BM, D, PB, false, true);
             const bool split = (sh.causal ? (r0 + (sh.n_kv - sh.n_q) + 1) : sh.n_kv) <
                                pf::kSplitKeys;
             auto issue_qk = [&](int buf, int ks) {
-                const uint32_t kb = sK + ks * KV_BYTES;
+                const uint32_t kb = sK + ks * C::K_BYTES;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t offa = (k / 4) * (BM * 128) + (k % 4) * 32;
-                    const uint32_t offb = (k / 4) * (BN * 128) + (k % 4) * 32;
-                    mma_ss(tmem + S_COL0 + buf * BN, sdesc_sw128(sQ + offa, 16, 1024),
-                           sdesc_sw128(kb + offb, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+                for (int k = 0; k < D * C::EB / 32; ++k) {
+                    const uint32_t byte = k * 32;
+                    const uint32_t offa = (byte / C::PW) * (BM * C::PW) + byte % C::PW;
+                    const uint32_t offb = (byte / C::PW) * (BN * C::PW) + byte % C::PW;
+                    const uint64_t ad = sdesc_kmajor(sQ + offa, C::PW);
+                    const uint64_t bd = sdesc_kmajor(kb + offb, C::PW);
+                    if constexpr (F8)
+                        mma_ss_f8(tmem + S_COL0 + buf * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+                    else
+                        mma_ss(tmem + S_COL0 + buf * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int buf, int vs, bool first) {
-                const uint32_t vb = sV + vs * KV_BYTES;
+                const uint32_t vb = sV + vs * C::V_BYTES;
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
@@ -738,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + O_COL;
         const int off = sh.n_kv - sh.n_q;
         const bool split = (sh.causal ? (r0 + off + 1) : sh.n_kv) < pf::kSplitKeys;
-        const float c = sh.c;
+        const float c = F8 ? sh.c * sc.q[bh] * sc.k[bkv] : sh.c;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
@@ -799,8 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(tO + ch * 32, u);
                 }
             }
-            const float sum = split ? exp_pack_store64<BF16, true>(s, c, neg, tS)
-                                    : exp_pack_store64<BF16, false>(s, c, neg, tS);
+            const float sum = split ? pf::exp_pack_store<BN, PB, true>(s, c, neg, tS)
+                                    : pf::exp_pack_store<BN, PB, false>(s, c, neg, tS);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -813,7 +946,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(b_ofull, 0, abort_flag, err);
         tc_fence_after();
         const bool row_ok = row_g < sh.n_q;
-        const float inv = (ok && l > 0.f) ? 1.0f / l : 0.f;
+        const float vsc = F8 ? sc.v[bkv] : 1.0f;
+        const float inv = (ok && l > 0.f) ? vsc / l : 0.f;
         const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row_g) * D;
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
@@ -859,25 +993,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host
 
-// [d, n, bh] bf16/f16 tensor, box {64, rows, 1}, 128-byte swizzle, zero fill.
-static bool make_map(CUtensorMap *m, const void *ptr, int d, int n, int bh, bool bf16,
-                     int rows = 128) {
+// [d, n, bh] tensor map: 16-bit elements in 128-byte (64-element) panel
+// rows, or E4M3 bytes in min(d, 128)-byte panel rows; `rows` per box, the
+// panel width as swizzle span, zero fill past n.
+static bool make_map(CUtensorMap *m, const void *ptr, int d, int n, int bh, bool bf16, bool f8,
+                     int rows) {
+    const uint64_t esz = f8 ? 1 : 2;
+    const int pw = f8 ? (d < 128 ? d : 128) : 128;
     const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(n),
                               static_cast<uint64_t>(bh)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2,
-                                 static_cast<uint64_t>(d) * 2 * static_cast<uint64_t>(n)};
-    const uint32_t box[3] = {64, static_cast<uint32_t>(rows), 1};
-    return make_tmap_3d_16bit(m, ptr, bf16, dims, strides, box);
+    const uint64_t strides[2] = {static_cast<uint64_t>(d) * esz,
+                                 static_cast<uint64_t>(d) * esz * static_cast<uint64_t>(n)};
+    const uint32_t box[3] = {static_cast<uint32_t>(pw / esz), static_cast<uint32_t>(rows), 1};
+    const TmapElem el = f8 ? TmapElem::U8 : (bf16 ? TmapElem::BF16 : TmapElem::F16);
+    return make_tmap_3d(m, ptr, el, dims, strides, box, pw);
 }
 
-template <int D, bool BF16, int OUT>
-static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
-    using C = pf::Cfg<D>;
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.Q, D, a.n_q, a.B * a.Hq, BF16) ||
-        !make_map(&mk, a.K, D, a.n_kv, a.B * a.Hkv, BF16) ||
-        !make_map(&mv, a.V, D, a.n_kv, a.B * a.Hkv, BF16))
-        return cudaErrorInvalidValue;
+static pf::Shape make_shape(const PrefillArgs &a, int rows_per_cta) {
     pf::Shape sh;
     sh.B = a.B;
     sh.Hq = a.Hq;
@@ -886,10 +1018,23 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
     sh.n_q = a.n_q;
     sh.n_kv = a.n_kv;
     sh.causal = a.causal;
-    sh.nqb = (a.n_q + pf::NT * pf::BM - 1) / (pf::NT * pf::BM);
+    sh.nqb = (a.n_q + rows_per_cta - 1) / rows_per_cta;
     sh.c = a.scale * 1.4426950408889634f;
     sh.scale = a.scale;
-    auto kern = pf::prefill_kernel<D, BF16, OUT>;
+    return sh;
+}
+
+template <int D, bool BF16, bool F8, int OUT>
+static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
+    using C = pf::Cfg<D, F8>;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.Q, D, a.n_q, a.B * a.Hq, BF16, F8, pf::BM) ||
+        !make_map(&mk, a.K, D, a.n_kv, a.B * a.Hkv, BF16, F8, pf::BN) ||
+        !make_map(&mv, a.V, D, a.n_kv, a.B * a.Hkv, BF16, F8, pf::BN))
+        return cudaErrorInvalidValue;
+    const pf::Shape sh = make_shape(a, pf::NT * pf::BM);
+    const pf::Scales sc{a.q_scale, a.k_scale, a.v_scale};
+    auto kern = pf::prefill_kernel<D, BF16, F8, OUT>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
@@ -897,68 +1042,64 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
     const long long grid = static_cast<long long>(sh.nqb) * a.B * a.Hq;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidValue;
-    kern<<<static_cast<unsigned>(grid), pf::kThreads, C::SMEM, st>>>(mq, mk, mv, a.O, a.lse, sh,
-                                                                     a.err);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(mq, mk, mv, a.O, a.lse, sh, sc,
+                                                                  a.err);
     return cudaGetLastError();
 }
 
-template <int D, bool BF16>
-static cudaError_t launch_prefill_out(const PrefillArgs &a, cudaStream_t st) {
-    switch (a.out_dtype) {
-    case 0: return launch_prefill_t<D, BF16, 0>(a, st);
-    case 1: return launch_prefill_t<D, BF16, 1>(a, st);
-    default: return launch_prefill_t<D, BF16, 2>(a, st);
-    }
-}
-
-template <bool BF16, int OUT>
+template <bool BF16, bool F8, int OUT>
 static cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t st) {
+    using C = pfw::Cfg<F8>;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.Q, pfw::D, a.n_q, a.B * a.Hq, BF16, pfw::BM) ||
-        !make_map(&mk, a.K, pfw::D, a.n_kv, a.B * a.Hkv, BF16, pfw::BN) ||
-        !make_map(&mv, a.V, pfw::D, a.n_kv, a.B * a.Hkv, BF16, pfw::BN))
+    if (!make_map(&mq, a.Q, pfw::D, a.n_q, a.B * a.Hq, BF16, F8, pfw::BM) ||
+        !make_map(&mk, a.K, pfw::D, a.n_kv, a.B * a.Hkv, BF16, F8, pfw::BN) ||
+        !make_map(&mv, a.V, pfw::D, a.n_kv, a.B * a.Hkv, BF16, F8, pfw::BN))
         return cudaErrorInvalidValue;
-    pf::Shape sh;
-    sh.B = a.B;
-    sh.Hq = a.Hq;
-    sh.Hkv = a.Hkv;
-    sh.G = a.Hq / a.Hkv;
-    sh.n_q = a.n_q;
-    sh.n_kv = a.n_kv;
-    sh.causal = a.causal;
-    sh.nqb = (a.n_q + pfw::BM - 1) / pfw::BM;
-    sh.c = a.scale * 1.4426950408889634f;
-    sh.scale = a.scale;
-    auto kern = pfw::prefill_wide_kernel<BF16, OUT>;
+    const pf::Shape sh = make_shape(a, pfw::BM);
+    const pf::Scales sc{a.q_scale, a.k_scale, a.v_scale};
+    auto kern = pfw::prefill_wide_kernel<BF16, F8, OUT>;
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pfw::SMEM);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
         return e;
     const long long grid = static_cast<long long>(sh.nqb) * a.B * a.Hq;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidValue;
-    kern<<<static_cast<unsigned>(grid), pfw::kThreads, pfw::SMEM, st>>>(mq, mk, mv, a.O, a.lse,
-                                                                        sh, a.err);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(mq, mk, mv, a.O, a.lse, sh, sc,
+                                                                  a.err);
     return cudaGetLastError();
 }
 
-template <bool BF16>
-static cudaError_t launch_prefill_wide_out(const PrefillArgs &a, cudaStream_t st) {
-    switch (a.out_dtype) {
-    case 0: return launch_prefill_wide<BF16, 0>(a, st);
-    case 1: return launch_prefill_wide<BF16, 1>(a, st);
-    default: return launch_prefill_wide<BF16, 2>(a, st);
+template <int D, bool BF16, bool F8>
+static cudaError_t launch_out(const PrefillArgs &a, cudaStream_t st) {
+    if constexpr (D == 256) {
+        switch (a.out_dtype) {
+        case 0: return launch_prefill_wide<BF16, F8, 0>(a, st);
+        case 1: return launch_prefill_wide<BF16, F8, 1>(a, st);
+        default: return launch_prefill_wide<BF16, F8, 2>(a, st);
+        }
+    } else {
+        switch (a.out_dtype) {
+        case 0: return launch_prefill_t<D, BF16, F8, 0>(a, st);
+        case 1: return launch_prefill_t<D, BF16, F8, 1>(a, st);
+        default: return launch_prefill_t<D, BF16, F8, 2>(a, st);
+        }
     }
 }
 
+template <int D>
+static cudaError_t launch_d(const PrefillArgs &a, cudaStream_t st) {
+    if (a.e4m3)
+        return launch_out<D, false, true>(a, st);
+    return a.bf16 ? launch_out<D, true, false>(a, st) : launch_out<D, false, false>(a, st);
+}
+
 cudaError_t prefill_launch(const PrefillArgs &a, cudaStream_t st) {
-    if (a.d == 256)
-        return a.bf16 ? launch_prefill_wide_out<true>(a, st) : launch_prefill_wide_out<false>(a, st);
-    if (a.d == 64)
-        return a.bf16 ? launch_prefill_out<64, true>(a, st) : launch_prefill_out<64, false>(a, st);
-    if (a.d == 128)
-        return a.bf16 ? launch_prefill_out<128, true>(a, st)
-                      : launch_prefill_out<128, false>(a, st);
+    switch (a.d) {
+    case 64: return launch_d<64>(a, st);
+    case 128: return launch_d<128>(a, st);
+    case 256: return launch_d<256>(a, st);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -69,19 +69,25 @@ typedef enum {
 } attn_dtype;
 
 /* Prefill / full attention.
- *   Q   [B, Hq,  n_q,  d]   in_dtype (F16 or BF16)
+ *   Q   [B, Hq,  n_q,  d]   in_dtype (F16, BF16 or E4M3)
  *   K,V [B, Hkv, n_kv, d]   in_dtype
  *   O   [B, Hq,  n_q,  d]   out_dtype (F16, BF16 or F32)
  *   lse [B, Hq,  n_q]       fp32, or NULL
+ *   q_scale [B * Hq], k_scale, v_scale [B * Hkv]: fp32 per-head scales of
+ *           an E4M3 input (dequantised value = code * scale); NULL for
+ *           16-bit inputs.  With E4M3 inputs q K^T runs on the 8-bit tensor
+ *           cores and P V in f16 (V widened on chip, exactly).
  * d in {64, 128, 256}; Hq % Hkv == 0; causal requires n_q <= n_kv.
  * scale is the factor applied to q.k (1/sqrt(d) for the textbook form).
- * Host-side errors: ATTN_ERR_INVALID for null pointers, non-positive sizes,
- * misalignment, Hq % Hkv != 0, causal with n_q > n_kv; ATTN_ERR_UNSUPPORTED
- * for other d or dtype combinations.  One kernel launch. */
+ * Host-side errors: ATTN_ERR_INVALID for null pointers (scales included for
+ * E4M3), non-positive sizes, misalignment, Hq % Hkv != 0, causal with
+ * n_q > n_kv; ATTN_ERR_UNSUPPORTED for other d or dtype combinations.  One
+ * kernel launch. */
 ATTN_API attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O,
                          float *lse, int B, int Hq, int Hkv, int n_q, int n_kv,
                          int d, int causal, float scale, attn_dtype in_dtype,
-                         attn_dtype out_dtype, void *stream);
+                         attn_dtype out_dtype, const float *q_scale,
+                         const float *k_scale, const float *v_scale, void *stream);
 
 /* Bytes of caller-provided device workspace attn_decode needs for these
  * sizes (split-KV partial states).  max_seq_len bounds every seq_lens[s]. */

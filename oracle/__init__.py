@@ -212,6 +212,25 @@ def kv_append(k_new, v_new, Kc, Vc, block_table, seq_ids, positions, k_scale=Non
     return Kout, Vout
 
 
+_E4M3_LUT = None
+
+
+def dequantize_e4m3(codes, scale, head_dim: int = 1) -> np.ndarray:
+    """fp64 values of E4M3 codes times a per-head scale: code -> value by the
+    oracle's own bit-level decoder (all 256 codes), multiplied by
+    scale[head] along axis `head_dim` after flattening the axes before it
+    (scale has one entry per (leading index, head) pair, in order)."""
+    global _E4M3_LUT
+    if _E4M3_LUT is None:
+        _E4M3_LUT = np.array([e4m3_decode(i) for i in range(256)], np.float64)
+    c = _as_np(codes)
+    v = _E4M3_LUT[c]
+    sc = np.asarray(_as_np(scale), np.float64).reshape(-1)
+    lead = int(np.prod(c.shape[:head_dim + 1]))
+    assert sc.size == lead, "one scale per head"
+    return (v.reshape(lead, -1) * sc[:, None]).reshape(c.shape)
+
+
 def e4m3_decode(code: int) -> float:
     return float(lib().oracle_e4m3_to_f64(code))
 

@@ -49,11 +49,11 @@ FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced by the host check
 
 def _prefill(L, **kw):
     a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, lse=None, B=1, Hq=4, Hkv=2, nq=128, nkv=128, d=128,
-             causal=1, scale=0.1, ind=1, outd=1)
+             causal=1, scale=0.1, ind=1, outd=1, qs=None, ks=None, vs=None)
     a.update(kw)
     return L.attn_prefill(a["Q"], a["K"], a["V"], a["O"], a["lse"], a["B"], a["Hq"], a["Hkv"],
                           a["nq"], a["nkv"], a["d"], a["causal"], a["scale"], a["ind"], a["outd"],
-                          None)
+                          a["qs"], a["ks"], a["vs"], None)
 
 
 def test_prefill_host_validation(L):
@@ -66,6 +66,8 @@ def test_prefill_host_validation(L):
     assert _prefill(L, d=96) == attn.ERR_UNSUPPORTED
     assert _prefill(L, ind=2) == attn.ERR_UNSUPPORTED                 # fp32 inputs
     assert _prefill(L, outd=3) == attn.ERR_UNSUPPORTED
+    assert _prefill(L, ind=3) == attn.ERR_INVALID                     # E4M3 without scales
+    assert _prefill(L, ind=3, qs=FAKE, ks=FAKE, vs=None) == attn.ERR_INVALID
     assert L.attn_last_launch_count() == 0
 
 

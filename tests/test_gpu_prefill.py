@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from exact_io_aware_106_b300 import attn, workloads as W
-from tests.parity import assert_lse, assert_out
+from tests.parity import ATOL_FP8, assert_lse, assert_out
 
 pytestmark = pytest.mark.gpu
 
@@ -127,3 +127,74 @@ def test_prefill_full_size_sampled_rows(name):
             assert_lse(lse[b, h, rows], lr, what=f"{name} b{b} h{h}")
     # the output is finite everywhere
     assert torch.isfinite(O.float()).all() and torch.isfinite(lse).all()
+
+
+# ------------------------------------------------------------ E4M3 inputs
+
+E4M3_SMALL = [
+    # B, Hq, Hkv, n_q, n_kv, d, causal, out
+    (1, 2, 1, 300, 300, 128, True, "bf16"),
+    (2, 4, 2, 129, 1000, 128, False, "f32"),    # non-causal, 1000 keys per row
+    (1, 4, 1, 200, 700, 64, True, "f32"),       # n_q < n_kv, bottom-right mask
+    (1, 2, 2, 333, 333, 64, False, "bf16"),
+    (1, 2, 1, 257, 257, 256, True, "f32"),
+    (1, 4, 2, 100, 600, 256, False, "bf16"),
+]
+
+
+def _run_e4m3(B, Hq, Hkv, nq, nkv, d, causal, outd, seed=0):
+    spec = W.PrefillSpec(B, Hq, Hkv, nq, nkv, d, causal, "bf16", outd)
+    t = W.make_prefill(spec, seed=seed)
+    qz = W.quantize_prefill_e4m3(t)
+    g = {k: v.cuda() for k, v in qz.items()}
+    O, lse = attn.prefill(g["Q"], g["K"], g["V"], causal, out_dtype=DT[outd],
+                          q_scale=g["q_scale"], k_scale=g["k_scale"], v_scale=g["v_scale"])
+    assert attn.last_launch_count() == 1
+    assert attn.last_error() == attn.OK
+    deq = {n: oracle.dequantize_e4m3(qz[n], qz[n.lower() + "_scale"], 1) for n in "QKV"}
+    return t, O, lse, deq
+
+
+@pytest.mark.parametrize("case", E4M3_SMALL, ids=lambda c: "x".join(map(str, c)))
+def test_prefill_e4m3_matches_oracle_on_dequantised_inputs(case):
+    """The kernel's arithmetic: every element against the oracle fed the
+    dequantised inputs (code * per-head scale), under the 16-bit rules."""
+    t, O, lse, deq = _run_e4m3(*case)
+    O_ref, lse_ref = oracle.sdpa(deq["Q"], deq["K"], deq["V"], case[6])
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("case", [E4M3_SMALL[1], E4M3_SMALL[5]], ids=lambda c: "x".join(map(str, c)))
+def test_prefill_e4m3_quantisation_budget(case):
+    """The quantisation budget: rows that average >= 512 keys against the
+    oracle fed the unquantised inputs, 3e-2 max-abs."""
+    t, O, lse, _ = _run_e4m3(*case)
+    O_src, _ = oracle.sdpa(t["Q"], t["K"], t["V"], case[6])
+    assert case[4] >= 512 and not case[6]
+    assert_out(O.float(), O_src, atol=ATOL_FP8)
+
+
+SWEEP_PREFILL_E4M3 = [W.sweep_prefill(G, d, "e4m3") for G, d in ((1, 64), (8, 128), (16, 256))]
+
+
+@pytest.mark.parametrize("spec", SWEEP_PREFILL_E4M3, ids=lambda s: s.name)
+def test_prefill_e4m3_full_size_sampled_rows(spec):
+    t = W.make_prefill(spec, seed=0, device="cuda")
+    qz = W.quantize_prefill_e4m3(t)
+    O, lse = attn.prefill(qz["Q"], qz["K"], qz["V"], spec.causal,
+                          out_dtype=W.DTYPES[spec.out_dtype], q_scale=qz["q_scale"],
+                          k_scale=qz["k_scale"], v_scale=qz["v_scale"])
+    assert attn.last_error() == attn.OK
+    rng = np.random.default_rng(1)
+    G = spec.Hq // spec.Hkv
+    for h in sorted({0, spec.Hq - 1, int(rng.integers(0, spec.Hq))}):
+        hk = h // G
+        Qh = oracle.dequantize_e4m3(qz["Q"][:, h:h + 1].cpu(), qz["q_scale"][h:h + 1].cpu(), 1)
+        Kh = oracle.dequantize_e4m3(qz["K"][:, hk:hk + 1].cpu(), qz["k_scale"][hk:hk + 1].cpu(), 1)
+        Vh = oracle.dequantize_e4m3(qz["V"][:, hk:hk + 1].cpu(), qz["v_scale"][hk:hk + 1].cpu(), 1)
+        rows = _sample_rows(spec.n_q, rng)
+        Or, lr = oracle.sdpa_rows(Qh, Kh, Vh, [(0, 0, r) for r in rows], spec.causal, nthreads=0)
+        assert_out(O[0, h, rows], Or, what=f"{spec.name} h{h}")
+        assert_lse(lse[0, h, rows], lr, what=f"{spec.name} h{h}")
+    assert torch.isfinite(O.float()).all()

@@ -308,3 +308,14 @@ def test_kv_append_writes_slot(kv):
     for b, h, s in changed:
         assert any(b == int(bt[sid[r], pos[r] // 16]) and s == int(pos[r] % 16)
                    for r in range(3))
+
+
+def test_dequantize_e4m3_per_head_matches_torch_cast():
+    """The oracle's per-head E4M3 dequantisation (its own bit-level decoder)
+    equals torch's decode of the same codes times the per-head scale."""
+    x = torch.randn(2, 3, 5, 8, generator=torch.Generator().manual_seed(11)) * 3
+    codes = (x / 0.05).to(torch.float8_e4m3fn)
+    scale = torch.linspace(0.5, 2.0, 6)
+    got = oracle.dequantize_e4m3(codes, scale, 1)
+    want = (codes.to(torch.float64) * scale.double().view(2, 3, 1, 1)).numpy()
+    assert np.array_equal(got, want)
