@@ -59,11 +59,36 @@ class DecodeSpec:
     name: str = ""
 
 
+@dataclass(frozen=True)
+class PagedPrefillSpec:
+    """n_q new query tokens per sequence attending to the sequence's whole
+    block-paged cache (prefix + the new tokens, length U[len_lo, len_hi])."""
+    B: int
+    Hq: int
+    Hkv: int
+    n_q: int
+    d: int
+    len_lo: int
+    len_hi: int
+    block_size: int = 16
+    causal: bool = True
+    dtype: str = "bf16"
+    out_dtype: str = "bf16"
+    name: str = ""
+
+
 PREFILL_WORKLOADS = {
     "single-head": PrefillSpec(1, 1, 1, 512, 512, 64, False, "f16", "f32", "single-head"),
     "gqa-4k": PrefillSpec(4, 32, 8, 4096, 4096, 128, True, "bf16", "bf16", "gqa-4k"),
     "long-23k": PrefillSpec(1, 12, 12, 23400, 23400, 64, True, "f16", "f16", "long-23k"),
     "long-32k": PrefillSpec(1, 64, 8, 32768, 32768, 128, True, "bf16", "bf16", "long-32k"),
+}
+
+PAGED_PREFILL_WORKLOADS = {
+    # chunked prefill over cached prefixes: 8 sequences x 1024 new tokens,
+    # total lengths U[4096, 16384], GQA 32/8, d 128, bf16, 16-token blocks
+    "paged-prefill": PagedPrefillSpec(8, 32, 8, 1024, 128, 4096, 16384, 16, True, "bf16", "bf16",
+                                      "paged-prefill"),
 }
 
 DECODE_WORKLOADS = {
@@ -187,3 +212,18 @@ def quantize_prefill_e4m3(t: dict) -> dict:
         out[name] = codes.reshape(x.shape)
         out[name.lower() + "_scale"] = scale
     return out
+
+
+def make_paged_prefill(spec: PagedPrefillSpec, seed: int = 0, device="cpu", lens=None):
+    """Q [B,Hq,n_q,d]; K/V cache [num_blocks,Hkv,block_size,d] holding every
+    sequence's tokens (the new ones last); block_table, seq_lens as for
+    decode."""
+    lens_t, table, num_blocks = make_seq_structure(spec.B, spec.len_lo, spec.len_hi,
+                                                   spec.block_size, seed, 0, lens)
+    g = _gen(device, seed)
+    dt = DTYPES[spec.dtype]
+    Q = _randn((spec.B, spec.Hq, spec.n_q, spec.d), dt, g, device)
+    Kc = _randn((num_blocks, spec.Hkv, spec.block_size, spec.d), dt, g, device)
+    Vc = _randn((num_blocks, spec.Hkv, spec.block_size, spec.d), dt, g, device)
+    return {"Q": Q, "Kc": Kc, "Vc": Vc, "block_table": table.to(device),
+            "seq_lens": lens_t.to(device), "num_blocks": num_blocks}

@@ -65,6 +65,10 @@ def lib():
                                           i32, i32, i32, i32, i32, i32, i32, f64, vp, i32,
                                           i32, vp]
         L.oracle_decode_paged.restype = i32
+        L.oracle_prefill_paged.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, vp, i32, i32,
+                                           i32, i32, i32, i32, i32, i32, i32, f64, i32, i32,
+                                           i32]
+        L.oracle_prefill_paged.restype = i32
         L.oracle_kv_append.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, i32,
                                        i32, i32, i32, i32, i32, i32]
         L.oracle_kv_append.restype = i32
@@ -187,6 +191,31 @@ def decode_paged(q, Kc, Vc, block_table, seq_lens, scale: float | None = None,
         raise ValueError("oracle_decode_paged: invalid arguments")
     if return_counts:
         return O, lse, (int(counts[0]), int(counts[1]))
+    return O, lse
+
+
+def prefill_paged(Q, Kc, Vc, block_table, seq_lens, causal: bool, scale: float | None = None,
+                  rows=None, nthreads: int = 0):
+    """n_q query rows per sequence against its block-paged cache (the new
+    tokens are the sequence's last n_q).  Q [B,Hq,n_q,d]; caches
+    [num_blocks,Hkv,bs,d]; rows = (lo, hi) limits the query rows computed.
+    Returns (O [B,Hq,hi-lo,d], lse [B,Hq,hi-lo]) in fp64."""
+    qn, Kn, Vn = _as_np(Q), _as_np(Kc), _as_np(Vc)
+    bt = np.ascontiguousarray(_as_np(block_table).astype(np.int32))
+    sl = np.ascontiguousarray(_as_np(seq_lens).astype(np.int32))
+    B, Hq, n_q, d = qn.shape
+    num_blocks, Hkv, bs, _ = Kn.shape
+    lo, hi = (0, n_q) if rows is None else rows
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    O = np.zeros((B, Hq, hi - lo, d), np.float64)
+    lse = np.zeros((B, Hq, hi - lo), np.float64)
+    rc = lib().oracle_prefill_paged(_p(qn), dtype_code(Q), _p(Kn), _p(Vn), dtype_code(Kc),
+                                    _p(bt), _p(sl), _p(O), _p(lse), B, Hq, Hkv, n_q, d, bs,
+                                    bt.shape[1], num_blocks, int(causal), float(scale), lo, hi,
+                                    nthreads)
+    if rc != 0:
+        raise ValueError("oracle_prefill_paged: invalid arguments")
     return O, lse
 
 

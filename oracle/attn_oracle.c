@@ -424,6 +424,92 @@ int oracle_decode_paged(const void *q, int q_dtype, const void *Kc,
 
 /* ------------------------------------------------------------ kv append */
 
+/* Prefill over a block-paged cache (prefix caching / chunked prefill):
+ * for every sequence b and query head h, the n_q query rows Q[b,h] attend
+ * to the len = seq_lens[b] cached keys of KV head h / G, gathered in token
+ * order from cache[block_table[b][t / block_size]][h_kv][t % block_size]
+ * ([TCOS] block-wise KV cache).  With causal set, query i sees key j iff
+ * j <= i + (len - n_q) -- the new tokens are the last n_q of the sequence
+ * (bottom-right alignment, [FASL] causal masking).  Only query rows
+ * [row_lo, row_hi) are computed; O is [B, Hq, row_hi - row_lo, d] and lse
+ * [B, Hq, row_hi - row_lo].  The scores of a row are materialised in fp64,
+ * the row max is subtracted before exp ([IOAE] §8). */
+int oracle_prefill_paged(const void *Q, int q_dtype, const void *Kc, const void *Vc,
+                         int kv_dtype, const int32_t *block_table, const int32_t *seq_lens,
+                         double *O, double *lse, int B, int Hq, int Hkv, int n_q, int d,
+                         int block_size, int max_blocks_per_seq, int num_blocks, int causal,
+                         double scale, int row_lo, int row_hi, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || n_q <= 0 || d <= 0 || block_size <= 0 ||
+        Hq % Hkv != 0 || row_lo < 0 || row_hi > n_q || row_lo >= row_hi)
+        return -1;
+    if (kv_dtype == OR_E4M3)
+        return -1;
+    const int G = Hq / Hkv;
+    const int nr = row_hi - row_lo;
+    for (int b = 0; b < B; ++b) {
+        const int len = seq_lens[b];
+        if (len < (causal ? n_q : 1) || (len + block_size - 1) / block_size > max_blocks_per_seq)
+            return -1;
+        for (int t = 0; t < len; t += block_size) {
+            const int blk = block_table[(size_t)b * max_blocks_per_seq + t / block_size];
+            if (blk < 0 || blk >= num_blocks)
+                return -1;
+        }
+    }
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int bh = 0; bh < B * Hq; ++bh) {
+        const int b = bh / Hq, h = bh % Hq, hk = h / G;
+        const int len = seq_lens[b];
+        double *k = (double *)malloc(((size_t)len * d + 1) * sizeof(double));
+        double *v = (double *)malloc(((size_t)len * d + 1) * sizeof(double));
+        double *srow = (double *)malloc(((size_t)len + 1) * sizeof(double));
+        for (int t = 0; t < len; ++t) {
+            const int blk = block_table[(size_t)b * max_blocks_per_seq + t / block_size];
+            const size_t base = (((size_t)blk * Hkv + hk) * block_size + t % block_size) * d;
+            for (int c = 0; c < d; ++c) {
+                k[(size_t)t * d + c] = load_elem(Kc, kv_dtype, base + c);
+                v[(size_t)t * d + c] = load_elem(Vc, kv_dtype, base + c);
+            }
+        }
+        for (int i = row_lo; i < row_hi; ++i) {
+            double *q = decode_rows(Q, q_dtype, (((size_t)b * Hq + h) * n_q + i) * d, (size_t)d);
+            /* scores of row i, future keys masked to -inf */
+            double m = -INFINITY;
+            for (int j = 0; j < len; ++j) {
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c)
+                    acc += q[c] * k[(size_t)j * d + c];
+                srow[j] = (causal && j > i + (len - n_q)) ? -INFINITY : acc * scale;
+                if (srow[j] > m)
+                    m = srow[j];
+            }
+            double *o = O + (((size_t)b * Hq + h) * nr + (i - row_lo)) * d;
+            double l = 0.0;
+            for (int j = 0; j < len; ++j) {
+                srow[j] = exp(srow[j] - m);
+                l += srow[j];
+            }
+            for (int c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int j = 0; j < len; ++j)
+                    acc += (srow[j] / l) * v[(size_t)j * d + c];
+                o[c] = acc;
+            }
+            if (lse)
+                lse[((size_t)b * Hq + h) * nr + (i - row_lo)] = m + log(l);
+            free(q);
+        }
+        free(k);
+        free(v);
+        free(srow);
+    }
+    return 0;
+}
+
 /* Write T new tokens into the paged cache ([TCOS] KV cache concept: the new
  * K/V of each generated token is added to the cache).  k_new/v_new
  * [T][Hkv][d] (src_dtype), token r goes to sequence seq_ids[r] at position

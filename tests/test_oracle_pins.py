@@ -319,3 +319,59 @@ def test_dequantize_e4m3_per_head_matches_torch_cast():
     got = oracle.dequantize_e4m3(codes, scale, 1)
     want = (codes.to(torch.float64) * scale.double().view(2, 3, 1, 1)).numpy()
     assert np.array_equal(got, want)
+
+
+
+# ------------------------------------------------------------ paged prefill
+
+def _gather(Kc, bt, lens, b):
+    """Dense [1, Hkv, len, d] copy of sequence b's cache (data movement)."""
+    bs = Kc.shape[2]
+    L = int(lens[b])
+    blocks = bt[b, :(L + bs - 1) // bs].long()
+    x = Kc[blocks]                                   # [nblk, Hkv, bs, d]
+    x = x.permute(1, 0, 2, 3).reshape(Kc.shape[1], -1, Kc.shape[3])[:, :L]
+    return x.unsqueeze(0).contiguous()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_paged_equals_sdpa_on_gathered_cache(causal):
+    spec = W.PagedPrefillSpec(3, 4, 2, 21, 16, 21, 70, 16, causal, "bf16", "f32")
+    t = W.make_paged_prefill(spec, seed=3)
+    O, lse = oracle.prefill_paged(t["Q"], t["Kc"], t["Vc"], t["block_table"], t["seq_lens"],
+                                  causal)
+    for b in range(spec.B):
+        K = _gather(t["Kc"], t["block_table"], t["seq_lens"], b)
+        V = _gather(t["Vc"], t["block_table"], t["seq_lens"], b)
+        Ob, lb = oracle.sdpa(t["Q"][b:b + 1], K, V, causal)
+        assert np.allclose(O[b], Ob[0], rtol=0, atol=1e-12)
+        assert np.allclose(lse[b], lb[0], rtol=0, atol=1e-12)
+
+
+def test_prefill_paged_one_query_equals_decode():
+    spec = W.PagedPrefillSpec(4, 8, 2, 1, 32, 1, 90, 16, True, "f16", "f32")
+    t = W.make_paged_prefill(spec, seed=4)
+    O, lse = oracle.prefill_paged(t["Q"], t["Kc"], t["Vc"], t["block_table"], t["seq_lens"],
+                                  True)
+    Od, ld = oracle.decode_paged(t["Q"][:, :, 0], t["Kc"], t["Vc"], t["block_table"],
+                                 t["seq_lens"])
+    assert np.allclose(O[:, :, 0], Od, rtol=0, atol=1e-12)
+    assert np.allclose(lse[:, :, 0], ld, rtol=0, atol=1e-12)
+
+
+def test_prefill_paged_row_range_and_validation():
+    spec = W.PagedPrefillSpec(2, 2, 1, 40, 16, 40, 100, 32, True, "bf16", "f32")
+    t = W.make_paged_prefill(spec, seed=5)
+    O, lse = oracle.prefill_paged(t["Q"], t["Kc"], t["Vc"], t["block_table"], t["seq_lens"], True)
+    Os, ls = oracle.prefill_paged(t["Q"], t["Kc"], t["Vc"], t["block_table"], t["seq_lens"], True,
+                                  rows=(7, 19))
+    assert np.array_equal(Os, O[:, :, 7:19]) and np.array_equal(ls, lse[:, :, 7:19])
+    # the last query of a causal row sees every key: equal to the full row
+    bt = t["block_table"].clone()
+    bt[0, 0] = t["num_blocks"] + 3
+    with pytest.raises(ValueError):
+        oracle.prefill_paged(t["Q"], t["Kc"], t["Vc"], bt, t["seq_lens"], True)
+    short = t["seq_lens"].clone()
+    short[1] = spec.n_q - 1                      # causal needs len >= n_q
+    with pytest.raises(ValueError):
+        oracle.prefill_paged(t["Q"], t["Kc"], t["Vc"], t["block_table"], short, True)
