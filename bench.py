@@ -387,6 +387,8 @@ def workload_lines(name: str, steps: int, warmup: int):
     jobs = []
     if name in W.PREFILL_WORKLOADS:
         jobs.append(("prefill", W.PREFILL_WORKLOADS[name]))
+    elif name in W.PAGED_PREFILL_WORKLOADS:
+        jobs.append(("paged-prefill", W.PAGED_PREFILL_WORKLOADS[name]))
     elif name in W.DECODE_WORKLOADS:
         jobs.append(("decode", W.DECODE_WORKLOADS[name]))
     elif name == "sweep":
@@ -422,6 +424,29 @@ def workload_lines(name: str, steps: int, warmup: int):
                             peak_tflops=peak,
                             peak_kind="measured burst bf16" + (
                                 " x 2 (nominal fp8/bf16 ratio)" if spec.dtype == "e4m3" else ""))
+            elif kind == "paged-prefill":
+                t = W.make_paged_prefill(spec, seed=0, device=dev)
+                lens = t["seq_lens"].cpu()
+                O = torch.empty(t["Q"].shape, dtype=W.DTYPES[spec.out_dtype], device=dev)
+                lse = torch.empty(t["Q"].shape[:3], dtype=torch.float32, device=dev)
+
+                def fn():
+                    attn.prefill_paged(t["Q"], t["Kc"], t["Vc"], t["block_table"],
+                                       t["seq_lens"], max_seq_len=spec.len_hi,
+                                       causal=spec.causal, O=O, lse=lse, stream=stream)
+                med, best = _time_kernel(fn, stream, warmup, steps, flush)
+                # pairs: new token i of sequence b sees len_b - n_q + i + 1 keys
+                n = spec.n_q
+                pairs = sum(n * (int(L) - n) + n * (n + 1) // 2 for L in lens) * spec.Hq
+                F = 4.0 * spec.d * pairs
+                e = ESZ[spec.dtype]
+                Bp = (2 * spec.B * spec.Hq * n * spec.d * e
+                      + 2 * spec.Hkv * spec.d * e * float(sum(int(L) for L in lens)))
+                roof = max(F / (pk["bf16_tflops"] * 1e12), Bp / (pk["hbm_gbs"] * 1e9))
+                line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            tflops=round(F / med / 1e12, 2),
+                            pct_roofline=round(100 * roof / med, 2),
+                            peak_tflops=pk["bf16_tflops"], peak_kind="measured burst bf16")
             else:
                 dd = W.make_decode(spec, seed=0, device=dev)
                 lens = dd["seq_lens"].cpu()

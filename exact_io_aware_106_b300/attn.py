@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libattn.so")
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 _DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.float8_e4m3fn: 3}
 
-EXPORTS = ("attn_prefill", "attn_decode_workspace_bytes", "attn_decode", "attn_kv_append",
+EXPORTS = ("attn_prefill", "attn_prefill_paged", "attn_decode_workspace_bytes", "attn_decode",
+           "attn_kv_append",
            "attn_last_error", "attn_status_str", "attn_last_launch_count",
            "attn_decode_static_ws")
 
@@ -47,6 +48,9 @@ def lib():
         L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                    i32, i32, vp, vp, vp, vp]
         L.attn_prefill.restype = i32
+        L.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                         i32, i32, i32, i32, i32, f32, i32, i32, vp]
+        L.attn_prefill_paged.restype = i32
         L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.attn_decode_workspace_bytes.restype = sz
         L.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
@@ -128,6 +132,33 @@ def prefill(Q, K, V, causal: bool, scale: float | None = None, out_dtype=None, O
                             d, int(bool(causal)), float(scale), _DT[Q.dtype], _DT[O.dtype],
                             _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _stream(stream))
     _check("attn_prefill", st)
+    return O, lse
+
+
+def prefill_paged(Q, Kc, Vc, block_table, seq_lens, max_seq_len: int, causal: bool = True,
+                  scale: float | None = None, out_dtype=None, O=None, lse=None,
+                  want_lse: bool = True, stream=None):
+    """n_q new tokens per sequence (the last n_q of each sequence, already in
+    the cache) against the whole block-paged cache [num_blocks,Hkv,bs,d].
+    Q [B,Hq,n_q,d]; returns (O [B,Hq,n_q,d], lse [B,Hq,n_q])."""
+    _cuda(Q, Kc, Vc, block_table, seq_lens)
+    B, Hq, nq, d = Q.shape
+    num_blocks, Hkv, bs, _ = Kc.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out_dtype is None:
+        out_dtype = Q.dtype
+    if O is None:
+        O = torch.empty((B, Hq, nq, d), dtype=out_dtype, device=Q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, nq), dtype=torch.float32, device=Q.device)
+    _cuda(O, lse)
+    st = lib().attn_prefill_paged(_ptr(Q), _ptr(Kc), _ptr(Vc), _ptr(block_table),
+                                  _ptr(seq_lens), _ptr(O), _ptr(lse), B, Hq, Hkv, nq, d, bs,
+                                  block_table.shape[1], num_blocks, int(max_seq_len),
+                                  int(bool(causal)), float(scale), _DT[Q.dtype], _DT[O.dtype],
+                                  _stream(stream))
+    _check("attn_prefill_paged", st)
     return O, lse
 
 

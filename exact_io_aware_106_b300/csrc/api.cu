@@ -97,6 +97,53 @@ attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, f
     return ATTN_OK;
 }
 
+attn_status attn_prefill_paged(const void *Q, const void *Kcache, const void *Vcache,
+                               const int32_t *block_table, const int32_t *seq_lens, void *O,
+                               float *lse, int B, int Hq, int Hkv, int n_q, int d,
+                               int block_size, int max_blocks_per_seq, int num_blocks,
+                               int max_seq_len, int causal, float scale, attn_dtype in_dtype,
+                               attn_dtype out_dtype, void *stream) {
+    t_last_launches = 0;
+    if (!Q || !Kcache || !Vcache || !block_table || !seq_lens || !O)
+        return ATTN_ERR_INVALID;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || n_q <= 0 || d <= 0 || Hq % Hkv != 0 ||
+        block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_seq_len <= 0)
+        return ATTN_ERR_INVALID;
+    if (static_cast<long long>(max_seq_len) >
+        static_cast<long long>(max_blocks_per_seq) * block_size)
+        return ATTN_ERR_INVALID;
+    if (causal && n_q > max_seq_len)
+        return ATTN_ERR_INVALID;
+    if (!isfinite(scale))
+        return ATTN_ERR_INVALID;
+    if (!aligned(Q, 16) || !aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(O, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)))
+        return ATTN_ERR_INVALID;
+    if (!is16(in_dtype) || !is_out(out_dtype) || (d != 64 && d != 128 && d != 256) ||
+        (block_size != 16 && block_size != 32 && block_size != 64))
+        return ATTN_ERR_UNSUPPORTED;
+    const long long nqb = (n_q + 127) / 128;
+    if (nqb * B * Hq > 0x7fffffffLL)
+        return ATTN_ERR_UNSUPPORTED;
+    unsigned *err = err_word();
+    if (!err)
+        return ATTN_ERR_CUDA;
+    attn::PrefillArgs a{Q, Kcache, Vcache, O, lse, B, Hq, Hkv, n_q, max_seq_len, d,
+                        causal ? 1 : 0, scale, in_dtype == ATTN_BF16, false,
+                        out_code(out_dtype), nullptr, nullptr, nullptr, err};
+    a.paged = true;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.block_size = block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.max_seq_len = max_seq_len;
+    if (attn::prefill_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = 1;
+    return ATTN_OK;
+}
+
 size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int max_seq_len) {
     if (num_seqs <= 0 || Hq <= 0 || d <= 0 || max_seq_len < 0)
         return 0;

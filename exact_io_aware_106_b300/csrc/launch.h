@@ -24,6 +24,11 @@ struct PrefillArgs {
     const float *k_scale;
     const float *v_scale;
     unsigned *err;
+    // prefill over a block-paged cache (K, V are then the caches)
+    bool paged = false;
+    const int32_t *block_table = nullptr;
+    const int32_t *seq_lens = nullptr;
+    int block_size = 0, max_blocks = 0, num_blocks = 0, max_seq_len = 0;
 };
 
 struct DecodeArgs {

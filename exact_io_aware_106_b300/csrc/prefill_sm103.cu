@@ -103,6 +103,158 @@ struct Scales {
     const float *v;
 };
 
+// Block-paged K/V (prefill over a cache): per sequence b, seq_lens[b]
+// tokens, token t in slot t % bs of block table[b][t / bs], layout
+// [num_blocks, Hkv, bs, d].  Unused (null) for dense K/V.
+struct Paged {
+    const int32_t *table;
+    const int32_t *lens;
+    const uint8_t *vcache;
+    int bs, max_blocks, num_blocks, max_len;
+};
+
+// Whole-warp producer of the K and V blocks (BN keys, 16-bit, D) of one
+// (sequence, KV head) from a block-paged cache: one TMA box (16 tokens x 64
+// elements) per 16-token unit and 128-byte panel, into the same swizzled
+// stage layout dense tiles have.  Units past the sequence end read a block
+// coordinate past the tensor, which TMA fills with zeros.  The one V unit
+// that holds the sequence end is copied with plain loads and its rows past
+// the end zeroed: their p is 0, and 0 * (stale non-finite cache contents)
+// must not reach u.  K rows past the end need no care -- their scores are
+// replaced by -inf.  Block ids are fetched one key block ahead, one lane per
+// unit.  Returns false if a wait gave up.
+template <int D, int BN, int NK, int NV>
+__device__ __forceinline__ void paged_kv_producer(
+    const Paged &pg, int b, int hkv, int Hkv, int n_kv, int nb_max, const CUtensorMap *tm_k,
+    const CUtensorMap *tm_v, uint32_t sK, uint32_t sV, uint32_t kfull0, uint32_t kempty0,
+    uint32_t vfull0, uint32_t vempty0, volatile int *abort_flag, unsigned *err, int lane) {
+    constexpr int UPB = BN / 16;                // 16-token units per key block
+    constexpr int PANELS = D / 64;
+    constexpr int STAGE = BN * D * 2;
+    constexpr int UNIT = 16 * 128 * PANELS;     // bytes of one unit
+    const unsigned full = 0xffffffffu;
+    const int32_t *trow = pg.table + static_cast<size_t>(b) * pg.max_blocks;
+    auto unit_blk = [&](int j) -> int {
+        const int tok = j * BN + 16 * lane;
+        if (lane >= UPB || tok >= n_kv)
+            return -1;
+        const int phys = trow[tok / pg.bs];
+        return (phys >= 0 && phys < pg.num_blocks) ? phys : -2;
+    };
+    int nxt = nb_max > 0 ? unit_blk(0) : -1;
+    bool bad = false;
+    int k_issued = 0, v_issued = 0;
+    for (int j = 0; j < nb_max; ++j) {
+        const int cur = nxt;
+        if (j + 1 < nb_max)
+            nxt = unit_blk(j + 1);
+        bad |= cur == -2;
+        // ---- K
+        const int ks = j % NK;
+        int ok = 1;
+        if (j >= NK) {
+            if (lane == 0)
+                ok = mbar_wait(kempty0 + 8u * ks, ((j / NK) - 1) & 1, abort_flag, err);
+            ok = __shfl_sync(full, ok, 0);
+        }
+        if (!ok)
+            break;
+        if (lane == 0)
+            mbar_arrive_expect_tx(kfull0 + 8u * ks, STAGE);
+#pragma unroll
+        for (int u = 0; u < UPB; ++u) {
+            const int blk = __shfl_sync(full, cur, u);
+            if (lane == 0) {
+                const int z = blk >= 0 ? blk : pg.num_blocks;
+                const int y = hkv * pg.bs + (j * BN + 16 * u) % pg.bs;
+#pragma unroll
+                for (int p = 0; p < PANELS; ++p)
+                    tma_load_3d(sK + ks * STAGE + p * BN * 128 + u * 16 * 128, tm_k,
+                                kfull0 + 8u * ks, p * 64, y, z);
+            }
+        }
+        k_issued = j + 1;
+        // ---- V
+        const int vs = j % NV;
+        if (j >= NV) {
+            if (lane == 0)
+                ok = mbar_wait(vempty0 + 8u * vs, ((j / NV) - 1) & 1, abort_flag, err);
+            ok = __shfl_sync(full, ok, 0);
+        }
+        if (!ok)
+            break;
+        const int rem = n_kv - j * BN; // keys of this block inside the sequence
+        const int up = (rem > 0 && rem < BN && (rem & 15) != 0) ? (rem >> 4) : -1;
+        if (up >= 0) {
+            const int blk = __shfl_sync(full, cur, up);
+            const int nval = rem & 15;
+            const size_t row0 = (static_cast<size_t>(blk >= 0 ? blk : 0) * Hkv + hkv) * pg.bs +
+                                (j * BN + 16 * up) % pg.bs;
+            for (int i = lane; i < 16 * (D / 8); i += 32) {
+                const int r = i / (D / 8), c = i % (D / 8);
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (r < nval && blk >= 0)
+                    v = *reinterpret_cast<const uint4 *>(pg.vcache + (row0 + r) * (D * 2) + c * 16);
+                sts_v4(sV + vs * STAGE + (c / 8) * (BN * 128) + swz_offset<128>(up * 16 + r, c % 8),
+                       v.x, v.y, v.z, v.w);
+            }
+            fence_proxy_async_smem(); // generic writes -> tensor-core reads
+            __syncwarp();
+        }
+        if (lane == 0)
+            mbar_arrive_expect_tx(vfull0 + 8u * vs, (UPB - (up >= 0 ? 1 : 0)) * UNIT);
+#pragma unroll
+        for (int u = 0; u < UPB; ++u) {
+            const int blk = __shfl_sync(full, cur, u);
+            if (lane == 0 && u != up) {
+                const int z = blk >= 0 ? blk : pg.num_blocks;
+                const int y = hkv * pg.bs + (j * BN + 16 * u) % pg.bs;
+#pragma unroll
+                for (int p = 0; p < PANELS; ++p)
+                    tma_load_3d(sV + vs * STAGE + p * BN * 128 + u * 16 * 128, tm_v,
+                                vfull0 + 8u * vs, p * 64, y, z);
+            }
+        }
+        v_issued = j + 1;
+    }
+    if (__any_sync(full, bad) && lane == 0)
+        atomicOr(err, DERR_INDEX);
+    if (lane == 0 && *abort_flag) { // let in-flight copies land before the CTA exits
+        for (int u = max(0, k_issued - NK); u < k_issued; ++u)
+            mbar_wait_drain(kfull0 + 8u * (u % NK), (u / NK) & 1);
+        for (int u = max(0, v_issued - NV); u < v_issued; ++u)
+            mbar_wait_drain(vfull0 + 8u * (u % NV), (u / NV) & 1);
+    }
+}
+
+// A paged sequence whose length the table cannot hold (or that is shorter
+// than its causal query rows): the CTA writes O = 0, lse = NaN and records
+// the error.  Returns the sequence length, or -1 after handling an invalid one.
+template <int D, int OUT>
+__device__ __forceinline__ int paged_len_or_reject(const Paged &pg, const Shape &sh, int b, int bh,
+                                                   int row0, int rows, void *O, float *lse,
+                                                   unsigned *err) {
+    const int len = pg.lens[b];
+    const bool ok = len >= (sh.causal ? sh.n_q : 1) && len <= pg.max_len &&
+                    (len + pg.bs - 1) / pg.bs <= pg.max_blocks;
+    if (ok)
+        return len;
+    if (threadIdx.x == 0)
+        atomicOr(err, DERR_INDEX);
+    const int r_hi = min(row0 + rows, sh.n_q);
+    for (int i = threadIdx.x; i < (r_hi - row0) * D; i += blockDim.x) {
+        const size_t o = (static_cast<size_t>(bh) * sh.n_q + row0) * D + i;
+        if constexpr (OUT == 2)
+            static_cast<float *>(O)[o] = 0.f;
+        else
+            static_cast<uint16_t *>(O)[o] = 0;
+    }
+    if (lse != nullptr)
+        for (int i = threadIdx.x; i < r_hi - row0; i += blockDim.x)
+            lse[static_cast<size_t>(bh) * sh.n_q + row0 + i] = __int_as_float(0x7fc00000);
+    return -1;
+}
+
 __device__ __forceinline__ int tile_blocks(const Shape &sh, int q0, int t) {
     const int r0 = q0 + t * BM;
     if (r0 >= sh.n_q)
@@ -171,13 +323,16 @@ __device__ __forceinline__ void widen_v_tile(uint32_t src, uint32_t dst, int lan
     }
 }
 
-template <int D, bool BF16, bool F8, int OUT>
+template <int D, bool BF16, bool F8, bool PAGED, int OUT>
 __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, void *__restrict__ O,
-                   float *__restrict__ lse, const Shape sh, const Scales sc, unsigned *err) {
+                   float *__restrict__ lse, const Shape sh_in, const Scales sc, const Paged pg,
+                   unsigned *err) {
     using C = Cfg<D, F8>;
+    static_assert(!(PAGED && F8), "paged prefill reads 16-bit caches");
+    Shape sh = sh_in;
     constexpr bool PB = F8 ? false : BF16; // format of P and of the V operand
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (128-byte swizzle atoms repeat every 1 KB)
@@ -216,6 +371,12 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     const int b = bh / sh.Hq, h = bh % sh.Hq;
     const int bkv = b * sh.Hkv + h / sh.G;
     const int q0 = qb * (NT * BM);
+    if constexpr (PAGED) {
+        const int len = paged_len_or_reject<D, OUT>(pg, sh, b, bh, q0, NT * BM, O, lse, err);
+        if (len < 0)
+            return;
+        sh.n_kv = len;
+    }
     int nb[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t)
@@ -260,7 +421,25 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kProducerWarp) {
+    if (warp == kProducerWarp && PAGED) {
+        // ================================================= paged producer
+        if (lane == 0) {
+            int ntiles = 0;
+            for (int t = 0; t < NT; ++t)
+                ntiles += nb[t] > 0;
+            mbar_arrive_expect_tx(b_qfull, ntiles * C::Q_TILE_BYTES);
+            for (int t = 0; t < NT; ++t)
+                if (nb[t] > 0)
+                    for (int p = 0; p < C::QK_PANELS; ++p)
+                        tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q, b_qfull,
+                                    p * 64, q0 + t * BM, bh);
+        }
+        paged_kv_producer<D, BN, C::NK, C::NV>(pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb_max, &tm_k,
+                                               &tm_v, sK, sV, b_kfull(0), b_kempty(0),
+                                               b_vfull(0), b_vempty(0), abort_flag, err, lane);
+        if (lane == 0 && *abort_flag)
+            mbar_wait_drain(b_qfull, 0);
+    } else if (warp == kProducerWarp) {
         // ================================================= TMA producer
         if (lane == 0) {
             constexpr int XP = C::PW / C::EB; // elements per Q/K panel row
@@ -637,14 +816,16 @@ __device__ __forceinline__ int tile_blocks(const pf::Shape &sh, int r0) {
     return min(nkb, (r_last + (sh.n_kv - sh.n_q)) / BN + 1);
 }
 
-template <bool BF16, bool F8, int OUT>
+template <bool BF16, bool F8, bool PAGED, int OUT>
 __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
     prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, void *__restrict__ O,
-                        float *__restrict__ lse, const pf::Shape sh, const pf::Scales sc,
-                        unsigned *err) {
+                        float *__restrict__ lse, const pf::Shape sh_in, const pf::Scales sc,
+                        const pf::Paged pg, unsigned *err) {
     using C = Cfg<F8>;
+    static_assert(!(PAGED && F8), "paged prefill reads 16-bit caches");
+    pf::Shape sh = sh_in;
     constexpr bool PB = F8 ? false : BF16;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -676,6 +857,12 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
     const int b = bh / sh.Hq, h = bh % sh.Hq;
     const int bkv = b * sh.Hkv + h / sh.G;
     const int r0 = qb * BM;
+    if constexpr (PAGED) {
+        const int len = pf::paged_len_or_reject<D, OUT>(pg, sh, b, bh, r0, BM, O, lse, err);
+        if (len < 0)
+            return;
+        sh.n_kv = len;
+    }
     const int nb = tile_blocks(sh, r0);
 
     if (threadIdx.x == 0) {
@@ -716,7 +903,19 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kProducerWarp) {
+    if (warp == kProducerWarp && PAGED) {
+        // ================================================= paged producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(b_qfull, C::Q_BYTES);
+            for (int p = 0; p < C::QK_PANELS; ++p)
+                tma_load_3d(sQ + p * BM * C::PW, &tm_q, b_qfull, p * 64, r0, bh);
+        }
+        pf::paged_kv_producer<D, BN, NK, NV>(pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb, &tm_k, &tm_v,
+                                             sK, sV, b_kfull(0), b_kempty(0), b_vfull(0),
+                                             b_vempty(0), abort_flag, err, lane);
+        if (lane == 0 && *abort_flag)
+            mbar_wait_drain(b_qfull, 0);
+    } else if (warp == kProducerWarp) {
         // ================================================= TMA producer
         if (lane == 0) {
             constexpr int XP = C::PW / C::EB;
@@ -1024,17 +1223,50 @@ static pf::Shape make_shape(const PrefillArgs &a, int rows_per_cta) {
     return sh;
 }
 
-template <int D, bool BF16, bool F8, int OUT>
+// Cache [num_blocks, Hkv, bs, d] (16-bit) viewed as {d, Hkv * bs, num_blocks},
+// box 64 x 16 x 1, 128-byte swizzle.
+static bool make_cache_map(CUtensorMap *m, const void *ptr, const PrefillArgs &a) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(a.d),
+                              static_cast<uint64_t>(a.Hkv) * a.block_size,
+                              static_cast<uint64_t>(a.num_blocks)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(a.d) * 2,
+                                 static_cast<uint64_t>(a.Hkv) * a.block_size * a.d * 2};
+    const uint32_t box[3] = {64, 16, 1};
+    return make_tmap_3d(m, ptr, a.bf16 ? TmapElem::BF16 : TmapElem::F16, dims, strides, box, 128);
+}
+
+static bool make_kv_maps(CUtensorMap *mk, CUtensorMap *mv, const PrefillArgs &a, int D, bool bf16,
+                         bool f8, int rows) {
+    if (a.paged)
+        return make_cache_map(mk, a.K, a) && make_cache_map(mv, a.V, a);
+    return make_map(mk, a.K, D, a.n_kv, a.B * a.Hkv, bf16, f8, rows) &&
+           make_map(mv, a.V, D, a.n_kv, a.B * a.Hkv, bf16, f8, rows);
+}
+
+static pf::Paged make_paged(const PrefillArgs &a) {
+    pf::Paged pg{};
+    if (a.paged) {
+        pg.table = a.block_table;
+        pg.lens = a.seq_lens;
+        pg.vcache = static_cast<const uint8_t *>(a.V);
+        pg.bs = a.block_size;
+        pg.max_blocks = a.max_blocks;
+        pg.num_blocks = a.num_blocks;
+        pg.max_len = a.max_seq_len;
+    }
+    return pg;
+}
+
+template <int D, bool BF16, bool F8, bool PAGED, int OUT>
 static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
     using C = pf::Cfg<D, F8>;
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, a.Q, D, a.n_q, a.B * a.Hq, BF16, F8, pf::BM) ||
-        !make_map(&mk, a.K, D, a.n_kv, a.B * a.Hkv, BF16, F8, pf::BN) ||
-        !make_map(&mv, a.V, D, a.n_kv, a.B * a.Hkv, BF16, F8, pf::BN))
+        !make_kv_maps(&mk, &mv, a, D, BF16, F8, pf::BN))
         return cudaErrorInvalidValue;
     const pf::Shape sh = make_shape(a, pf::NT * pf::BM);
     const pf::Scales sc{a.q_scale, a.k_scale, a.v_scale};
-    auto kern = pf::prefill_kernel<D, BF16, F8, OUT>;
+    auto kern = pf::prefill_kernel<D, BF16, F8, PAGED, OUT>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
@@ -1043,21 +1275,20 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidValue;
     kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(mq, mk, mv, a.O, a.lse, sh, sc,
-                                                                  a.err);
+                                                                  make_paged(a), a.err);
     return cudaGetLastError();
 }
 
-template <bool BF16, bool F8, int OUT>
+template <bool BF16, bool F8, bool PAGED, int OUT>
 static cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t st) {
     using C = pfw::Cfg<F8>;
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, a.Q, pfw::D, a.n_q, a.B * a.Hq, BF16, F8, pfw::BM) ||
-        !make_map(&mk, a.K, pfw::D, a.n_kv, a.B * a.Hkv, BF16, F8, pfw::BN) ||
-        !make_map(&mv, a.V, pfw::D, a.n_kv, a.B * a.Hkv, BF16, F8, pfw::BN))
+        !make_kv_maps(&mk, &mv, a, pfw::D, BF16, F8, pfw::BN))
         return cudaErrorInvalidValue;
     const pf::Shape sh = make_shape(a, pfw::BM);
     const pf::Scales sc{a.q_scale, a.k_scale, a.v_scale};
-    auto kern = pfw::prefill_wide_kernel<BF16, F8, OUT>;
+    auto kern = pfw::prefill_wide_kernel<BF16, F8, PAGED, OUT>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
@@ -1066,32 +1297,36 @@ static cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t st) {
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidValue;
     kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(mq, mk, mv, a.O, a.lse, sh, sc,
-                                                                  a.err);
+                                                                  make_paged(a), a.err);
     return cudaGetLastError();
 }
 
-template <int D, bool BF16, bool F8>
+template <int D, bool BF16, bool F8, bool PAGED>
 static cudaError_t launch_out(const PrefillArgs &a, cudaStream_t st) {
     if constexpr (D == 256) {
         switch (a.out_dtype) {
-        case 0: return launch_prefill_wide<BF16, F8, 0>(a, st);
-        case 1: return launch_prefill_wide<BF16, F8, 1>(a, st);
-        default: return launch_prefill_wide<BF16, F8, 2>(a, st);
+        case 0: return launch_prefill_wide<BF16, F8, PAGED, 0>(a, st);
+        case 1: return launch_prefill_wide<BF16, F8, PAGED, 1>(a, st);
+        default: return launch_prefill_wide<BF16, F8, PAGED, 2>(a, st);
         }
     } else {
         switch (a.out_dtype) {
-        case 0: return launch_prefill_t<D, BF16, F8, 0>(a, st);
-        case 1: return launch_prefill_t<D, BF16, F8, 1>(a, st);
-        default: return launch_prefill_t<D, BF16, F8, 2>(a, st);
+        case 0: return launch_prefill_t<D, BF16, F8, PAGED, 0>(a, st);
+        case 1: return launch_prefill_t<D, BF16, F8, PAGED, 1>(a, st);
+        default: return launch_prefill_t<D, BF16, F8, PAGED, 2>(a, st);
         }
     }
 }
 
 template <int D>
 static cudaError_t launch_d(const PrefillArgs &a, cudaStream_t st) {
+    if (a.paged)
+        return a.bf16 ? launch_out<D, true, false, true>(a, st)
+                      : launch_out<D, false, false, true>(a, st);
     if (a.e4m3)
-        return launch_out<D, false, true>(a, st);
-    return a.bf16 ? launch_out<D, true, false>(a, st) : launch_out<D, false, false>(a, st);
+        return launch_out<D, false, true, false>(a, st);
+    return a.bf16 ? launch_out<D, true, false, false>(a, st)
+                  : launch_out<D, false, false, false>(a, st);
 }
 
 cudaError_t prefill_launch(const PrefillArgs &a, cudaStream_t st) {

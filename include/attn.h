@@ -89,6 +89,32 @@ ATTN_API attn_status attn_prefill(const void *Q, const void *K, const void *V, v
                          attn_dtype out_dtype, const float *q_scale,
                          const float *k_scale, const float *v_scale, void *stream);
 
+/* Prefill over a block-paged KV cache: prefix caching / chunked prefill
+ * (code-journey.com, "Attention co-design", short ISL over a long cached
+ * prefix; papanda925.com, block-wise KV cache).  The n_q new tokens of each
+ * sequence are its last n_q; their K/V must already be in the cache
+ * (attn_kv_append).
+ *   Q        [B, Hq, n_q, d]                    in_dtype (F16 / BF16)
+ *   Kcache,
+ *   Vcache   [num_blocks, Hkv, block_size, d]    in_dtype
+ *   block_table [B, max_blocks_per_seq] int32, seq_lens [B] int32: token t
+ *            of sequence b is slot t % block_size of block
+ *            block_table[b][t / block_size]; seq_lens[b] is the sequence's
+ *            total length (prefix + n_q), in [n_q, max_seq_len] when causal
+ *   O        [B, Hq, n_q, d] out_dtype;  lse [B, Hq, n_q] fp32 or NULL
+ * Causal rows are aligned bottom-right: new token i of sequence b sees
+ * cached token j iff j <= i + seq_lens[b] - n_q.  d in {64, 128, 256};
+ * block_size in {16, 32, 64}.  A sequence whose length or block entries the
+ * table cannot hold gets O = 0, lse = NaN, and the device error word
+ * records ATTN_ERR_INVALID.  One kernel launch. */
+ATTN_API attn_status attn_prefill_paged(const void *Q, const void *Kcache, const void *Vcache,
+                                        const int32_t *block_table, const int32_t *seq_lens,
+                                        void *O, float *lse, int B, int Hq, int Hkv, int n_q,
+                                        int d, int block_size, int max_blocks_per_seq,
+                                        int num_blocks, int max_seq_len, int causal,
+                                        float scale, attn_dtype in_dtype,
+                                        attn_dtype out_dtype, void *stream);
+
 /* Bytes of caller-provided device workspace attn_decode needs for these
  * sizes (split-KV partial states).  max_seq_len bounds every seq_lens[s]. */
 ATTN_API size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d,

@@ -71,6 +71,26 @@ def test_prefill_host_validation(L):
     assert L.attn_last_launch_count() == 0
 
 
+def _prefill_paged(L, **kw):
+    a = dict(B=2, Hq=4, Hkv=2, nq=64, d=128, bs=16, mb=8, nb=32, msl=128, causal=1, scale=0.1,
+             ind=1, outd=1, bt=FAKE)
+    a.update(kw)
+    return L.attn_prefill_paged(FAKE, FAKE, FAKE, a["bt"], FAKE, FAKE, None, a["B"], a["Hq"],
+                                a["Hkv"], a["nq"], a["d"], a["bs"], a["mb"], a["nb"], a["msl"],
+                                a["causal"], a["scale"], a["ind"], a["outd"], None)
+
+
+def test_prefill_paged_host_validation(L):
+    assert _prefill_paged(L, bt=None) == attn.ERR_INVALID
+    assert _prefill_paged(L, Hq=6, Hkv=4) == attn.ERR_INVALID
+    assert _prefill_paged(L, msl=8 * 16 + 1) == attn.ERR_INVALID       # longer than the table
+    assert _prefill_paged(L, nq=200) == attn.ERR_INVALID               # causal, n_q > max length
+    assert _prefill_paged(L, ind=3) == attn.ERR_UNSUPPORTED            # E4M3 cache
+    assert _prefill_paged(L, d=80) == attn.ERR_UNSUPPORTED
+    assert _prefill_paged(L, bs=8, msl=64) == attn.ERR_UNSUPPORTED
+    assert L.attn_last_launch_count() == 0
+
+
 def _decode(L, **kw):
     a = dict(S=4, Hq=8, Hkv=2, d=128, bs=16, mb=8, nb=32, msl=128, scale=0.1, qd=1, kvd=1,
              od=1, ks=None, vs=None, ws=FAKE, wsb=1 << 30, bt=FAKE)
