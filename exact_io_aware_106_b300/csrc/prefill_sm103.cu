@@ -122,7 +122,7 @@ struct Paged {
 // the end zeroed: their p is 0, and 0 * (stale non-finite cache contents)
 // must not reach u.  K rows past the end need no care -- their scores are
 // replaced by -inf.  Block ids are fetched one key block ahead, one lane per
-// unit.  Returns false if a wait gave up.
+// unit; lane u issues unit u's boxes.
 template <int D, int BN, int NK, int NV>
 __device__ __forceinline__ void paged_kv_producer(
     const Paged &pg, int b, int hkv, int Hkv, int n_kv, int nb_max, const CUtensorMap *tm_k,
@@ -161,17 +161,15 @@ __device__ __forceinline__ void paged_kv_producer(
             break;
         if (lane == 0)
             mbar_arrive_expect_tx(kfull0 + 8u * ks, STAGE);
+        __syncwarp();
+        // lane u issues unit u's boxes: one instruction starts every unit's copy
+        const int z = cur >= 0 ? cur : pg.num_blocks;
+        const int y = hkv * pg.bs + (j * BN + 16 * lane) % pg.bs;
+        if (lane < UPB) {
 #pragma unroll
-        for (int u = 0; u < UPB; ++u) {
-            const int blk = __shfl_sync(full, cur, u);
-            if (lane == 0) {
-                const int z = blk >= 0 ? blk : pg.num_blocks;
-                const int y = hkv * pg.bs + (j * BN + 16 * u) % pg.bs;
-#pragma unroll
-                for (int p = 0; p < PANELS; ++p)
-                    tma_load_3d(sK + ks * STAGE + p * BN * 128 + u * 16 * 128, tm_k,
-                                kfull0 + 8u * ks, p * 64, y, z);
-            }
+            for (int p = 0; p < PANELS; ++p)
+                tma_load_3d(sK + ks * STAGE + p * BN * 128 + lane * 16 * 128, tm_k,
+                            kfull0 + 8u * ks, p * 64, y, z);
         }
         k_issued = j + 1;
         // ---- V
@@ -203,17 +201,12 @@ __device__ __forceinline__ void paged_kv_producer(
         }
         if (lane == 0)
             mbar_arrive_expect_tx(vfull0 + 8u * vs, (UPB - (up >= 0 ? 1 : 0)) * UNIT);
+        __syncwarp();
+        if (lane < UPB && lane != up) {
 #pragma unroll
-        for (int u = 0; u < UPB; ++u) {
-            const int blk = __shfl_sync(full, cur, u);
-            if (lane == 0 && u != up) {
-                const int z = blk >= 0 ? blk : pg.num_blocks;
-                const int y = hkv * pg.bs + (j * BN + 16 * u) % pg.bs;
-#pragma unroll
-                for (int p = 0; p < PANELS; ++p)
-                    tma_load_3d(sV + vs * STAGE + p * BN * 128 + u * 16 * 128, tm_v,
-                                vfull0 + 8u * vs, p * 64, y, z);
-            }
+            for (int p = 0; p < PANELS; ++p)
+                tma_load_3d(sV + vs * STAGE + p * BN * 128 + lane * 16 * 128, tm_v,
+                            vfull0 + 8u * vs, p * 64, y, z);
         }
         v_issued = j + 1;
     }
@@ -253,6 +246,25 @@ __device__ __forceinline__ int paged_len_or_reject(const Paged &pg, const Shape 
         for (int i = threadIdx.x; i < r_hi - row0; i += blockDim.x)
             lse[static_cast<size_t>(bh) * sh.n_q + row0 + i] = __int_as_float(0x7fc00000);
     return -1;
+}
+
+// CTA index -> (query block, batch, head).  Dense: query blocks in
+// descending order (heaviest causal work first), (batch, head) fastest.
+// Paged: (batch, KV head) slowest, then query block, then the G heads.
+__device__ __forceinline__ void work_item(const Shape &sh, bool paged, int idx, int &qb, int &b,
+                                          int &h) {
+    if (!paged) {
+        const int BH = sh.B * sh.Hq;
+        qb = sh.nqb - 1 - idx / BH;
+        b = (idx % BH) / sh.Hq;
+        h = (idx % BH) % sh.Hq;
+    } else {
+        const int per_kv = sh.nqb * sh.G;
+        const int kvi = idx / per_kv, rem = idx % per_kv;
+        qb = sh.nqb - 1 - rem / sh.G;
+        b = kvi / sh.Hkv;
+        h = (kvi % sh.Hkv) * sh.G + rem % sh.G;
+    }
 }
 
 __device__ __forceinline__ int tile_blocks(const Shape &sh, int q0, int t) {
@@ -364,11 +376,14 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- work item: heaviest query blocks first (causal work grows with q)
-    const int BH = sh.B * sh.Hq;
-    const int qb = sh.nqb - 1 - static_cast<int>(blockIdx.x) / BH;
-    const int bh = static_cast<int>(blockIdx.x) % BH;
-    const int b = bh / sh.Hq, h = bh % sh.Hq;
+    // ---- work item.  Dense: heaviest query blocks first (causal work grows
+    // with q).  Paged: the CTAs sharing one (sequence, KV head) -- all its
+    // query blocks and the G heads of the group -- are adjacent, so that its
+    // cached K/V (a long prefix, read by every one of them) streams from
+    // DRAM about once and is reused from L2.
+    int qb, b, h;
+    work_item(sh, PAGED, static_cast<int>(blockIdx.x), qb, b, h);
+    const int bh = b * sh.Hq + h;
     const int bkv = b * sh.Hkv + h / sh.G;
     const int q0 = qb * (NT * BM);
     if constexpr (PAGED) {
@@ -851,10 +866,9 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int BH = sh.B * sh.Hq;
-    const int qb = sh.nqb - 1 - static_cast<int>(blockIdx.x) / BH; // heaviest first
-    const int bh = static_cast<int>(blockIdx.x) % BH;
-    const int b = bh / sh.Hq, h = bh % sh.Hq;
+    int qb, b, h;
+    pf::work_item(sh, PAGED, static_cast<int>(blockIdx.x), qb, b, h);
+    const int bh = b * sh.Hq + h;
     const int bkv = b * sh.Hkv + h / sh.G;
     const int r0 = qb * BM;
     if constexpr (PAGED) {
