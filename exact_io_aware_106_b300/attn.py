@@ -20,7 +20,7 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 _DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.float8_e4m3fn: 3}
 
 EXPORTS = ("attn_prefill", "attn_prefill_paged", "attn_decode_workspace_bytes", "attn_decode",
-           "attn_kv_append",
+           "attn_decode_tokens", "attn_kv_append",
            "attn_last_error", "attn_status_str", "attn_last_launch_count",
            "attn_decode_static_ws")
 
@@ -56,6 +56,10 @@ def lib():
         L.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                   i32, f32, i32, i32, i32, vp, vp, vp, sz, vp]
         L.attn_decode.restype = i32
+        L.attn_decode_tokens.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                         i32, i32, i32, i32, f32, i32, i32, i32, vp, vp, vp, sz,
+                                         vp]
+        L.attn_decode_tokens.restype = i32
         L.attn_kv_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                      i32, i32, i32, vp, vp, vp]
         L.attn_kv_append.restype = i32
@@ -192,6 +196,37 @@ def decode(q, Kc, Vc, block_table, seq_lens, max_seq_len: int, scale: float | No
                            _DT[Kc.dtype], _DT[O.dtype], _ptr(k_scale), _ptr(v_scale),
                            _ptr(workspace), workspace.numel(), _stream(stream))
     _check("attn_decode", st)
+    return O, lse
+
+
+def decode_tokens(q, Kc, Vc, block_table, seq_lens, max_seq_len: int, scale: float | None = None,
+                  k_scale=None, v_scale=None, out_dtype=None, O=None, lse=None, workspace=None,
+                  want_lse: bool = True, stream=None):
+    """n_new new tokens per sequence (its last n_new, already in the cache):
+    q [S,Hq,n_new,d] against the paged cache.  Returns (O [S,Hq,n_new,d],
+    lse [S,Hq,n_new])."""
+    _cuda(q, Kc, Vc, block_table, seq_lens, k_scale, v_scale)
+    S, Hq, T, d = q.shape
+    num_blocks, Hkv, bs, _ = Kc.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out_dtype is None:
+        out_dtype = q.dtype
+    if O is None:
+        O = torch.empty((S, Hq, T, d), dtype=out_dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((S, Hq, T), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(S * T, Hq, d, max_seq_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _cuda(O, lse, workspace)
+    st = lib().attn_decode_tokens(_ptr(q), _ptr(Kc), _ptr(Vc), _ptr(block_table),
+                                  _ptr(seq_lens), _ptr(O), _ptr(lse), S, T, Hq, Hkv, d, bs,
+                                  block_table.shape[1], num_blocks, int(max_seq_len),
+                                  float(scale), _DT[q.dtype], _DT[Kc.dtype], _DT[O.dtype],
+                                  _ptr(k_scale), _ptr(v_scale), _ptr(workspace),
+                                  workspace.numel(), _stream(stream))
+    _check("attn_decode_tokens", st)
     return O, lse
 
 

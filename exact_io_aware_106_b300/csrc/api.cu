@@ -150,9 +150,14 @@ size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int max_seq_len)
     return attn::decode_workspace_bytes(num_seqs, Hq, d, max_seq_len);
 }
 
-attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache,
+} // extern "C"
+
+namespace {
+
+// Shared by attn_decode (T = 1) and attn_decode_tokens.
+attn_status decode_impl(const void *q, const void *Kcache, const void *Vcache,
                         const int32_t *block_table, const int32_t *seq_lens, void *O, float *lse,
-                        int num_seqs, int Hq, int Hkv, int d, int block_size,
+                        int num_seqs, int T, int Hq, int Hkv, int d, int block_size,
                         int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
                         attn_dtype q_dtype, attn_dtype kv_dtype, attn_dtype out_dtype,
                         const float *k_scale, const float *v_scale, void *workspace,
@@ -160,11 +165,13 @@ attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache,
     t_last_launches = 0;
     if (!q || !Kcache || !Vcache || !block_table || !seq_lens || !O || !workspace)
         return ATTN_ERR_INVALID;
-    if (num_seqs <= 0 || num_seqs > 65535 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 ||
+    if (num_seqs <= 0 || num_seqs > 65535 || T <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 ||
         block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_seq_len < 0)
         return ATTN_ERR_INVALID;
     if (static_cast<long long>(max_seq_len) >
         static_cast<long long>(max_blocks_per_seq) * block_size)
+        return ATTN_ERR_INVALID;
+    if (T > 1 && max_seq_len < T)
         return ATTN_ERR_INVALID;
     if (!isfinite(scale))
         return ATTN_ERR_INVALID;
@@ -176,12 +183,15 @@ attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache,
     if (e4 && (!k_scale || !v_scale))
         return ATTN_ERR_INVALID;
     if ((d != 64 && d != 128 && d != 256) ||
-        (block_size != 16 && block_size != 32 && block_size != 64) || Hq / Hkv > 16)
+        (block_size != 16 && block_size != 32 && block_size != 64) ||
+        static_cast<long long>(Hq / Hkv) * T > 16)
+        return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_seqs) * Hq * T > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
     if (!aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(q, 16) || !aligned(O, 4) ||
         !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return ATTN_ERR_INVALID;
-    if (workspace_bytes < attn::decode_workspace_bytes(num_seqs, Hq, d, max_seq_len))
+    if (workspace_bytes < attn::decode_workspace_bytes(num_seqs * T, Hq, d, max_seq_len))
         return ATTN_ERR_INVALID;
     unsigned *err = err_word();
     if (!err)
@@ -190,10 +200,41 @@ attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache,
                        block_size, max_blocks_per_seq, num_blocks, max_seq_len, scale,
                        q_dtype == ATTN_BF16, e4, out_code(out_dtype), k_scale, v_scale,
                        workspace, err};
+    a.T = T;
     if (attn::decode_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     t_last_launches = 2;
     return ATTN_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache,
+                        const int32_t *block_table, const int32_t *seq_lens, void *O, float *lse,
+                        int num_seqs, int Hq, int Hkv, int d, int block_size,
+                        int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
+                        attn_dtype q_dtype, attn_dtype kv_dtype, attn_dtype out_dtype,
+                        const float *k_scale, const float *v_scale, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    return decode_impl(q, Kcache, Vcache, block_table, seq_lens, O, lse, num_seqs, 1, Hq, Hkv,
+                       d, block_size, max_blocks_per_seq, num_blocks, max_seq_len, scale, q_dtype,
+                       kv_dtype, out_dtype, k_scale, v_scale, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_decode_tokens(const void *q, const void *Kcache, const void *Vcache,
+                               const int32_t *block_table, const int32_t *seq_lens, void *O,
+                               float *lse, int num_seqs, int n_new, int Hq, int Hkv, int d,
+                               int block_size, int max_blocks_per_seq, int num_blocks,
+                               int max_seq_len, float scale, attn_dtype q_dtype,
+                               attn_dtype kv_dtype, attn_dtype out_dtype, const float *k_scale,
+                               const float *v_scale, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+    return decode_impl(q, Kcache, Vcache, block_table, seq_lens, O, lse, num_seqs, n_new, Hq,
+                       Hkv, d, block_size, max_blocks_per_seq, num_blocks, max_seq_len, scale,
+                       q_dtype, kv_dtype, out_dtype, k_scale, v_scale, workspace,
+                       workspace_bytes, stream);
 }
 
 attn_status attn_kv_append(const void *k_new, const void *v_new, void *Kcache, void *Vcache,

@@ -50,13 +50,13 @@ template <int D, typename OutT>
 __global__ void __launch_bounds__(D)
     decode_combine_kernel(const float2 *__restrict__ ws_ml, const float *__restrict__ ws_u,
                           const int32_t *__restrict__ seq_lens, OutT *__restrict__ O,
-                          float *__restrict__ lse, int Hq, int block_size, int max_blocks,
-                          int max_seq_len, int tps, int max_splits) {
-    const int sh = blockIdx.x;
-    const int s = sh / Hq;
+                          float *__restrict__ lse, int Hq, int T, int block_size,
+                          int max_blocks, int max_seq_len, int tps, int max_splits) {
+    const int sh = blockIdx.x; // (sequence, query head, new token)
+    const int s = sh / (Hq * T);
     const int e = threadIdx.x;
     const int len = seq_lens[s];
-    const bool len_ok = len >= 0 && len <= max_seq_len &&
+    const bool len_ok = len >= (T > 1 ? T : 0) && len <= max_seq_len &&
                         (len + block_size - 1) / block_size <= max_blocks;
     const int nsplit = len_ok ? (len + tps - 1) / tps : 0;
     const float2 *ml = ws_ml + static_cast<size_t>(sh) * max_splits;
@@ -188,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
                       const int32_t *__restrict__ block_table,
                       const int32_t *__restrict__ seq_lens, const float *__restrict__ k_scale,
                       const float *__restrict__ v_scale, float2 *__restrict__ ws_ml,
-                      float *__restrict__ ws_u, int Hq, int G, int block_size, int max_blocks,
+                      float *__restrict__ ws_u, int Hq, int G, int T, int block_size,
+                      int max_blocks,
                       int num_blocks, int max_seq_len, int tps, int max_splits, float c,
                       unsigned *err) {
     using Ly = Lay<D, KV8>;
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     const int split = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int len = seq_lens[s];
-    const bool len_ok = len >= 0 && len <= max_seq_len &&
+    const bool len_ok = len >= (T > 1 ? T : 0) && len <= max_seq_len &&
                         (len + block_size - 1) / block_size <= max_blocks;
     if (!len_ok) { // the combine kernel zeroes this sequence's output
         if (split == 0 && hk == 0 && threadIdx.x == 0)
@@ -222,8 +223,11 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     const int t1 = min(len, t0 + tps);
     const int nunits = (t1 - t0 + kUnit - 1) / kUnit;
     const int head0 = hk * G;
-    const uint16_t *qg = static_cast<const uint16_t *>(q_) + static_cast<size_t>(s) * Hq * D +
-                         static_cast<size_t>(head0) * D;
+    // rows of the MMA tile: r = g * T + i for head head0 + g and new token i
+    // (q [num_seqs, Hq, T, d], so a group's rows are contiguous)
+    const int R = G * T;
+    const uint16_t *qg = static_cast<const uint16_t *>(q_) +
+                         (static_cast<size_t>(s) * Hq + head0) * T * D;
 
     if (threadIdx.x == 0) {
         s_flag = 0;
@@ -243,13 +247,13 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
         for (int i = threadIdx.x; i < 16 * (D / 8); i += kThreads) {
             const int r = i / (D / 8), c8 = i % (D / 8);
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < G)
+            if (r < R)
                 v = *reinterpret_cast<const uint4 *>(qg + static_cast<size_t>(r) * D + c8 * 8);
             *reinterpret_cast<uint4 *>(base + Ly::OFF_Q + r * Ly::QROW + c8 * 16) = v;
         }
     } else {
         float amax = 0.f;
-        for (int i = threadIdx.x; i < G * D; i += kThreads) {
+        for (int i = threadIdx.x; i < R * D; i += kThreads) {
             const float x = QBF16 ? __uint_as_float(static_cast<uint32_t>(qg[i]) << 16)
                                   : __half2float(__ushort_as_half(qg[i]));
             amax = fmaxf(amax, fabsf(x));
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
                 for (int k = 0; k < 2; ++k) { // elements 4t + 2k, 4t + 2k + 1
                     const int row = gg + 8 * h;
                     float x0 = 0.f, x1 = 0.f;
-                    if (row < G) {
+                    if (row < R) {
                         const int e = ch * 16 + 4 * tt + 2 * k;
                         const uint16_t *src = qg + static_cast<size_t>(row) * D + e;
                         x0 = QBF16 ? __uint_as_float(static_cast<uint32_t>(src[0]) << 16)
@@ -300,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     if (s_flag) {
         if (threadIdx.x == 0)
             atomicOr(err, DERR_INDEX);
-        for (int r = threadIdx.x; r < G; r += kThreads)
-            ws_ml[(static_cast<size_t>(s) * Hq + head0 + r) * max_splits + split] =
+        for (int r = threadIdx.x; r < R; r += kThreads)
+            ws_ml[((static_cast<size_t>(s) * Hq + head0) * T + r) * max_splits + split] =
                 make_float2(0.f, -1.f); // l < 0 marks an unusable partial
         return;
     }
@@ -417,6 +421,18 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
                     sc[i] = sc[4 + i] = -INFINITY;
             }
         }
+        if (T > 1 && t0 + u * kUnit + kUnit - 1 > len - T) {
+            // new token i sees cached token p iff p <= len - T + i (bottom-right)
+            const int lim0 = len - T + (g % T), lim1 = len - T + ((g + 8) % T);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int p = t0 + u * kUnit + (i >> 1) * 8 + 2 * t + (i & 1);
+                if (p > lim0)
+                    sc[i] = -INFINITY;
+                if (p > lim1)
+                    sc[4 + i] = -INFINITY;
+            }
+        }
         float mx[2] = {max4(sc[0], sc[1], sc[2], sc[3]), max4(sc[4], sc[5], sc[6], sc[7])};
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -528,10 +544,10 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
             const int col = n * 8 + 2 * t;
-            if (g < G)
+            if (g < R)
                 *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g) * D + col) =
                     make_float2(o[n][0], o[n][1]);
-            if (g + 8 < G)
+            if (g + 8 < R)
                 *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g + 8) * D + col) =
                     make_float2(o[n][2], o[n][3]);
         }
@@ -541,10 +557,10 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
 #pragma unroll
         for (int ch = 0; ch < D / 16; ++ch) {
             const int col = ch * 16 + 4 * t;
-            if (g < G)
+            if (g < R)
                 *reinterpret_cast<float4 *>(mrg_u + (warp * 16 + g) * D + col) =
                     make_float4(o[2 * ch][0], o[2 * ch + 1][0], o[2 * ch][1], o[2 * ch + 1][1]);
-            if (g + 8 < G)
+            if (g + 8 < R)
                 *reinterpret_cast<float4 *>(mrg_u + (warp * 16 + g + 8) * D + col) =
                     make_float4(o[2 * ch][2], o[2 * ch + 1][2], o[2 * ch][3], o[2 * ch + 1][3]);
         }
@@ -556,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
     const bool bad = s_flag != 0;
     const float vsc = KV8 ? v_scale[hk] : 1.0f;
-    for (int idx = threadIdx.x; idx < G * D; idx += kNC * 32) {
+    for (int idx = threadIdx.x; idx < R * D; idx += kNC * 32) {
         const int r = idx / D, e = idx % D;
         float M = -INFINITY;
 #pragma unroll
@@ -570,7 +586,8 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
             Lsum += sc * ml.y;
             U += sc * mrg_u[(w * 16 + r) * D + e];
         }
-        const size_t o_idx = (static_cast<size_t>(s) * Hq + head0 + r) * max_splits + split;
+        const size_t o_idx =
+            ((static_cast<size_t>(s) * Hq + head0) * T + r) * max_splits + split;
         ws_u[o_idx * D + e] = U * vsc;
         if (e == 0)
             ws_ml[o_idx] = bad ? make_float2(0.f, -1.f) : make_float2(M, Lsum);
@@ -605,8 +622,8 @@ size_t decode_workspace_bytes(int num_seqs, int Hq, int d, int max_seq_len) {
 template <int D, typename OutT>
 static cudaError_t launch_combine(const DecodeArgs &a, const float2 *ws_ml, const float *ws_u,
                                   int tps, int max_splits, cudaStream_t st) {
-    dec::decode_combine_kernel<D, OutT><<<a.num_seqs * a.Hq, D, 0, st>>>(
-        ws_ml, ws_u, a.seq_lens, static_cast<OutT *>(a.O), a.lse, a.Hq, a.block_size,
+    dec::decode_combine_kernel<D, OutT><<<a.num_seqs * a.Hq * a.T, D, 0, st>>>(
+        ws_ml, ws_u, a.seq_lens, static_cast<OutT *>(a.O), a.lse, a.Hq, a.T, a.block_size,
         a.max_blocks, a.max_seq_len, tps, max_splits);
     return cudaGetLastError();
 }
@@ -636,7 +653,7 @@ static cudaError_t launch_mma(const DecodeArgs &a, float2 *ws_ml, float *ws_u, i
     dim3 grid(max_splits, a.Hkv, a.num_seqs);
     kern<<<grid, dm::kThreads, Ly::SMEM, st>>>(
         mk, mv, a.q, a.block_table, a.seq_lens, a.k_scale, a.v_scale, ws_ml, ws_u, a.Hq,
-        a.Hq / a.Hkv, a.block_size, a.max_blocks, a.num_blocks, a.max_seq_len, tps, max_splits,
+        a.Hq / a.Hkv, a.T, a.block_size, a.max_blocks, a.num_blocks, a.max_seq_len, tps, max_splits,
         a.scale * 1.4426950408889634f, a.err);
     return cudaGetLastError();
 }
@@ -661,7 +678,7 @@ template <int D>
 static cudaError_t decode_d(const DecodeArgs &a, cudaStream_t st) {
     const int tps = choose_tps(a, dm::min_ctas<D>());
     const int max_splits = max(1, (a.max_seq_len + tps - 1) / tps);
-    const size_t n = static_cast<size_t>(a.num_seqs) * a.Hq * max_splits;
+    const size_t n = static_cast<size_t>(a.num_seqs) * a.Hq * a.T * max_splits;
     size_t ml_bytes = (n * sizeof(float2) + 255) & ~static_cast<size_t>(255);
     float2 *ws_ml = static_cast<float2 *>(a.workspace);
     float *ws_u = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + ml_bytes);

@@ -47,6 +47,7 @@ struct DecodeArgs {
     const float *v_scale;
     void *workspace;
     unsigned *err;
+    int T = 1; // new query tokens per sequence (multi-token decode)
 };
 
 struct AppendArgs {

@@ -149,6 +149,27 @@ ATTN_API attn_status attn_decode(const void *q, const void *Kcache, const void *
                         const float *v_scale, void *workspace,
                         size_t workspace_bytes, void *stream);
 
+/* Multi-token decode (speculative / draft verification: several new tokens
+ * per sequence, code-journey.com "Attention co-design" -- more query rows
+ * per KV head raise decode's GEMM-M).  The n_new new tokens of sequence s
+ * are its last n_new; their K/V must already be in the cache.  New token i
+ * sees cached token p iff p <= seq_lens[s] - n_new + i (bottom-right).
+ *   q   [num_seqs, Hq, n_new, d];  O [num_seqs, Hq, n_new, d];
+ *   lse [num_seqs, Hq, n_new] or NULL
+ * Everything else as attn_decode, with (Hq / Hkv) * n_new <= 16, every
+ * seq_lens[s] >= n_new, and a workspace of at least
+ * attn_decode_workspace_bytes(num_seqs * n_new, Hq, d, max_seq_len) bytes.
+ * n_new = 1 is attn_decode.  Two kernel launches. */
+ATTN_API attn_status attn_decode_tokens(const void *q, const void *Kcache, const void *Vcache,
+                                        const int32_t *block_table, const int32_t *seq_lens,
+                                        void *O, float *lse, int num_seqs, int n_new, int Hq,
+                                        int Hkv, int d, int block_size,
+                                        int max_blocks_per_seq, int num_blocks,
+                                        int max_seq_len, float scale, attn_dtype q_dtype,
+                                        attn_dtype kv_dtype, attn_dtype out_dtype,
+                                        const float *k_scale, const float *v_scale,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
 /* KV-cache append (papanda925.com, KV-cache management concept: the K/V of
  * each new token is added to the cache).
  *   k_new, v_new [T, Hkv, d] src_dtype (F16 / BF16)

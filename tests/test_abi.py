@@ -113,6 +113,20 @@ def test_decode_host_validation(L):
     assert _decode(L, ws=ctypes.c_void_p((1 << 20) + 16)) == attn.ERR_INVALID
 
 
+def test_decode_tokens_host_validation(L):
+    def call(**kw):
+        a = dict(S=4, T=4, Hq=8, Hkv=2, d=128, msl=128, wsb=1 << 30)
+        a.update(kw)
+        return L.attn_decode_tokens(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, a["S"], a["T"],
+                                    a["Hq"], a["Hkv"], a["d"], 16, 8, 32, a["msl"], 0.1, 1, 1, 1,
+                                    None, None, FAKE, a["wsb"], None)
+    assert call(T=0) == attn.ERR_INVALID
+    assert call(T=5) == attn.ERR_UNSUPPORTED                           # G * T = 20 > 16
+    assert call(T=4, msl=3) == attn.ERR_INVALID                        # shorter than its new tokens
+    assert call(wsb=1024) == attn.ERR_INVALID                          # workspace too small
+    assert L.attn_last_launch_count() == 0
+
+
 def test_decode_workspace_size_is_monotone(L):
     a = attn.decode_workspace_bytes(64, 32, 128, 32768)
     b = attn.decode_workspace_bytes(64, 32, 128, 1024)
