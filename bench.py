@@ -389,6 +389,9 @@ def workload_lines(name: str, steps: int, warmup: int):
         jobs.append(("prefill", W.PREFILL_WORKLOADS[name]))
     elif name in W.PAGED_PREFILL_WORKLOADS:
         jobs.append(("paged-prefill", W.PAGED_PREFILL_WORKLOADS[name]))
+    elif name in W.DECODE_TOKENS_WORKLOADS:
+        base = W.DECODE_WORKLOADS["paged-decode"]
+        jobs.append(("decode-tokens", (W.DECODE_TOKENS_WORKLOADS[name][0], base, name)))
     elif name in W.DECODE_WORKLOADS:
         jobs.append(("decode", W.DECODE_WORKLOADS[name]))
     elif name == "sweep":
@@ -400,7 +403,7 @@ def workload_lines(name: str, steps: int, warmup: int):
     else:
         raise SystemExit(f"unknown workload {name}")
     for kind, spec in jobs:
-        line = {"workload": spec.name, "kind": kind}
+        line = {"workload": getattr(spec, "name", ""), "kind": kind}
         try:
             if kind == "prefill":
                 t = W.make_prefill(spec, seed=0, device=dev)
@@ -424,6 +427,32 @@ def workload_lines(name: str, steps: int, warmup: int):
                             peak_tflops=peak,
                             peak_kind="measured burst bf16" + (
                                 " x 2 (nominal fp8/bf16 ratio)" if spec.dtype == "e4m3" else ""))
+            elif kind == "decode-tokens":
+                T, base, wname = spec
+                line["workload"] = wname
+                dd = W.make_decode(base, seed=0, device=dev)
+                lens = dd["seq_lens"].cpu()
+                g = torch.Generator(device=dev).manual_seed(5)
+                q = torch.randn((base.num_seqs, base.Hq, T, base.d), generator=g, device=dev,
+                                dtype=torch.float32).to(W.DTYPES[base.q_dtype])
+                Od = torch.empty(q.shape, dtype=W.DTYPES[base.out_dtype], device=dev)
+                lsed = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+                ws = torch.empty(attn.decode_workspace_bytes(base.num_seqs * T, base.Hq, base.d,
+                                                             base.len_hi),
+                                 dtype=torch.uint8, device=dev)
+
+                def fn():
+                    attn.decode_tokens(q, dd["Kc"], dd["Vc"], dd["block_table"],
+                                       dd["seq_lens"], max_seq_len=base.len_hi, O=Od, lse=lsed,
+                                       workspace=ws, stream=stream)
+                med, best = _time_kernel(fn, stream, warmup, steps, flush)
+                Bd = decode_bytes(base, lens) + (T - 1) * 2 * base.num_seqs * base.Hq * base.d * 2
+                roof = max(T * decode_flops(base, lens) / (pk["bf16_tflops"] * 1e12),
+                           Bd / (pk["hbm_gbs"] * 1e9))
+                line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            gbs=round(Bd / med / 1e9, 1), bytes=Bd, new_tokens=T,
+                            pct_roofline=round(100 * roof / med, 2),
+                            peak_gbs=pk["hbm_gbs"], peak_kind="measured HBM copy")
             elif kind == "paged-prefill":
                 t = W.make_paged_prefill(spec, seed=0, device=dev)
                 lens = t["seq_lens"].cpu()

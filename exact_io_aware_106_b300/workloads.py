@@ -91,6 +91,12 @@ PAGED_PREFILL_WORKLOADS = {
                                       "paged-prefill"),
 }
 
+# multi-token decode: the paged-decode workload with 4 new tokens per
+# sequence (e.g. speculative drafts), G * 4 = 16 query rows per KV head
+DECODE_TOKENS_WORKLOADS = {
+    "spec-decode-4": (4, None),
+}
+
 DECODE_WORKLOADS = {
     "paged-decode": DecodeSpec(64, 32, 8, 128, 1024, 32768, 16, "bf16", "bf16", "bf16",
                                "paged-decode"),
