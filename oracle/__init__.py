@@ -65,6 +65,9 @@ def lib():
                                           i32, i32, i32, i32, i32, i32, i32, f64, vp, i32,
                                           i32, vp]
         L.oracle_decode_paged.restype = i32
+        L.oracle_backward.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32,
+                                      i32, i32, i32, i32, i32, f64, i32]
+        L.oracle_backward.restype = i32
         L.oracle_prefill_paged.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, vp, i32, i32,
                                            i32, i32, i32, i32, i32, i32, i32, f64, i32, i32,
                                            i32]
@@ -192,6 +195,34 @@ def decode_paged(q, Kc, Vc, block_table, seq_lens, scale: float | None = None,
     if return_counts:
         return O, lse, (int(counts[0]), int(counts[1]))
     return O, lse
+
+
+def backward(Q, K, V, dO, causal: bool, scale: float | None = None, nthreads: int = 0,
+             magnitudes: bool = False):
+    """Gradients of exact attention for upstream gradient dO [B,Hq,nq,d]:
+    returns (dQ [B,Hq,nq,d], dK, dV [B,Hkv,nkv,d]) in fp64, plus (with
+    magnitudes=True) the per-element sums of |terms| (mag_q, mag_k, mag_v)."""
+    code = dtype_code(Q)
+    assert dtype_code(K) == code and dtype_code(V) == code and dtype_code(dO) == code
+    q, k, v, go = _as_np(Q), _as_np(K), _as_np(V), _as_np(dO)
+    B, Hq, nq, d = q.shape
+    _, Hkv, nkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dQ = np.zeros(q.shape, np.float64)
+    dK = np.zeros(k.shape, np.float64)
+    dV = np.zeros(k.shape, np.float64)
+    mq = np.zeros(q.shape, np.float64) if magnitudes else None
+    mk = np.zeros(k.shape, np.float64) if magnitudes else None
+    mv = np.zeros(k.shape, np.float64) if magnitudes else None
+    rc = lib().oracle_backward(_p(q), _p(k), _p(v), _p(go), code, _p(dQ), _p(dK), _p(dV),
+                               _p(mq), _p(mk), _p(mv), B, Hq, Hkv, nq, nkv, d, int(causal),
+                               float(scale), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_backward: invalid arguments")
+    if magnitudes:
+        return dQ, dK, dV, (mq, mk, mv)
+    return dQ, dK, dV
 
 
 def prefill_paged(Q, Kc, Vc, block_table, seq_lens, causal: bool, scale: float | None = None,

@@ -424,6 +424,130 @@ int oracle_decode_paged(const void *q, int q_dtype, const void *Kc,
 
 /* ------------------------------------------------------------ kv append */
 
+/* Backward pass of exact attention (marketmaker.cc, "Rückwärtsdurchlauf":
+ * the probabilities are recomputed from Q, K and the stored row statistics
+ * instead of being kept).  With S = scale Q K^T (causal: future keys
+ * masked), P = softmax(S) row-wise and O = P V, the gradients of a loss
+ * with dL/dO = dO are
+ *   dV = P^T dO,
+ *   dP = dO V^T,  D_i = sum_j P_ij dP_ij,  dS = P * (dP - D),
+ *   dQ = scale dS K,  dK = scale dS^T Q,
+ * with dK and dV of a KV head summed over the G query heads that read it.
+ * Everything is materialised in fp64 per (b, h).  mag_* (optional) receive,
+ * per gradient element, the sum of the absolute values of the terms it is a
+ * sum of (|P_ij dO_ic| for dV, scale |dS_ij K_jc| for dQ, scale |dS_ij Q_ic|
+ * for dK) -- the scale against which rounding errors are judged. */
+int oracle_backward(const void *Q, const void *K, const void *V, const void *dO, int in_dtype,
+                    double *dQ, double *dK, double *dV, double *mag_q, double *mag_k,
+                    double *mag_v, int B, int Hq, int Hkv, int nq, int nkv, int d, int causal,
+                    double scale, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || nq <= 0 || nkv <= 0 || d <= 0 || Hq % Hkv != 0)
+        return -1;
+    if (causal && nq > nkv)
+        return -1;
+    const int G = Hq / Hkv;
+    const size_t kv_elems = (size_t)B * Hkv * nkv * d;
+    memset(dK, 0, kv_elems * sizeof(double));
+    memset(dV, 0, kv_elems * sizeof(double));
+    if (mag_k)
+        memset(mag_k, 0, kv_elems * sizeof(double));
+    if (mag_v)
+        memset(mag_v, 0, kv_elems * sizeof(double));
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int bk = 0; bk < B * Hkv; ++bk) { /* one KV head: its G query heads in turn */
+        const int b = bk / Hkv, hk = bk % Hkv;
+        double *k = decode_rows(K, in_dtype, (size_t)bk * nkv * d, (size_t)nkv * d);
+        double *v = decode_rows(V, in_dtype, (size_t)bk * nkv * d, (size_t)nkv * d);
+        double *P = (double *)malloc((size_t)nq * nkv * sizeof(double));
+        double *dS = (double *)malloc((size_t)nq * nkv * sizeof(double));
+        double *dk = dK + (size_t)bk * nkv * d, *dv = dV + (size_t)bk * nkv * d;
+        double *mk = mag_k ? mag_k + (size_t)bk * nkv * d : NULL;
+        double *mv = mag_v ? mag_v + (size_t)bk * nkv * d : NULL;
+        for (int g = 0; g < G; ++g) {
+            const int h = hk * G + g;
+            const size_t qoff = ((size_t)b * Hq + h) * nq * d;
+            double *q = decode_rows(Q, in_dtype, qoff, (size_t)nq * d);
+            double *go = decode_rows(dO, in_dtype, qoff, (size_t)nq * d);
+            /* P = softmax(scale Q K^T), masked */
+            for (int i = 0; i < nq; ++i) {
+                double *row = P + (size_t)i * nkv;
+                double m = -INFINITY;
+                for (int j = 0; j < nkv; ++j) {
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c)
+                        acc += q[(size_t)i * d + c] * k[(size_t)j * d + c];
+                    row[j] = (causal && j > i + (nkv - nq)) ? -INFINITY : acc * scale;
+                    if (row[j] > m)
+                        m = row[j];
+                }
+                double l = 0.0;
+                for (int j = 0; j < nkv; ++j) {
+                    row[j] = exp(row[j] - m);
+                    l += row[j];
+                }
+                for (int j = 0; j < nkv; ++j)
+                    row[j] /= l;
+            }
+            /* dP = dO V^T, D = rowsum(P * dP), dS = P * (dP - D) */
+            for (int i = 0; i < nq; ++i) {
+                double Di = 0.0;
+                for (int j = 0; j < nkv; ++j) {
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c)
+                        acc += go[(size_t)i * d + c] * v[(size_t)j * d + c];
+                    dS[(size_t)i * nkv + j] = acc; /* dP for now */
+                    Di += P[(size_t)i * nkv + j] * acc;
+                }
+                for (int j = 0; j < nkv; ++j)
+                    dS[(size_t)i * nkv + j] = P[(size_t)i * nkv + j] * (dS[(size_t)i * nkv + j] - Di);
+            }
+            /* dV += P^T dO, dK += scale dS^T Q */
+            for (int j = 0; j < nkv; ++j)
+                for (int c = 0; c < d; ++c) {
+                    double av = 0.0, ak = 0.0, mav = 0.0, mak = 0.0;
+                    for (int i = 0; i < nq; ++i) {
+                        const double tv = P[(size_t)i * nkv + j] * go[(size_t)i * d + c];
+                        const double tk = dS[(size_t)i * nkv + j] * q[(size_t)i * d + c];
+                        av += tv;
+                        ak += tk;
+                        mav += fabs(tv);
+                        mak += fabs(tk);
+                    }
+                    dv[(size_t)j * d + c] += av;
+                    dk[(size_t)j * d + c] += scale * ak;
+                    if (mv)
+                        mv[(size_t)j * d + c] += mav;
+                    if (mk)
+                        mk[(size_t)j * d + c] += scale * mak;
+                }
+            /* dQ = scale dS K */
+            for (int i = 0; i < nq; ++i)
+                for (int c = 0; c < d; ++c) {
+                    double aq = 0.0, maq = 0.0;
+                    for (int j = 0; j < nkv; ++j) {
+                        const double tq = dS[(size_t)i * nkv + j] * k[(size_t)j * d + c];
+                        aq += tq;
+                        maq += fabs(tq);
+                    }
+                    dQ[qoff + (size_t)i * d + c] = scale * aq;
+                    if (mag_q)
+                        mag_q[qoff + (size_t)i * d + c] = scale * maq;
+                }
+            free(q);
+            free(go);
+        }
+        free(k);
+        free(v);
+        free(P);
+        free(dS);
+    }
+    return 0;
+}
+
 /* Prefill over a block-paged cache (prefix caching / chunked prefill):
  * for every sequence b and query head h, the n_q query rows Q[b,h] attend
  * to the len = seq_lens[b] cached keys of KV head h / G, gathered in token
