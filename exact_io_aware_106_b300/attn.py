@@ -20,7 +20,8 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 _DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.float8_e4m3fn: 3}
 
 EXPORTS = ("attn_prefill", "attn_prefill_paged", "attn_decode_workspace_bytes", "attn_decode",
-           "attn_decode_tokens", "attn_kv_append",
+           "attn_decode_tokens", "attn_kv_append", "attn_backward",
+           "attn_backward_workspace_bytes",
            "attn_last_error", "attn_status_str", "attn_last_launch_count",
            "attn_decode_static_ws")
 
@@ -63,6 +64,11 @@ def lib():
         L.attn_kv_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                      i32, i32, i32, vp, vp, vp]
         L.attn_kv_append.restype = i32
+        L.attn_backward_workspace_bytes.argtypes = [i32, i32, i32]
+        L.attn_backward_workspace_bytes.restype = sz
+        L.attn_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                    i32, i32, f32, i32, i32, i32, vp, sz, vp]
+        L.attn_backward.restype = i32
         L.attn_last_error.argtypes = [vp]
         L.attn_last_error.restype = i32
         L.attn_status_str.argtypes = [i32]
@@ -164,6 +170,32 @@ def prefill_paged(Q, Kc, Vc, block_table, seq_lens, max_seq_len: int, causal: bo
                                   _stream(stream))
     _check("attn_prefill_paged", st)
     return O, lse
+
+
+def backward(Q, K, V, O, dO, lse, causal: bool, scale: float | None = None, out_dtype=None,
+             dQ=None, dK=None, dV=None, workspace=None, stream=None):
+    """Gradients (dQ, dK, dV) of O = softmax(scale Q K^T [causal]) V for the
+    upstream gradient dO, given the forward's O (16-bit or fp32) and lse."""
+    _cuda(Q, K, V, O, dO, lse)
+    B, Hq, nq, d = Q.shape
+    _, Hkv, nkv, _ = K.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out_dtype is None:
+        out_dtype = Q.dtype
+    dQ = torch.empty(Q.shape, dtype=out_dtype, device=Q.device) if dQ is None else dQ
+    dK = torch.empty(K.shape, dtype=out_dtype, device=Q.device) if dK is None else dK
+    dV = torch.empty(V.shape, dtype=out_dtype, device=Q.device) if dV is None else dV
+    need = int(lib().attn_backward_workspace_bytes(B, Hq, nq))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    _cuda(dQ, dK, dV, workspace)
+    st = lib().attn_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse), _ptr(dQ),
+                             _ptr(dK), _ptr(dV), B, Hq, Hkv, nq, nkv, d, int(bool(causal)),
+                             float(scale), _DT[Q.dtype], _DT[O.dtype], _DT[dQ.dtype],
+                             _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("attn_backward", st)
+    return dQ, dK, dV
 
 
 def decode_workspace_bytes(num_seqs: int, Hq: int, d: int, max_seq_len: int) -> int:

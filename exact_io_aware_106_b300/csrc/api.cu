@@ -277,6 +277,50 @@ attn_status attn_kv_append(const void *k_new, const void *v_new, void *Kcache, v
     return ATTN_OK;
 }
 
+size_t attn_backward_workspace_bytes(int B, int Hq, int n_q) {
+    if (B <= 0 || Hq <= 0 || n_q <= 0)
+        return 0;
+    return attn::backward_workspace_bytes(B, Hq, n_q);
+}
+
+attn_status attn_backward(const void *Q, const void *K, const void *V, const void *O,
+                          const void *dO, const float *lse, void *dQ, void *dK, void *dV, int B,
+                          int Hq, int Hkv, int n_q, int n_kv, int d, int causal, float scale,
+                          attn_dtype in_dtype, attn_dtype o_dtype, attn_dtype out_dtype,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    t_last_launches = 0;
+    if (!Q || !K || !V || !O || !dO || !lse || !dQ || !dK || !dV || !workspace)
+        return ATTN_ERR_INVALID;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || n_q <= 0 || n_kv <= 0 || d <= 0 || Hq % Hkv != 0)
+        return ATTN_ERR_INVALID;
+    if (causal && n_q > n_kv)
+        return ATTN_ERR_INVALID;
+    if (!isfinite(scale))
+        return ATTN_ERR_INVALID;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+        !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) ||
+        !aligned(lse, 4) || !aligned(workspace, 256))
+        return ATTN_ERR_INVALID;
+    if (!is16(in_dtype) || !is_out(out_dtype) || (d != 64 && d != 128) ||
+        !(o_dtype == in_dtype || o_dtype == ATTN_F32))
+        return ATTN_ERR_UNSUPPORTED;
+    const long long nqb = (n_q + 127) / 128, nkb = (n_kv + 127) / 128;
+    if (nqb * B * Hq > 0x7fffffffLL || nkb * B * Hkv > 0x7fffffffLL)
+        return ATTN_ERR_UNSUPPORTED;
+    if (workspace_bytes < attn::backward_workspace_bytes(B, Hq, n_q))
+        return ATTN_ERR_INVALID;
+    unsigned *err = err_word();
+    if (!err)
+        return ATTN_ERR_CUDA;
+    attn::BackwardArgs a{Q, K, V, O, dO, lse, dQ, dK, dV, B, Hq, Hkv, n_q, n_kv, d,
+                         causal ? 1 : 0, scale, in_dtype == ATTN_BF16, o_dtype == ATTN_F32,
+                         out_code(out_dtype), workspace, err};
+    if (attn::backward_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = 3;
+    return ATTN_OK;
+}
+
 attn_status attn_last_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)

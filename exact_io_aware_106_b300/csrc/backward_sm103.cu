@@ -1,0 +1,673 @@
+// backward_sm103.cu -- gradients of exact attention on sm_103a tensor cores.
+//
+// The method (marketmaker.cc "Flash Attention and sequence length",
+// "Rückwärtsdurchlauf"): nothing n x n is kept from the forward pass; the
+// probabilities are recomputed block by block from Q, K and the stored row
+// statistic lse = ln sum_j exp(s_ij):  P = exp(s - lse).  With dO the
+// upstream gradient,
+//   dV = P^T dO,   dP = dO V^T,   D_i = sum_c dO_ic O_ic  (= sum_j P_ij dP_ij),
+//   dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q,
+// and dK, dV of a KV head summed over the G query heads that read it
+// (code-journey.com "Attention co-design", Group Size).
+//
+// Three kernels, no atomics (every gradient element has one writer):
+//   bwd_prep_kernel   D = rowsum(dO * O), one warp per row.
+//   bwd_kv_kernel     one CTA per (b, KV head, 128-key block): K and V stay
+//                     in shared memory; for every query head of the group
+//                     and every query block that sees the keys,
+//                       S^T = K Q^T, dP^T = V dO^T        (tcgen05, TMEM)
+//                       P^T, dS^T                          (4 warps, one key row each)
+//                       dV += P^T dO, dK += dS^T Q         (tcgen05, A = TMEM)
+//   bwd_q_kernel      one CTA per (b, head, 128-row query block): for every
+//                     key block it sees, S = Q K^T, dP = dO V^T, dS, and
+//                     dQ += dS K.
+// P and dS enter the second products in the inputs' 16-bit format; the
+// accumulators are fp32 in tensor memory.  Scores are in the log2 domain:
+// p = 2^(s c - lse log2 e), c = scale log2 e.
+#include "common.cuh"
+#include "launch.h"
+
+namespace attn {
+
+namespace bw {
+
+constexpr int BT = 128; // rows of a key block and of a query block
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+    static constexpr int TILE = BT * D * 2;          // one 128-row 16-bit tile
+    static constexpr int PANELS = D / 64;
+    static constexpr int NS = 2;                     // stages of the streamed pair of tiles
+    static constexpr int OFF_A = 0;                  // resident tile pair (K,V or Q,dO)
+    static constexpr int OFF_S = OFF_A + 2 * TILE;   // NS stages of the streamed pair
+    static constexpr int OFF_ROW = OFF_S + NS * 2 * TILE; // per-step lse2 / D of 128 rows
+    static constexpr int OFF_BAR = OFF_ROW + 2 * BT * 4;
+    static constexpr int NBAR = 1 + 2 * NS + 2 + 2;  // afull, sfull/sempty[NS], mma_s, p_ready, done, drain
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 64 + 1024;
+    static constexpr int S_COL = 0, DP_COL = BT, ACC0 = 2 * BT, ACC1 = 2 * BT + D;
+    static_assert(2 * BT + 2 * D <= 512, "tensor memory budget");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+struct Shape {
+    int B, Hq, Hkv, G, n_q, n_kv, causal, nqb, nkb;
+    float c, scale;
+};
+
+// D_i = sum_c dO_ic O_ic (fp32), one warp per row; O in the inputs' 16-bit
+// format or in fp32 (OF32).
+template <int D, bool BF16, bool OF32>
+__global__ void __launch_bounds__(256)
+    bwd_prep_kernel(const void *__restrict__ O_, const uint16_t *__restrict__ dO,
+                    float *__restrict__ Drow, long long rows) {
+    const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows)
+        return;
+    constexpr int EPL = D / 32; // 2 or 4 elements per lane
+    const uint16_t *g = dO + r * D + lane * EPL;
+    float gv[EPL], ov[EPL];
+    if constexpr (EPL == 2) {
+        const uint32_t b = *reinterpret_cast<const uint32_t *>(g);
+        gv[0] = lo16<BF16>(b), gv[1] = hi16<BF16>(b);
+    } else {
+        const uint2 b = *reinterpret_cast<const uint2 *>(g);
+        gv[0] = lo16<BF16>(b.x), gv[1] = hi16<BF16>(b.x), gv[2] = lo16<BF16>(b.y),
+        gv[3] = hi16<BF16>(b.y);
+    }
+    if constexpr (OF32) {
+        const float *o = static_cast<const float *>(O_) + r * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+            ov[e] = o[e];
+    } else {
+        const uint16_t *o = static_cast<const uint16_t *>(O_) + r * D + lane * EPL;
+        if constexpr (EPL == 2) {
+            const uint32_t a = *reinterpret_cast<const uint32_t *>(o);
+            ov[0] = lo16<BF16>(a), ov[1] = hi16<BF16>(a);
+        } else {
+            const uint2 a = *reinterpret_cast<const uint2 *>(o);
+            ov[0] = lo16<BF16>(a.x), ov[1] = hi16<BF16>(a.x), ov[2] = lo16<BF16>(a.y),
+            ov[3] = hi16<BF16>(a.y);
+        }
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+        acc = fmaf(gv[e], ov[e], acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0)
+        Drow[r] = acc;
+}
+
+// Loads one 128-row tile of a [d, n, bh] tensor map (all d/64 panels).
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                          int row, int bh) {
+#pragma unroll
+    for (int p = 0; p < D / 64; ++p)
+        tma_load_3d(dst + p * BT * 128, map, bar, p * 64, row, bh);
+}
+
+// Issues acc += A(tmem, 128 x 128 in 16-bit, K = 128) * B(smem tile,
+// MN-major: K = tile rows, N = D).
+template <int D>
+__device__ __forceinline__ void mma_tmem_a(uint32_t acc, uint32_t a_tmem, uint32_t b_tile,
+                                           uint32_t idesc, bool first) {
+#pragma unroll
+    for (int k = 0; k < BT / 16; ++k) {
+        const uint64_t bd = sdesc_sw128(b_tile + k * 16 * 128, BT * 128, 1024);
+        mma_ts(acc, a_tmem + k * 8, bd, idesc, (first && k == 0) ? 0u : 1u);
+    }
+}
+
+// Issues acc = A(smem tile, K-major, 128 rows) * B(smem tile, K-major,
+// 128 rows)^T over K = D.
+template <int D>
+__device__ __forceinline__ void mma_ss_tiles(uint32_t acc, uint32_t a_tile, uint32_t b_tile,
+                                             uint32_t idesc) {
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k / 4) * (BT * 128) + (k % 4) * 32;
+        mma_ss(acc, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024),
+               idesc, k > 0 ? 1u : 0u);
+    }
+}
+
+// Writes 32 accumulator columns of this thread's row to global memory.
+template <int OUT>
+__device__ __forceinline__ void store32(void *dst_base, size_t elem_off, const float (&o)[32]) {
+    if constexpr (OUT == 2) {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(dst_base) + elem_off);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dst_base) + elem_off);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pack2<OUT == 1>(o[8 * i], o[8 * i + 1]),
+                                pack2<OUT == 1>(o[8 * i + 2], o[8 * i + 3]),
+                                pack2<OUT == 1>(o[8 * i + 4], o[8 * i + 5]),
+                                pack2<OUT == 1>(o[8 * i + 6], o[8 * i + 7]));
+    }
+}
+
+// First query block that sees key block kb (bottom-right causal), else 0.
+__device__ __forceinline__ int first_qblock(const Shape &sh, int kb) {
+    if (!sh.causal)
+        return 0;
+    const int off = sh.n_kv - sh.n_q;
+    const int need = kb * BT - off; // smallest query row that sees key kb*BT
+    return need <= 0 ? 0 : need / BT;
+}
+
+// Number of key blocks query block qb sees.
+__device__ __forceinline__ int key_blocks(const Shape &sh, int qb) {
+    if (!sh.causal)
+        return sh.nkb;
+    const int r_last = min(qb * BT + BT - 1, sh.n_q - 1);
+    return min(sh.nkb, (r_last + sh.n_kv - sh.n_q) / BT + 1);
+}
+
+// ========================================================================
+// dK, dV: one CTA per (b, KV head, key block)
+template <int D, bool BF16, int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_do, const float *__restrict__ lse,
+                  const float *__restrict__ Drow, void *__restrict__ dK, void *__restrict__ dV,
+                  const Shape sh, unsigned *err) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+    const uint32_t sK = base_s + C::OFF_A, sV = sK + C::TILE;
+    auto sQ = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE; };
+    auto sDO = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE + C::TILE; };
+    float *s_lse2 = reinterpret_cast<float *>(base + C::OFF_ROW);
+    float *s_D = s_lse2 + BT;
+    const uint32_t bar0 = base_s + C::OFF_BAR;
+    const uint32_t b_afull = bar0;
+    auto b_sfull = [&](int i) { return bar0 + 8u * (1 + i); };
+    auto b_sempty = [&](int i) { return bar0 + 8u * (1 + C::NS + i); };
+    const uint32_t b_mma = bar0 + 8u * (1 + 2 * C::NS);    // S^T, dP^T of a step are in TMEM
+    const uint32_t b_pready = b_mma + 8u;                 // P^T, dS^T of a step are in TMEM
+    const uint32_t b_done = b_pready + 8u;
+    const uint32_t b_drain = b_done + 8u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // heaviest key blocks first (causal: early keys are seen by more queries)
+    const int per_bkv = sh.nkb;
+    const int kb = static_cast<int>(blockIdx.x) / (sh.B * sh.Hkv);
+    const int bkv = static_cast<int>(blockIdx.x) % (sh.B * sh.Hkv);
+    (void)per_bkv;
+    const int b = bkv / sh.Hkv, hk = bkv % sh.Hkv;
+    const int qb0 = first_qblock(sh, kb);
+    const int nq_steps = sh.nqb - qb0;     // query blocks per query head
+    const int nsteps = sh.G * nq_steps;    // (head, query block) steps
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(b_afull, 1);
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(b_sfull(i), 1);
+            mbar_init(b_sempty(i), 1);
+        }
+        mbar_init(b_mma, 1);
+        mbar_init(b_pready, 4);
+        mbar_init(b_done, 1);
+        mbar_init(b_drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(b_afull, 2 * C::TILE);
+            load_tile<D>(sK, &tm_k, b_afull, kb * BT, bkv);
+            load_tile<D>(sV, &tm_v, b_afull, kb * BT, bkv);
+            int issued = 0;
+            for (int t = 0; t < nsteps; ++t) {
+                const int st = t % C::NS;
+                if (t >= C::NS &&
+                    !mbar_wait(b_sempty(st), ((t / C::NS) - 1) & 1, abort_flag, err))
+                    break;
+                const int h = hk * sh.G + t / nq_steps;
+                const int qb = qb0 + t % nq_steps;
+                const int bh = b * sh.Hq + h;
+                mbar_arrive_expect_tx(b_sfull(st), 2 * C::TILE);
+                load_tile<D>(sQ(st), &tm_q, b_sfull(st), qb * BT, bh);
+                load_tile<D>(sDO(st), &tm_do, b_sfull(st), qb * BT, bh);
+                issued = t + 1;
+            }
+            if (*abort_flag) {
+                mbar_wait_drain(b_afull, 0);
+                for (int u = max(0, issued - C::NS); u < issued; ++u)
+                    mbar_wait_drain(b_sfull(u % C::NS), (u / C::NS) & 1);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f16(BT, BT, BF16, false, false);
+            constexpr uint32_t idesc_acc = idesc_f16(BT, D, BF16, false, true);
+            bool ok = mbar_wait(b_afull, 0, abort_flag, err);
+            for (int t = 0; ok && t <= nsteps; ++t) {
+                if (t > 0) {
+                    // second products of step t-1: P^T, dS^T are in TMEM
+                    const int sp = (t - 1) % C::NS;
+                    if (!mbar_wait(b_pready, (t - 1) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_tmem_a<D>(tmem + C::ACC0, tmem + C::S_COL, sDO(sp), idesc_acc, t == 1);
+                    mma_tmem_a<D>(tmem + C::ACC1, tmem + C::DP_COL, sQ(sp), idesc_acc, t == 1);
+                    tc_commit(b_sempty(sp));
+                }
+                if (t < nsteps) {
+                    const int st = t % C::NS;
+                    if (!mbar_wait(b_sfull(st), (t / C::NS) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_ss_tiles<D>(tmem + C::S_COL, sK, sQ(st), idesc_s);  // S^T = K Q^T
+                    mma_ss_tiles<D>(tmem + C::DP_COL, sV, sDO(st), idesc_s); // dP^T = V dO^T
+                    tc_commit(b_mma);
+                }
+            }
+            if (ok)
+                tc_commit(b_done);
+            tc_commit(b_drain);
+            mbar_wait_drain(b_drain, 0);
+        }
+    } else {
+        // ---- warps 0-3: one key row each
+        const int j = warp * 32 + lane; // key within the block
+        const int key = kb * BT + j;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::S_COL;
+        const uint32_t tP = tmem + lane_off + C::DP_COL;
+        const int off = sh.n_kv - sh.n_q;
+        const bool key_ok = key < sh.n_kv;
+        bool ok = true;
+        for (int t = 0; t < nsteps; ++t) {
+            const int h = hk * sh.G + t / nq_steps;
+            const int qb = qb0 + t % nq_steps;
+            const int bh = b * sh.Hq + h;
+            // this step's per-query lse (log2 domain) and D, one row per thread
+            {
+                const int q = qb * BT + j;
+                const bool q_ok = q < sh.n_q;
+                asm volatile("bar.sync 1, 128;" ::: "memory"); // previous step's reads done
+                s_lse2[j] = q_ok ? lse[static_cast<size_t>(bh) * sh.n_q + q] * kLog2e : INFINITY;
+                s_D[j] = q_ok ? Drow[static_cast<size_t>(bh) * sh.n_q + q] : 0.f;
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+            // after a failed wait the warp keeps looping (and meeting the
+            // named barriers above) without touching tensor memory, so that
+            // its sibling warps never wait on it there
+            if (!ok || !mbar_wait_warp(b_mma, t & 1, abort_flag, err)) {
+                ok = false;
+                continue;
+            }
+            tc_fence_after();
+            // query i of this block sees this key iff key <= qb*BT + i + off
+            const int i_min = key - off - qb * BT; // first visible query (causal)
+#pragma unroll 1
+            for (int ch = 0; ch < BT / 32; ++ch) {
+                uint32_t us[32], ud[32];
+                tmem_ld32(tS + ch * 32, us);
+                tmem_ld32(tP + ch * 32, ud);
+                uint32_t pw[16], dw[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int i = ch * 32 + 2 * e + h2;
+                        const bool vis = key_ok && (!sh.causal || i >= i_min);
+                        const float p =
+                            vis ? ex2(fmaf(__uint_as_float(us[2 * e + h2]), sh.c, -s_lse2[i]))
+                                : 0.f;
+                        pv[h2] = p;
+                        dv[h2] = p * (__uint_as_float(ud[2 * e + h2]) - s_D[i]);
+                    }
+                    pw[e] = pack2<BF16>(pv[0], pv[1]);
+                    dw[e] = pack2<BF16>(dv[0], dv[1]);
+                }
+                tmem_st16(tS + ch * 16, pw);
+                tmem_st16(tP + ch * 16, dw);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b_pready);
+        }
+        if (ok && nsteps > 0)
+            ok = mbar_wait_warp(b_done, 0, abort_flag, err);
+        tc_fence_after();
+        // the tensor-memory loads are warp-wide (.sync.aligned): every lane
+        // executes them; only the stores depend on the row being real
+        const size_t orow = (static_cast<size_t>(bkv) * sh.n_kv + key) * D;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t uv[32], uk[32];
+            tmem_ld32(tmem + lane_off + C::ACC0 + ch * 32, uv);
+            tmem_ld32(tmem + lane_off + C::ACC1 + ch * 32, uk);
+            if (key_ok) {
+                float ov[32], ok_[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    ov[i] = (ok && nsteps > 0) ? __uint_as_float(uv[i]) : 0.f;
+                    ok_[i] = (ok && nsteps > 0) ? __uint_as_float(uk[i]) * sh.scale : 0.f;
+                }
+                store32<OUT>(dV, orow + ch * 32, ov);
+                store32<OUT>(dK, orow + ch * 32, ok_);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ========================================================================
+// dQ: one CTA per (b, query head, query block)
+template <int D, bool BF16, int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_do, const float *__restrict__ lse,
+                 const float *__restrict__ Drow, void *__restrict__ dQ, const Shape sh,
+                 unsigned *err) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+    const uint32_t sQ = base_s + C::OFF_A, sDO = sQ + C::TILE;
+    auto sK = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE; };
+    auto sV = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE + C::TILE; };
+    const uint32_t bar0 = base_s + C::OFF_BAR;
+    const uint32_t b_afull = bar0;
+    auto b_sfull = [&](int i) { return bar0 + 8u * (1 + i); };
+    auto b_sempty = [&](int i) { return bar0 + 8u * (1 + C::NS + i); };
+    const uint32_t b_mma = bar0 + 8u * (1 + 2 * C::NS);
+    const uint32_t b_pready = b_mma + 8u;
+    const uint32_t b_done = b_pready + 8u;
+    const uint32_t b_drain = b_done + 8u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = sh.B * sh.Hq;
+    const int qb = sh.nqb - 1 - static_cast<int>(blockIdx.x) / BH; // heaviest first
+    const int bh = static_cast<int>(blockIdx.x) % BH;
+    const int b = bh / sh.Hq, h = bh % sh.Hq;
+    const int bkv = b * sh.Hkv + h / sh.G;
+    const int nsteps = key_blocks(sh, qb);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(b_afull, 1);
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(b_sfull(i), 1);
+            mbar_init(b_sempty(i), 1);
+        }
+        mbar_init(b_mma, 1);
+        mbar_init(b_pready, 4);
+        mbar_init(b_done, 1);
+        mbar_init(b_drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(b_afull, 2 * C::TILE);
+            load_tile<D>(sQ, &tm_q, b_afull, qb * BT, bh);
+            load_tile<D>(sDO, &tm_do, b_afull, qb * BT, bh);
+            int issued = 0;
+            for (int t = 0; t < nsteps; ++t) {
+                const int st = t % C::NS;
+                if (t >= C::NS &&
+                    !mbar_wait(b_sempty(st), ((t / C::NS) - 1) & 1, abort_flag, err))
+                    break;
+                mbar_arrive_expect_tx(b_sfull(st), 2 * C::TILE);
+                load_tile<D>(sK(st), &tm_k, b_sfull(st), t * BT, bkv);
+                load_tile<D>(sV(st), &tm_v, b_sfull(st), t * BT, bkv);
+                issued = t + 1;
+            }
+            if (*abort_flag) {
+                mbar_wait_drain(b_afull, 0);
+                for (int u = max(0, issued - C::NS); u < issued; ++u)
+                    mbar_wait_drain(b_sfull(u % C::NS), (u / C::NS) & 1);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f16(BT, BT, BF16, false, false);
+            constexpr uint32_t idesc_acc = idesc_f16(BT, D, BF16, false, true);
+            bool ok = mbar_wait(b_afull, 0, abort_flag, err);
+            for (int t = 0; ok && t <= nsteps; ++t) {
+                if (t > 0) {
+                    const int sp = (t - 1) % C::NS;
+                    if (!mbar_wait(b_pready, (t - 1) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_tmem_a<D>(tmem + C::ACC0, tmem + C::DP_COL, sK(sp), idesc_acc, t == 1);
+                    tc_commit(b_sempty(sp));
+                }
+                if (t < nsteps) {
+                    const int st = t % C::NS;
+                    if (!mbar_wait(b_sfull(st), (t / C::NS) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_ss_tiles<D>(tmem + C::S_COL, sQ, sK(st), idesc_s);   // S = Q K^T
+                    mma_ss_tiles<D>(tmem + C::DP_COL, sDO, sV(st), idesc_s); // dP = dO V^T
+                    tc_commit(b_mma);
+                }
+            }
+            if (ok)
+                tc_commit(b_done);
+            tc_commit(b_drain);
+            mbar_wait_drain(b_drain, 0);
+        }
+    } else {
+        // ---- warps 0-3: one query row each
+        const int i = warp * 32 + lane;
+        const int row = qb * BT + i;
+        const bool row_ok = row < sh.n_q;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::S_COL;
+        const uint32_t tP = tmem + lane_off + C::DP_COL;
+        const float lse2 =
+            row_ok ? lse[static_cast<size_t>(bh) * sh.n_q + row] * kLog2e : INFINITY;
+        const float Dr = row_ok ? Drow[static_cast<size_t>(bh) * sh.n_q + row] : 0.f;
+        const int lim = sh.causal ? row + (sh.n_kv - sh.n_q) : sh.n_kv - 1; // last visible key
+        const int klim = min(lim, sh.n_kv - 1);
+        bool ok = true;
+        for (int t = 0; t < nsteps; ++t) {
+            if (!mbar_wait_warp(b_mma, t & 1, abort_flag, err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int kl = klim - t * BT; // last visible key within this block
+#pragma unroll 1
+            for (int ch = 0; ch < BT / 32; ++ch) {
+                uint32_t us[32], ud[32];
+                tmem_ld32(tS + ch * 32, us);
+                tmem_ld32(tP + ch * 32, ud);
+                uint32_t dw[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float dv[2];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int k = ch * 32 + 2 * e + h2;
+                        const float p =
+                            (k <= kl) ? ex2(fmaf(__uint_as_float(us[2 * e + h2]), sh.c, -lse2))
+                                      : 0.f;
+                        dv[h2] = p * (__uint_as_float(ud[2 * e + h2]) - Dr);
+                    }
+                    dw[e] = pack2<BF16>(dv[0], dv[1]);
+                }
+                tmem_st16(tP + ch * 16, dw);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b_pready);
+        }
+        if (ok && nsteps > 0)
+            ok = mbar_wait_warp(b_done, 0, abort_flag, err);
+        tc_fence_after();
+        const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row) * D;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_off + C::ACC0 + ch * 32, u); // warp-wide
+            if (row_ok) {
+                float o[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    o[k] = (ok && nsteps > 0) ? __uint_as_float(u[k]) * sh.scale : 0.f;
+                store32<OUT>(dQ, orow + ch * 32, o);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+} // namespace bw
+
+// ------------------------------------------------------------------ host
+
+// [d, n, bh] 16-bit tensor map, box {64, 128, 1}, 128-byte swizzle.
+static bool bw_map(CUtensorMap *m, const void *ptr, int d, int n, int bh, bool bf16) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(n),
+                              static_cast<uint64_t>(bh)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2,
+                                 static_cast<uint64_t>(d) * 2 * static_cast<uint64_t>(n)};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(bw::BT), 1};
+    return make_tmap_3d_16bit(m, ptr, bf16, dims, strides, box);
+}
+
+size_t backward_workspace_bytes(int B, int Hq, int n_q) {
+    const size_t n = static_cast<size_t>(B) * Hq * n_q * sizeof(float);
+    return (n + 255) & ~static_cast<size_t>(255);
+}
+
+template <int D, bool BF16, int OUT>
+static cudaError_t backward_t(const BackwardArgs &a, cudaStream_t st) {
+    using C = bw::Cfg<D>;
+    CUtensorMap mq, mk, mv, mdo;
+    if (!bw_map(&mq, a.Q, D, a.n_q, a.B * a.Hq, BF16) ||
+        !bw_map(&mk, a.K, D, a.n_kv, a.B * a.Hkv, BF16) ||
+        !bw_map(&mv, a.V, D, a.n_kv, a.B * a.Hkv, BF16) ||
+        !bw_map(&mdo, a.dO, D, a.n_q, a.B * a.Hq, BF16))
+        return cudaErrorInvalidValue;
+    bw::Shape sh;
+    sh.B = a.B;
+    sh.Hq = a.Hq;
+    sh.Hkv = a.Hkv;
+    sh.G = a.Hq / a.Hkv;
+    sh.n_q = a.n_q;
+    sh.n_kv = a.n_kv;
+    sh.causal = a.causal;
+    sh.nqb = (a.n_q + bw::BT - 1) / bw::BT;
+    sh.nkb = (a.n_kv + bw::BT - 1) / bw::BT;
+    sh.c = a.scale * bw::kLog2e;
+    sh.scale = a.scale;
+    float *Drow = static_cast<float *>(a.workspace);
+    const long long rows = static_cast<long long>(a.B) * a.Hq * a.n_q;
+    if (a.o_f32)
+        bw::bwd_prep_kernel<D, BF16, true><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+            a.O, static_cast<const uint16_t *>(a.dO), Drow, rows);
+    else
+        bw::bwd_prep_kernel<D, BF16, false><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+            a.O, static_cast<const uint16_t *>(a.dO), Drow, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    auto kkv = bw::bwd_kv_kernel<D, BF16, OUT>;
+    e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    kkv<<<static_cast<unsigned>(sh.nkb * a.B * a.Hkv), bw::kThreads, C::SMEM, st>>>(
+        mq, mk, mv, mdo, a.lse, Drow, a.dK, a.dV, sh, a.err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    auto kq = bw::bwd_q_kernel<D, BF16, OUT>;
+    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    kq<<<static_cast<unsigned>(sh.nqb * a.B * a.Hq), bw::kThreads, C::SMEM, st>>>(
+        mq, mk, mv, mdo, a.lse, Drow, a.dQ, sh, a.err);
+    return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+static cudaError_t backward_out(const BackwardArgs &a, cudaStream_t st) {
+    switch (a.out_dtype) {
+    case 0: return backward_t<D, BF16, 0>(a, st);
+    case 1: return backward_t<D, BF16, 1>(a, st);
+    default: return backward_t<D, BF16, 2>(a, st);
+    }
+}
+
+cudaError_t backward_launch(const BackwardArgs &a, cudaStream_t st) {
+    if (a.d == 64)
+        return a.bf16 ? backward_out<64, true>(a, st) : backward_out<64, false>(a, st);
+    if (a.d == 128)
+        return a.bf16 ? backward_out<128, true>(a, st) : backward_out<128, false>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+} // namespace attn

@@ -84,6 +84,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// mbar_wait by a whole warp whose next instructions are warp-wide
+// (.sync.aligned tensor-memory loads, ldmatrix, mma.sync): the result is the
+// same in every lane, so a wait that gives up in one lane never leaves the
+// others to enter a warp-wide instruction alone.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile int *abort_flag, unsigned *err) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err));
+}
+
 // Wait used only while unwinding after an abort: ignores the abort flag so
 // that copies already in flight land before the CTA exits; still bounded.
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {

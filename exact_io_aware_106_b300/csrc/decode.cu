@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
 
     for (int u = warp; u < nunits; u += kNC) {
         const int st = u % Ly::NST;
-        if (!mbar_wait(b_full(st), (u / Ly::NST) & 1, abort_flag, err)) {
+        if (!mbar_wait_warp(b_full(st), (u / Ly::NST) & 1, abort_flag, err)) {
             ok = false;
             break;
         }

@@ -75,6 +75,22 @@ bool make_tmap_3d(CUtensorMap *m, const void *ptr, TmapElem elem, const uint64_t
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+struct BackwardArgs {
+    const void *Q, *K, *V, *O, *dO;
+    const float *lse;
+    void *dQ, *dK, *dV;
+    int B, Hq, Hkv, n_q, n_kv, d, causal;
+    float scale;
+    bool bf16;
+    bool o_f32;    // O given in fp32 (else in the inputs' 16-bit format)
+    int out_dtype; // 0 f16, 1 bf16, 2 f32
+    void *workspace;
+    unsigned *err;
+};
+
+cudaError_t backward_launch(const BackwardArgs &a, cudaStream_t st);
+size_t backward_workspace_bytes(int B, int Hq, int n_q);
+
 // 3-D tensor map over a 16-bit tensor with 128-byte swizzle and zero fill
 // outside the bounds (dims innermost first, strides in bytes for dims 1, 2).
 bool make_tmap_3d_16bit(CUtensorMap *m, const void *ptr, bool bf16, const uint64_t dims[3],

@@ -518,9 +518,10 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         if constexpr (F8) {
             for (int j = 0; j < nb_max; ++j) {
                 const int ss = j % C::NVS, vs = j % C::NV;
-                if (!mbar_wait(b_vsfull(ss), (j / C::NVS) & 1, abort_flag, err))
+                if (!mbar_wait_warp(b_vsfull(ss), (j / C::NVS) & 1, abort_flag, err))
                     break;
-                if (j >= C::NV && !mbar_wait(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
+                if (j >= C::NV &&
+                    !mbar_wait_warp(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
                     break;
                 widen_v_tile<D, BN, C::PW>(sVS + ss * C::VS_BYTES, sV + vs * C::V_BYTES, lane);
                 fence_proxy_async_smem(); // generic writes -> tensor-core reads
@@ -653,7 +654,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         bool ok = true;
 
         for (int j = 0; j < nb[t]; ++j) {
-            if (!mbar_wait(b_sfull(t), j & 1, abort_flag, err)) {
+            if (!mbar_wait_warp(b_sfull(t), j & 1, abort_flag, err)) {
                 ok = false;
                 break;
             }
@@ -718,7 +719,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             m = m_use;
         }
         if (ok && nb[t] > 0)
-            ok = mbar_wait(b_ofull, 0, abort_flag, err);
+            ok = mbar_wait_warp(b_ofull, 0, abort_flag, err);
         tc_fence_after();
         if (nb[t] > 0) {
             // ---- epilogue: O = u / l, lse = ln(sum exp(scale * s))
@@ -984,9 +985,9 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
         if constexpr (F8) {
             for (int j = 0; j < nb; ++j) {
                 const int ss = j % C::NVS, vs = j % NV;
-                if (!mbar_wait(b_vsfull(ss), (j / C::NVS) & 1, abort_flag, err))
+                if (!mbar_wait_warp(b_vsfull(ss), (j / C::NVS) & 1, abort_flag, err))
                     break;
-                if (j >= NV && !mbar_wait(b_vempty(vs), ((j / NV) - 1) & 1, abort_flag, err))
+                if (j >= NV && !mbar_wait_warp(b_vempty(vs), ((j / NV) - 1) & 1, abort_flag, err))
                     break;
                 pf::widen_v_tile<D, BN, C::PW>(sVS + ss * C::VS_BYTES, sV + vs * C::V_BYTES,
                                                lane);
@@ -1090,7 +1091,7 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
         for (int j = 0; j < nb; ++j) {
             const int buf = j & 1;
             const uint32_t tS = tmem + lane_off + S_COL0 + buf * BN;
-            if (!mbar_wait(b_sfull(buf), (j >> 1) & 1, abort_flag, err)) {
+            if (!mbar_wait_warp(b_sfull(buf), (j >> 1) & 1, abort_flag, err)) {
                 ok = false;
                 break;
             }
@@ -1130,7 +1131,7 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
             const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
             if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
                 // O must hold exactly the blocks before j: wait for P_(j-1) V_(j-1)
-                if (!mbar_wait(b_odone, (j - 1) & 1, abort_flag, err)) {
+                if (!mbar_wait_warp(b_odone, (j - 1) & 1, abort_flag, err)) {
                     ok = false;
                     break;
                 }
@@ -1156,7 +1157,7 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
             m = m_use;
         }
         if (ok && nb > 0)
-            ok = mbar_wait(b_ofull, 0, abort_flag, err);
+            ok = mbar_wait_warp(b_ofull, 0, abort_flag, err);
         tc_fence_after();
         const bool row_ok = row_g < sh.n_q;
         const float vsc = F8 ? sc.v[bkv] : 1.0f;

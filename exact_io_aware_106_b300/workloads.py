@@ -233,3 +233,15 @@ def make_paged_prefill(spec: PagedPrefillSpec, seed: int = 0, device="cpu", lens
     Vc = _randn((num_blocks, spec.Hkv, spec.block_size, spec.d), dt, g, device)
     return {"Q": Q, "Kc": Kc, "Vc": Vc, "block_table": table.to(device),
             "seq_lens": lens_t.to(device), "num_blocks": num_blocks}
+
+
+def make_backward(spec: PrefillSpec, seed: int = 0, device="cpu"):
+    """Forward inputs (as make_prefill) plus an upstream gradient dO
+    [B,Hq,n_q,d] iid N(0,1), drawn after V from the same generator."""
+    g = _gen(device, seed)
+    dt = DTYPES[spec.dtype]
+    Q = _randn((spec.B, spec.Hq, spec.n_q, spec.d), dt, g, device)
+    K = _randn((spec.B, spec.Hkv, spec.n_kv, spec.d), dt, g, device)
+    V = _randn((spec.B, spec.Hkv, spec.n_kv, spec.d), dt, g, device)
+    dO = _randn((spec.B, spec.Hq, spec.n_q, spec.d), dt, g, device)
+    return {"Q": Q, "K": K, "V": V, "dO": dO}

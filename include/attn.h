@@ -189,6 +189,35 @@ ATTN_API attn_status attn_kv_append(const void *k_new, const void *v_new, void *
                            const float *k_scale, const float *v_scale,
                            void *stream);
 
+/* Bytes of caller-provided device workspace attn_backward needs (one fp32
+ * per query row). */
+ATTN_API size_t attn_backward_workspace_bytes(int B, int Hq, int n_q);
+
+/* Backward pass (marketmaker.cc, "Flash Attention and sequence length",
+ * backward pass: probabilities recomputed from Q, K and the stored row
+ * statistic, O(n) extra memory).  For the forward O = softmax(scale Q K^T
+ * [causal]) V and upstream gradient dO:
+ *   dV = P^T dO, dP = dO V^T, D_i = sum_c dO_ic O_ic, dS = P * (dP - D),
+ *   dQ = scale dS K, dK = scale dS^T Q,
+ * dK and dV of a KV head summed over its G query heads.
+ *   Q, dO [B, Hq, n_q, d] in_dtype (F16 / BF16);  K, V [B, Hkv, n_kv, d]
+ *   O   [B, Hq, n_q, d] o_dtype: in_dtype or F32 -- the forward's output; D_i
+ *       is formed from it, so a 16-bit O moves D_i by its rounding error
+ *       (in a row that averages few keys this shows in dQ, dK at the
+ *       rounding level of O; an fp32 O removes it)
+ *   lse [B, Hq, n_q] fp32: the forward's log-sum-exp (attn_prefill)
+ *   dQ [B, Hq, n_q, d], dK, dV [B, Hkv, n_kv, d] out_dtype (F16/BF16/F32)
+ *   workspace >= attn_backward_workspace_bytes(B, Hq, n_q), 256-aligned.
+ * d in {64, 128}; causal requires n_q <= n_kv (bottom-right).  Three kernel
+ * launches (D, then dK/dV, then dQ); every gradient element is written by
+ * exactly one thread (no atomics). */
+ATTN_API attn_status attn_backward(const void *Q, const void *K, const void *V, const void *O,
+                                   const void *dO, const float *lse, void *dQ, void *dK,
+                                   void *dV, int B, int Hq, int Hkv, int n_q, int n_kv, int d,
+                                   int causal, float scale, attn_dtype in_dtype,
+                                   attn_dtype o_dtype, attn_dtype out_dtype, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
 /* Synchronises `stream`, then returns and clears the current device's error
  * word: ATTN_ERR_TIMEOUT if a bounded wait expired, ATTN_ERR_INVALID if a
  * device-side index check failed, ATTN_ERR_CUDA if the stream reports a

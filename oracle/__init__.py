@@ -65,8 +65,8 @@ def lib():
                                           i32, i32, i32, i32, i32, i32, i32, f64, vp, i32,
                                           i32, vp]
         L.oracle_decode_paged.restype = i32
-        L.oracle_backward.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32,
-                                      i32, i32, i32, i32, i32, f64, i32]
+        L.oracle_backward.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      i32, i32, i32, i32, i32, i32, i32, f64, i32]
         L.oracle_backward.restype = i32
         L.oracle_prefill_paged.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, vp, i32, i32,
                                            i32, i32, i32, i32, i32, i32, i32, f64, i32, i32,
@@ -198,10 +198,13 @@ def decode_paged(q, Kc, Vc, block_table, seq_lens, scale: float | None = None,
 
 
 def backward(Q, K, V, dO, causal: bool, scale: float | None = None, nthreads: int = 0,
-             magnitudes: bool = False):
+             magnitudes: bool = False, d_err=None):
     """Gradients of exact attention for upstream gradient dO [B,Hq,nq,d]:
     returns (dQ [B,Hq,nq,d], dK, dV [B,Hkv,nkv,d]) in fp64, plus (with
-    magnitudes=True) the per-element sums of |terms| (mag_q, mag_k, mag_v)."""
+    magnitudes=True) the per-element sums of |terms| (mag_q, mag_k, mag_v).
+    With d_err [B,Hq,nq] (a bound on a perturbation of each row's D_i), the
+    magnitudes tuple also carries the resulting bounds on the change of dQ
+    and dK (dsens_q, dsens_k)."""
     code = dtype_code(Q)
     assert dtype_code(K) == code and dtype_code(V) == code and dtype_code(dO) == code
     q, k, v, go = _as_np(Q), _as_np(K), _as_np(V), _as_np(dO)
@@ -215,13 +218,17 @@ def backward(Q, K, V, dO, causal: bool, scale: float | None = None, nthreads: in
     mq = np.zeros(q.shape, np.float64) if magnitudes else None
     mk = np.zeros(k.shape, np.float64) if magnitudes else None
     mv = np.zeros(k.shape, np.float64) if magnitudes else None
+    de = None if d_err is None else np.ascontiguousarray(np.asarray(d_err, np.float64))
+    sq = np.zeros(q.shape, np.float64) if de is not None else None
+    sk = np.zeros(k.shape, np.float64) if de is not None else None
     rc = lib().oracle_backward(_p(q), _p(k), _p(v), _p(go), code, _p(dQ), _p(dK), _p(dV),
-                               _p(mq), _p(mk), _p(mv), B, Hq, Hkv, nq, nkv, d, int(causal),
-                               float(scale), nthreads)
+                               _p(mq), _p(mk), _p(mv), _p(de), _p(sq), _p(sk), B, Hq, Hkv, nq,
+                               nkv, d, int(causal), float(scale), nthreads)
     if rc != 0:
         raise ValueError("oracle_backward: invalid arguments")
     if magnitudes:
-        return dQ, dK, dV, (mq, mk, mv)
+        mags = (mq, mk, mv) if de is None else (mq, mk, mv, sq, sk)
+        return dQ, dK, dV, mags
     return dQ, dK, dV
 
 

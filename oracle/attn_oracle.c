@@ -436,11 +436,17 @@ int oracle_decode_paged(const void *q, int q_dtype, const void *Kc,
  * Everything is materialised in fp64 per (b, h).  mag_* (optional) receive,
  * per gradient element, the sum of the absolute values of the terms it is a
  * sum of (|P_ij dO_ic| for dV, scale |dS_ij K_jc| for dQ, scale |dS_ij Q_ic|
- * for dK) -- the scale against which rounding errors are judged. */
+ * for dK) -- the scale against which rounding errors are judged.
+ * d_err (optional, [B, Hq, nq]) bounds a perturbation of each row's D_i (an
+ * implementation that forms D_i from a rounded copy of O sees one); dsens_q,
+ * dsens_k then receive the resulting bound on the change of every dQ, dK
+ * element: dS_ij moves by P_ij |dD_i|, so dQ_ic by scale d_err_i
+ * sum_j P_ij |K_jc| and dK_jc by scale sum_i P_ij d_err_i |Q_ic|. */
 int oracle_backward(const void *Q, const void *K, const void *V, const void *dO, int in_dtype,
                     double *dQ, double *dK, double *dV, double *mag_q, double *mag_k,
-                    double *mag_v, int B, int Hq, int Hkv, int nq, int nkv, int d, int causal,
-                    double scale, int nthreads) {
+                    double *mag_v, const double *d_err, double *dsens_q, double *dsens_k,
+                    int B, int Hq, int Hkv, int nq, int nkv, int d, int causal, double scale,
+                    int nthreads) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || nq <= 0 || nkv <= 0 || d <= 0 || Hq % Hkv != 0)
         return -1;
     if (causal && nq > nkv)
@@ -453,6 +459,8 @@ int oracle_backward(const void *Q, const void *K, const void *V, const void *dO,
         memset(mag_k, 0, kv_elems * sizeof(double));
     if (mag_v)
         memset(mag_v, 0, kv_elems * sizeof(double));
+    if (dsens_k)
+        memset(dsens_k, 0, kv_elems * sizeof(double));
 #ifdef _OPENMP
     if (nthreads > 0)
         omp_set_num_threads(nthreads);
@@ -504,6 +512,29 @@ int oracle_backward(const void *Q, const void *K, const void *V, const void *dO,
                 }
                 for (int j = 0; j < nkv; ++j)
                     dS[(size_t)i * nkv + j] = P[(size_t)i * nkv + j] * (dS[(size_t)i * nkv + j] - Di);
+            }
+            /* sensitivity of dQ, dK to perturbed D_i (bounds, not gradients) */
+            if (d_err && (dsens_q || dsens_k)) {
+                const double *de = d_err + ((size_t)b * Hq + h) * nq;
+                for (int i = 0; i < nq; ++i)
+                    for (int c = 0; c < d; ++c) {
+                        if (dsens_q) {
+                            double a = 0.0;
+                            for (int j = 0; j < nkv; ++j)
+                                a += P[(size_t)i * nkv + j] * fabs(k[(size_t)j * d + c]);
+                            dsens_q[qoff + (size_t)i * d + c] = scale * de[i] * a;
+                        }
+                    }
+                if (dsens_k) {
+                    double *sk = dsens_k + (size_t)bk * nkv * d;
+                    for (int j = 0; j < nkv; ++j)
+                        for (int c = 0; c < d; ++c) {
+                            double a = 0.0;
+                            for (int i = 0; i < nq; ++i)
+                                a += P[(size_t)i * nkv + j] * de[i] * fabs(q[(size_t)i * d + c]);
+                            sk[(size_t)j * d + c] += scale * a;
+                        }
+                }
             }
             /* dV += P^T dO, dK += scale dS^T Q */
             for (int j = 0; j < nkv; ++j)

@@ -65,3 +65,33 @@ def test_backward_dv_column_sums_and_magnitudes():
     # each gradient is bounded by the sum of the magnitudes of its terms
     assert (np.abs(dQ) <= mq + 1e-15).all() and (np.abs(dK) <= mk + 1e-15).all()
     assert (np.abs(dV) <= mv + 1e-15).all()
+
+
+def test_backward_d_sensitivity_bounds_a_perturbed_d():
+    """dsens_q / dsens_k bound the change of dQ / dK when every D_i moves by
+    up to d_err_i: perturb D directly (dS = P (dP - D - delta)) and compare."""
+    B, Hq, Hkv, nq, nkv, d = 1, 2, 1, 5, 7, 4
+    Q, K, V, dO = _inputs(B, Hq, Hkv, nq, nkv, d, seed=4)
+    scale = 1.0 / np.sqrt(d)
+    rng = np.random.default_rng(1)
+    delta = rng.uniform(-1, 1, (B, Hq, nq)) * 0.01
+    dQ, dK, _, (_, _, _, sq, sk) = oracle.backward(Q, K, V, dO, True, magnitudes=True,
+                                                   d_err=np.abs(delta))
+    # reference: the same gradients with D_i replaced by D_i + delta_i
+    G = Hq // Hkv
+    kk = K.repeat_interleave(G, dim=1).numpy()
+    vv = V.repeat_interleave(G, dim=1).numpy()
+    q, go = Q.numpy(), dO.numpy()
+    s = q @ kk.transpose(0, 1, 3, 2) * scale
+    i, j = np.arange(nq)[:, None], np.arange(nkv)[None, :]
+    s = np.where(j > i + (nkv - nq), -np.inf, s)
+    p = np.exp(s - s.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    dp = go @ vv.transpose(0, 1, 3, 2)
+    D = (p * dp).sum(-1, keepdims=True) + delta[..., None]
+    ds = p * (dp - D)
+    dQ2 = scale * ds @ kk
+    dK2 = (scale * ds.transpose(0, 1, 3, 2) @ q).reshape(B, Hkv, G, nkv, d).sum(2)
+    assert (np.abs(dQ2 - dQ) <= sq + 1e-12).all()
+    assert (np.abs(dK2 - dK) <= sk + 1e-12).all()
+    assert np.abs(dQ2 - dQ).max() > 0.1 * sq.max()   # the bound is not vacuous
