@@ -389,6 +389,8 @@ def workload_lines(name: str, steps: int, warmup: int):
         jobs.append(("prefill", W.PREFILL_WORKLOADS[name]))
     elif name in W.PAGED_PREFILL_WORKLOADS:
         jobs.append(("paged-prefill", W.PAGED_PREFILL_WORKLOADS[name]))
+    elif name.startswith("bwd-") and name[4:] in W.PREFILL_WORKLOADS:
+        jobs.append(("backward", W.PREFILL_WORKLOADS[name[4:]]))
     elif name in W.DECODE_TOKENS_WORKLOADS:
         base = W.DECODE_WORKLOADS["paged-decode"]
         jobs.append(("decode-tokens", (W.DECODE_TOKENS_WORKLOADS[name][0], base, name)))
@@ -427,6 +429,28 @@ def workload_lines(name: str, steps: int, warmup: int):
                             peak_tflops=peak,
                             peak_kind="measured burst bf16" + (
                                 " x 2 (nominal fp8/bf16 ratio)" if spec.dtype == "e4m3" else ""))
+            elif kind == "backward":
+                line["workload"] = "bwd-" + spec.name
+                t = W.make_backward(spec, seed=0, device=dev)
+                O, lse = attn.prefill(t["Q"], t["K"], t["V"], spec.causal,
+                                      out_dtype=W.DTYPES[spec.dtype])
+                dQ, dK, dV = (torch.empty_like(t[k]) for k in ("Q", "K", "V"))
+                ws = torch.empty(int(attn.lib().attn_backward_workspace_bytes(
+                    spec.B, spec.Hq, spec.n_q)), dtype=torch.uint8, device=dev)
+
+                def fn():
+                    attn.backward(t["Q"], t["K"], t["V"], O, t["dO"], lse, spec.causal,
+                                  dQ=dQ, dK=dK, dV=dV, workspace=ws, stream=stream)
+                med, best = _time_kernel(fn, stream, warmup, steps, flush)
+                # five products per visible pair (S, dP, dV, dK, dQ): 2.5 x the forward's
+                F = 2.5 * prefill_flops(spec)
+                roof = F / (pk["bf16_tflops"] * 1e12)
+                line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            tflops=round(F / med / 1e12, 2),
+                            pct_roofline=round(100 * roof / med, 2),
+                            peak_tflops=pk["bf16_tflops"], peak_kind="measured burst bf16",
+                            note="algorithmic flops = 5 products per pair; the kernels issue 7 "
+                                 "(S and dP are recomputed by the dQ kernel)")
             elif kind == "decode-tokens":
                 T, base, wname = spec
                 line["workload"] = wname
