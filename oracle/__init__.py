@@ -81,6 +81,8 @@ def lib():
         L.oracle_bf16_to_f64.restype = f64
         L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         L.oracle_e4m3_to_f64.restype = f64
+        L.oracle_encode_e4m3_array.argtypes = [vp, vp, ctypes.c_longlong]
+        L.oracle_encode_e4m3_array.restype = None
         L.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
         L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
         _lib = L
@@ -296,6 +298,15 @@ def dequantize_e4m3(codes, scale, head_dim: int = 1) -> np.ndarray:
     lead = int(np.prod(c.shape[:head_dim + 1]))
     assert sc.size == lead, "one scale per head"
     return (v.reshape(lead, -1) * sc[:, None]).reshape(c.shape)
+
+
+def encode_e4m3(x) -> np.ndarray:
+    """E4M3 codes (round to nearest even, saturating) of fp32 values, by the
+    oracle's own encoder."""
+    a = np.ascontiguousarray(np.asarray(x, np.float32))
+    out = np.zeros(a.shape, np.uint8)
+    lib().oracle_encode_e4m3_array(_p(a), _p(out), a.size)
+    return out
 
 
 def e4m3_decode(code: int) -> float:

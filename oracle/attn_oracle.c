@@ -121,6 +121,12 @@ uint8_t oracle_f32_to_e4m3(float xf) {
     return sign | (uint8_t)(e << 3) | (uint8_t)f;
 }
 
+/* Element-wise oracle_f32_to_e4m3 over an array. */
+void oracle_encode_e4m3_array(const float *x, uint8_t *out, long long n) {
+    for (long long i = 0; i < n; ++i)
+        out[i] = oracle_f32_to_e4m3(x[i]);
+}
+
 static double load_elem(const void *p, int dtype, size_t i) {
     switch (dtype) {
     case OR_F16: return oracle_f16_to_f64(((const uint16_t *)p)[i]);
