@@ -21,7 +21,7 @@ _DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.float8_e4m3f
 
 EXPORTS = ("attn_prefill", "attn_prefill_paged", "attn_decode_workspace_bytes", "attn_decode",
            "attn_decode_tokens", "attn_kv_append", "attn_backward",
-           "attn_backward_workspace_bytes",
+           "attn_backward_workspace_bytes", "attn_rotate_quantize_e4m3",
            "attn_last_error", "attn_status_str", "attn_last_launch_count",
            "attn_decode_static_ws")
 
@@ -69,6 +69,8 @@ def lib():
         L.attn_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                     i32, i32, f32, i32, i32, i32, vp, sz, vp]
         L.attn_backward.restype = i32
+        L.attn_rotate_quantize_e4m3.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+        L.attn_rotate_quantize_e4m3.restype = i32
         L.attn_last_error.argtypes = [vp]
         L.attn_last_error.restype = i32
         L.attn_status_str.argtypes = [i32]
@@ -196,6 +198,23 @@ def backward(Q, K, V, O, dO, lse, causal: bool, scale: float | None = None, out_
                              _ptr(workspace), workspace.numel(), _stream(stream))
     _check("attn_backward", st)
     return dQ, dK, dV
+
+
+def rotate_quantize_e4m3(X, signs, stream=None):
+    """Rows of X [..., n, d] times diag(signs) H_d, quantised to E4M3 with one
+    scale per head (all leading dims but the last two flattened).  Returns
+    (codes like X in float8_e4m3fn, scales [heads] fp32)."""
+    _cuda(X, signs)
+    d = X.shape[-1]
+    n = X.shape[-2]
+    heads = X.numel() // (n * d)
+    codes = torch.empty(X.shape, dtype=torch.float8_e4m3fn, device=X.device)
+    scales = torch.empty(heads, dtype=torch.float32, device=X.device)
+    ws = torch.empty(heads, dtype=torch.int32, device=X.device)
+    st = lib().attn_rotate_quantize_e4m3(_ptr(X), _ptr(signs), _ptr(codes), _ptr(scales),
+                                         _ptr(ws), heads, n, d, _DT[X.dtype], _stream(stream))
+    _check("attn_rotate_quantize_e4m3", st)
+    return codes, scales
 
 
 def decode_workspace_bytes(num_seqs: int, Hq: int, d: int, max_seq_len: int) -> int:

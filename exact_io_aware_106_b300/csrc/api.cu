@@ -321,6 +321,28 @@ attn_status attn_backward(const void *Q, const void *K, const void *V, const voi
     return ATTN_OK;
 }
 
+attn_status attn_rotate_quantize_e4m3(const void *X, const int8_t *signs, void *codes,
+                                      float *scales, void *amax_ws, int heads,
+                                      int rows_per_head, int d, attn_dtype in_dtype,
+                                      void *stream) {
+    t_last_launches = 0;
+    if (!X || !signs || !codes || !scales || !amax_ws || heads <= 0 || rows_per_head <= 0)
+        return ATTN_ERR_INVALID;
+    if (!is16(in_dtype) || (d != 64 && d != 128 && d != 256))
+        return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(X, 16) || !aligned(codes, 16) || !aligned(scales, 4) || !aligned(amax_ws, 4))
+        return ATTN_ERR_INVALID;
+    if (static_cast<long long>(heads) * rows_per_head > (1LL << 40))
+        return ATTN_ERR_UNSUPPORTED;
+    attn::RotQArgs a{X, signs, static_cast<uint8_t *>(codes), scales,
+                     static_cast<unsigned *>(amax_ws), heads, rows_per_head, d,
+                     in_dtype == ATTN_BF16};
+    if (attn::rotate_quantize_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = 2;
+    return ATTN_OK;
+}
+
 attn_status attn_last_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)

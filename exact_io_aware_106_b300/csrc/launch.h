@@ -89,6 +89,18 @@ struct BackwardArgs {
 };
 
 cudaError_t backward_launch(const BackwardArgs &a, cudaStream_t st);
+
+struct RotQArgs {
+    const void *X;       // [heads, rows_per_head, d] 16-bit
+    const int8_t *signs; // [d], +-1
+    uint8_t *codes;      // [heads, rows_per_head, d] E4M3
+    float *scales;       // [heads]
+    unsigned *amax_ws;   // [heads] scratch
+    int heads, rows_per_head, d;
+    bool bf16;
+};
+
+cudaError_t rotate_quantize_launch(const RotQArgs &a, cudaStream_t st);
 size_t backward_workspace_bytes(int B, int Hq, int n_q);
 
 // 3-D tensor map over a 16-bit tensor with 128-byte swizzle and zero fill

@@ -218,6 +218,24 @@ ATTN_API attn_status attn_backward(const void *Q, const void *K, const void *V, 
                                    attn_dtype o_dtype, attn_dtype out_dtype, void *workspace,
                                    size_t workspace_bytes, void *stream);
 
+/* Incoherent processing for fp8 attention (marketmaker.cc, "Flash Attention
+ * and sequence length", FA3: a random orthogonal rotation of Q and K before
+ * FP8 quantisation spreads outliers over all components).  Each row x of X
+ * becomes y = x diag(signs) H_d (H_d the Sylvester Hadamard matrix, entries
+ * +-1, unnormalised), quantised per head: scale[h] = amax_h / 448 over the
+ * head's rotated rows, codes = e4m3_rn_satfinite(y / scale[h]).  Rotating Q
+ * and K with the same signs gives (Q R)(K R)^T = d Q K^T: pass scale / d to
+ * attn_prefill with the codes (V is quantised without rotation).
+ *   X [heads, rows_per_head, d] in_dtype (F16 / BF16); signs [d] int8, +-1
+ *     (host-chosen, e.g. seeded random)
+ *   codes [heads, rows_per_head, d] E4M3; scales [heads] fp32
+ *   amax_ws: device scratch of heads * 4 bytes
+ * d in {64, 128, 256}.  One memset and two kernel launches. */
+ATTN_API attn_status attn_rotate_quantize_e4m3(const void *X, const int8_t *signs, void *codes,
+                                               float *scales, void *amax_ws, int heads,
+                                               int rows_per_head, int d, attn_dtype in_dtype,
+                                               void *stream);
+
 /* Synchronises `stream`, then returns and clears the current device's error
  * word: ATTN_ERR_TIMEOUT if a bounded wait expired, ATTN_ERR_INVALID if a
  * device-side index check failed, ATTN_ERR_CUDA if the stream reports a
