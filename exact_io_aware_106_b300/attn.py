@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libattn.so")
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 _DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.float8_e4m3fn: 3}
 
-EXPORTS = ("attn_prefill", "attn_prefill_paged", "attn_decode_workspace_bytes", "attn_decode",
+EXPORTS = ("attn_prefill", "attn_prefill_from_host", "attn_prefill_from_host_heads_per_chunk",
+           "attn_prefill_paged", "attn_decode_workspace_bytes", "attn_decode",
            "attn_decode_tokens", "attn_kv_append", "attn_backward",
            "attn_backward_workspace_bytes", "attn_rotate_quantize_e4m3",
            "attn_last_error", "attn_status_str", "attn_last_launch_count",
@@ -49,6 +50,12 @@ def lib():
         L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                    i32, i32, vp, vp, vp, vp]
         L.attn_prefill.restype = i32
+        L.attn_prefill_from_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                             i32, i32, i32, i32, i32, f32, i32, i32, vp, vp, vp,
+                                             i32, vp]
+        L.attn_prefill_from_host.restype = i32
+        L.attn_prefill_from_host_heads_per_chunk.argtypes = [i32] * 7
+        L.attn_prefill_from_host_heads_per_chunk.restype = i32
         L.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                          i32, i32, i32, i32, i32, f32, i32, i32, vp]
         L.attn_prefill_paged.restype = i32
@@ -145,6 +152,63 @@ def prefill(Q, K, V, causal: bool, scale: float | None = None, out_dtype=None, O
                             _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _stream(stream))
     _check("attn_prefill", st)
     return O, lse
+
+
+def _host(*ts):
+    for t in ts:
+        if t is not None:
+            if t.is_cuda:
+                raise ValueError("tensor must live in host memory")
+            if not t.is_contiguous():
+                raise ValueError("tensor must be contiguous")
+
+
+def prefill_from_host(hQ, hK, hV, causal: bool, scale: float | None = None, out_dtype=None,
+                      hO=None, hlse=None, want_lse: bool = True, Q=None, K=None, V=None,
+                      O=None, lse=None, q_scale=None, k_scale=None, v_scale=None,
+                      chunks: int = 0, device=None, stream=None):
+    """prefill() for host-resident hQ [B,Hq,n_q,d], hK/hV [B,Hkv,n_kv,d]: the
+    copies in and out are overlapped with the attention kernels, chunk by
+    chunk of heads.  Host tensors should be pinned.  Device buffers Q, K, V,
+    O, lse are allocated on `device` (default: the current one) when not
+    given.  Returns (hO, hlse); they are complete once `stream` has been
+    synchronised."""
+    _host(hQ, hK, hV, hO, hlse)
+    B, Hq, nq, d = hQ.shape
+    _, Hkv, nkv, _ = hK.shape
+    if device is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out_dtype is None:
+        out_dtype = torch.bfloat16 if hQ.dtype == torch.float8_e4m3fn else hQ.dtype
+    if hO is None:
+        hO = torch.empty((B, Hq, nq, d), dtype=out_dtype, pin_memory=True)
+    if hlse is None and want_lse:
+        hlse = torch.empty((B, Hq, nq), dtype=torch.float32, pin_memory=True)
+    Q = torch.empty(hQ.shape, dtype=hQ.dtype, device=device) if Q is None else Q
+    K = torch.empty(hK.shape, dtype=hK.dtype, device=device) if K is None else K
+    V = torch.empty(hV.shape, dtype=hV.dtype, device=device) if V is None else V
+    O = torch.empty(hO.shape, dtype=hO.dtype, device=device) if O is None else O
+    if hlse is not None and lse is None:
+        lse = torch.empty(hlse.shape, dtype=torch.float32, device=device)
+    _cuda(Q, K, V, O, lse, q_scale, k_scale, v_scale)
+    for h, t in ((hQ, Q), (hK, K), (hV, V), (hO, O), (hlse, lse)):
+        if (h is None) != (t is None) or (h is not None and (h.shape != t.shape or
+                                                               h.dtype != t.dtype)):
+            raise ValueError("host and device buffers differ in shape or dtype")
+    st = lib().attn_prefill_from_host(
+        _ptr(hQ), _ptr(hK), _ptr(hV), _ptr(hO), _ptr(hlse), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+        _ptr(lse), B, Hq, Hkv, nq, nkv, d, int(bool(causal)), float(scale), _DT[hQ.dtype],
+        _DT[hO.dtype], _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), int(chunks),
+        _stream(stream))
+    _check("attn_prefill_from_host", st)
+    return hO, hlse
+
+
+def prefill_from_host_heads_per_chunk(B, Hq, Hkv, n_q, d, chunks=0, sms=148) -> int:
+    """Heads per chunk attn_prefill_from_host uses (host arithmetic only)."""
+    return lib().attn_prefill_from_host_heads_per_chunk(B, Hq, Hkv, n_q, d, chunks, sms)
 
 
 def prefill_paged(Q, Kc, Vc, block_table, seq_lens, max_seq_len: int, causal: bool = True,

@@ -59,11 +59,17 @@ const char *attn_status_str(attn_status s) {
 
 int attn_last_launch_count(void) { return t_last_launches; }
 
-attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
-                         int Hq, int Hkv, int n_q, int n_kv, int d, int causal, float scale,
-                         attn_dtype in_dtype, attn_dtype out_dtype, const float *q_scale,
-                         const float *k_scale, const float *v_scale, void *stream) {
-    t_last_launches = 0;
+} // extern "C"
+
+namespace {
+
+// Host-side checks shared by attn_prefill and attn_prefill_from_host; fills
+// `a` on success.
+attn_status prefill_args(const void *Q, const void *K, const void *V, void *O, float *lse,
+                         int B, int Hq, int Hkv, int n_q, int n_kv, int d, int causal,
+                         float scale, attn_dtype in_dtype, attn_dtype out_dtype,
+                         const float *q_scale, const float *k_scale, const float *v_scale,
+                         attn::PrefillArgs *a) {
     if (!Q || !K || !V || !O)
         return ATTN_ERR_INVALID;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || n_q <= 0 || n_kv <= 0 || d <= 0 || Hq % Hkv != 0)
@@ -87,13 +93,64 @@ attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, f
     unsigned *err = err_word();
     if (!err)
         return ATTN_ERR_CUDA;
-    attn::PrefillArgs a{Q, K, V, O, lse, B, Hq, Hkv, n_q, n_kv, d, causal ? 1 : 0, scale,
-                        in_dtype == ATTN_BF16, e4, out_code(out_dtype),
-                        e4 ? q_scale : nullptr, e4 ? k_scale : nullptr,
-                        e4 ? v_scale : nullptr, err};
+    *a = attn::PrefillArgs{Q, K, V, O, lse, B, Hq, Hkv, n_q, n_kv, d, causal ? 1 : 0, scale,
+                           in_dtype == ATTN_BF16, e4, out_code(out_dtype),
+                           e4 ? q_scale : nullptr, e4 ? k_scale : nullptr,
+                           e4 ? v_scale : nullptr, err};
+    return ATTN_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                         int Hq, int Hkv, int n_q, int n_kv, int d, int causal, float scale,
+                         attn_dtype in_dtype, attn_dtype out_dtype, const float *q_scale,
+                         const float *k_scale, const float *v_scale, void *stream) {
+    t_last_launches = 0;
+    attn::PrefillArgs a;
+    const attn_status s = prefill_args(Q, K, V, O, lse, B, Hq, Hkv, n_q, n_kv, d, causal, scale,
+                                       in_dtype, out_dtype, q_scale, k_scale, v_scale, &a);
+    if (s != ATTN_OK)
+        return s;
     if (attn::prefill_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     t_last_launches = 1;
+    return ATTN_OK;
+}
+
+int attn_prefill_from_host_heads_per_chunk(int B, int Hq, int Hkv, int n_q, int d, int chunks,
+                                           int sms) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || n_q <= 0 || d <= 0 || chunks < 0 ||
+        sms <= 0)
+        return 0;
+    return attn::pipeline_heads_per_chunk(B, Hq, Hkv, n_q, d, chunks, sms);
+}
+
+attn_status attn_prefill_from_host(const void *Q_host, const void *K_host, const void *V_host,
+                                   void *O_host, float *lse_host, void *Q, void *K, void *V,
+                                   void *O, float *lse, int B, int Hq, int Hkv, int n_q,
+                                   int n_kv, int d, int causal, float scale,
+                                   attn_dtype in_dtype, attn_dtype out_dtype,
+                                   const float *q_scale, const float *k_scale,
+                                   const float *v_scale, int chunks, void *stream) {
+    t_last_launches = 0;
+    if (!Q_host || !K_host || !V_host || !O_host || (lse_host != nullptr) != (lse != nullptr))
+        return ATTN_ERR_INVALID;
+    if (chunks < 0)
+        return ATTN_ERR_INVALID;
+    attn::PrefillArgs a;
+    const attn_status s = prefill_args(Q, K, V, O, lse, B, Hq, Hkv, n_q, n_kv, d, causal, scale,
+                                       in_dtype, out_dtype, q_scale, k_scale, v_scale, &a);
+    if (s != ATTN_OK)
+        return s;
+    const attn::HostIO h{Q_host, K_host, V_host, O_host, lse_host};
+    int launches = 0;
+    if (attn::prefill_pipelined(a, h, chunks, static_cast<cudaStream_t>(stream), &launches) !=
+        cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = launches;
     return ATTN_OK;
 }
 

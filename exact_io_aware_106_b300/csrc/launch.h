@@ -75,6 +75,25 @@ bool make_tmap_3d(CUtensorMap *m, const void *ptr, TmapElem elem, const uint64_t
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Host-resident buffers of a pipelined prefill (same layouts as the device
+// ones in PrefillArgs).
+struct HostIO {
+    const void *Q;
+    const void *K;
+    const void *V;
+    void *O;
+    float *lse; // null: lse is not copied back
+};
+
+// Heads per chunk of the pipelined prefill (see pipeline.cu).
+int pipeline_heads_per_chunk(int B, int Hq, int Hkv, int n_q, int d, int want, int sms);
+
+// Prefill of `a` (device buffers) with inputs copied from and outputs copied
+// to `h` chunk by chunk, copies overlapped with compute; ordered after
+// earlier work on `st`, and later work on `st` waits for the last copy.
+cudaError_t prefill_pipelined(const PrefillArgs &a, const HostIO &h, int want_chunks,
+                              cudaStream_t st, int *launches);
+
 struct BackwardArgs {
     const void *Q, *K, *V, *O, *dO;
     const float *lse;

@@ -14,7 +14,9 @@
  * Conventions shared by every call
  *  - Every pointer argument is a DEVICE pointer unless stated otherwise; the
  *    caller owns every buffer.  The library keeps no allocation of its own
- *    beyond one 4-byte device error word per device.
+ *    beyond one 4-byte device error word per device (plus the scratch array
+ *    of attn_decode_static_ws, and the three streams and event set that
+ *    attn_prefill_from_host creates per device on first use).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls are asynchronous on that stream; results are valid once
  *    the stream has reached the call.
@@ -88,6 +90,45 @@ ATTN_API attn_status attn_prefill(const void *Q, const void *K, const void *V, v
                          int d, int causal, float scale, attn_dtype in_dtype,
                          attn_dtype out_dtype, const float *q_scale,
                          const float *k_scale, const float *v_scale, void *stream);
+
+/* attn_prefill with Q, K, V starting in host memory and O (and lse) ending
+ * there, the host<->device copies overlapped with the attention kernels
+ * (auturnal.com, "From attention to IO-aware execution" §10: the slowest
+ * memory level sets the pace -- here the host link).  The B*Hq heads are
+ * split into chunks of consecutive (batch, head) pairs, whole KV-head groups
+ * or an exact part of one; chunk c's Q (and the K, V of KV heads that begin
+ * in it) is copied in on a library-owned stream, its attention runs once the
+ * copy has landed, and its O / lse are copied out on a second library-owned
+ * stream once it is done, so that copy-in, attention and copy-out of
+ * neighbouring chunks run at the same time.
+ *   Q_host, K_host, V_host, O_host, lse_host: host buffers with the layouts
+ *     of attn_prefill's device buffers.  They should be page-locked
+ *     (cudaHostAlloc / cudaHostRegister); pageable memory gives the same
+ *     results but the copies then do not overlap.  lse_host and lse are both
+ *     NULL or both non-NULL.
+ *   Q, K, V, O, lse: caller-owned device buffers of the full sizes; on
+ *     completion they hold the inputs and outputs too.
+ *   chunks: wanted number of chunks (0: about 16, each >= 2 waves of CTAs;
+ *     rounded to what the head grouping allows, at most 64).
+ *   other arguments, checks and errors as attn_prefill.
+ * The work is ordered after everything already on `stream`, and work
+ * enqueued on `stream` after the call runs after the last copy-out: O_host
+ * is complete once `stream` has been synchronised.  Calls on one device are
+ * serialised by a lock while they enqueue.  One kernel launch per chunk. */
+ATTN_API attn_status attn_prefill_from_host(const void *Q_host, const void *K_host,
+                                            const void *V_host, void *O_host, float *lse_host,
+                                            void *Q, void *K, void *V, void *O, float *lse,
+                                            int B, int Hq, int Hkv, int n_q, int n_kv, int d,
+                                            int causal, float scale, attn_dtype in_dtype,
+                                            attn_dtype out_dtype, const float *q_scale,
+                                            const float *k_scale, const float *v_scale,
+                                            int chunks, void *stream);
+
+/* Heads per chunk attn_prefill_from_host uses for these sizes on a GPU with
+ * `sms` SMs (pure host arithmetic; the chunk count is ceil(B*Hq / result)).
+ * Returns 0 for invalid sizes. */
+ATTN_API int attn_prefill_from_host_heads_per_chunk(int B, int Hq, int Hkv, int n_q, int d,
+                                                    int chunks, int sms);
 
 /* Prefill over a block-paged KV cache: prefix caching / chunked prefill
  * (code-journey.com, "Attention co-design", short ISL over a long cached

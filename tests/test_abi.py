@@ -144,3 +144,63 @@ def test_kv_append_host_validation(L):
              None) == attn.ERR_INVALID                                 # fp8 without scales
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3, 2, 2, 100, 16, 4, 8, 1, 1, None, None,
              None) == attn.ERR_UNSUPPORTED
+
+
+def _from_host(L, **kw):
+    a = dict(hQ=FAKE, hK=FAKE, hV=FAKE, hO=FAKE, hl=None, Q=FAKE, K=FAKE, V=FAKE, O=FAKE,
+             lse=None, B=1, Hq=4, Hkv=2, nq=128, nkv=128, d=128, causal=1, scale=0.1, ind=1,
+             outd=1, chunks=0)
+    a.update(kw)
+    return L.attn_prefill_from_host(a["hQ"], a["hK"], a["hV"], a["hO"], a["hl"], a["Q"], a["K"],
+                                    a["V"], a["O"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["nq"],
+                                    a["nkv"], a["d"], a["causal"], a["scale"], a["ind"],
+                                    a["outd"], None, None, None, a["chunks"], None)
+
+
+def test_prefill_from_host_validation(L):
+    assert _from_host(L, hQ=None) == attn.ERR_INVALID
+    assert _from_host(L, hO=None) == attn.ERR_INVALID
+    assert _from_host(L, hl=FAKE) == attn.ERR_INVALID          # lse on one side only
+    assert _from_host(L, lse=FAKE) == attn.ERR_INVALID
+    assert _from_host(L, chunks=-1) == attn.ERR_INVALID
+    assert _from_host(L, Q=None) == attn.ERR_INVALID           # the device-side checks
+    assert _from_host(L, Hq=3) == attn.ERR_INVALID
+    assert _from_host(L, d=96) == attn.ERR_UNSUPPORTED
+    assert _from_host(L, ind=3) == attn.ERR_INVALID            # E4M3 without scales
+    assert L.attn_last_launch_count() == 0
+
+
+def _hpc(B, Hq, Hkv, n, d, chunks, sms=148):
+    return attn.prefill_from_host_heads_per_chunk(B, Hq, Hkv, n, d, chunks, sms)
+
+
+def test_prefill_from_host_chunk_plan(L):
+    # 64 query heads over 8 KV heads, 32768 rows (128 CTAs per head): 16 chunks
+    # of half a group by default, whole groups when 8 are asked for
+    assert _hpc(1, 64, 8, 32768, 128, 0) == 4
+    assert _hpc(1, 64, 8, 32768, 128, 8) == 8
+    assert _hpc(1, 64, 8, 32768, 128, 1) == 64
+    assert _hpc(1, 64, 8, 32768, 128, 3) == 24          # ceil(8/3) = 3 groups per chunk
+    # a small problem (2 CTAs per head) stays in one chunk by default
+    assert _hpc(1, 4, 2, 300, 128, 0) == 4
+    # more chunks than groups: the smallest divisor m of G with groups*m >= want
+    assert _hpc(1, 12, 1, 4096, 128, 5) == 2            # m = 6
+    # never more than 64 chunks
+    assert _hpc(40, 2, 1, 4096, 128, 64) == 2           # 80 would be needed: whole groups
+    assert _hpc(1, 4, 3, 128, 128, 0) == 0              # Hq % Hkv != 0
+    assert _hpc(1, 4, 2, 128, 128, -1) == 0
+
+
+def test_prefill_from_host_chunk_plan_is_always_valid(L):
+    import itertools
+    for B, Hkv, G, n, d, want in itertools.product((1, 2, 3), (1, 2, 8), (1, 2, 3, 4, 8, 16),
+                                                   (1, 300, 4096, 65536), (64, 128, 256),
+                                                   (0, 1, 2, 5, 16, 64, 100)):
+        Hq = Hkv * G
+        h = _hpc(B, Hq, Hkv, n, d, want)
+        assert h >= 1
+        assert h % G == 0 or G % h == 0, (B, Hq, Hkv, h)     # whole groups or a part of one
+        F = B * Hq
+        assert h <= max(F, G) and -(-F // h) <= 64
+        if h % G == 0 and h > G:
+            assert F % G == 0
