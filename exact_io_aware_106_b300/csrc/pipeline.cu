@@ -61,7 +61,10 @@ cudaError_t init_ctx(PipeCtx &c) {
 // Heads per chunk for F = B*Hq flattened heads in groups of G (one KV head
 // each): a whole number of groups, or an exact divisor of G, so that every
 // chunk is a valid prefill on its own (B' = 1, Hq' = heads, Hkv' = heads/G or
-// 1).  `want` = 0 picks about 16 chunks, each at least two waves of CTAs.
+// 1).  `want` = 0 picks about 32 chunks, each at least one wave of CTAs:
+// the first chunk's copy-in and the last chunk's copy-out are the only
+// copies nothing hides, so smaller chunks shorten them, while the two
+// alternating compute streams hide the tails of small launches.
 int pipeline_heads_per_chunk(int B, int Hq, int Hkv, int n_q, int d, int want, int sms) {
     const long long F = static_cast<long long>(B) * Hq;
     const int G = Hq / Hkv;
@@ -69,9 +72,9 @@ int pipeline_heads_per_chunk(int B, int Hq, int Hkv, int n_q, int d, int want, i
     if (want <= 0) {
         const long long rows_per_cta = d > 128 ? 128 : 256;
         const long long ctas_per_head = (n_q + rows_per_cta - 1) / rows_per_cta;
-        const long long min_heads = (2LL * sms + ctas_per_head - 1) / ctas_per_head;
+        const long long min_heads = (sms + ctas_per_head - 1) / ctas_per_head;
         long long w = F / (min_heads > 0 ? min_heads : 1);
-        want = static_cast<int>(w < 1 ? 1 : (w > 16 ? 16 : w));
+        want = static_cast<int>(w < 1 ? 1 : (w > 32 ? 32 : w));
     }
     if (want > kMaxChunks)
         want = kMaxChunks;

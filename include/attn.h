@@ -108,7 +108,7 @@ ATTN_API attn_status attn_prefill(const void *Q, const void *K, const void *V, v
  *     NULL or both non-NULL.
  *   Q, K, V, O, lse: caller-owned device buffers of the full sizes; on
  *     completion they hold the inputs and outputs too.
- *   chunks: wanted number of chunks (0: about 16, each >= 2 waves of CTAs;
+ *   chunks: wanted number of chunks (0: about 32, each >= 1 wave of CTAs;
  *     rounded to what the head grouping allows, at most 64).
  *   other arguments, checks and errors as attn_prefill.
  * The work is ordered after everything already on `stream`, and work

@@ -175,14 +175,17 @@ def _hpc(B, Hq, Hkv, n, d, chunks, sms=148):
 
 
 def test_prefill_from_host_chunk_plan(L):
-    # 64 query heads over 8 KV heads, 32768 rows (128 CTAs per head): 16 chunks
-    # of half a group by default, whole groups when 8 are asked for
-    assert _hpc(1, 64, 8, 32768, 128, 0) == 4
+    # 64 query heads over 8 KV heads, 32768 rows (128 CTAs per head): 32 chunks
+    # of a quarter group by default, whole groups when 8 are asked for
+    assert _hpc(1, 64, 8, 32768, 128, 0) == 2
+    assert _hpc(1, 64, 8, 32768, 128, 16) == 4
     assert _hpc(1, 64, 8, 32768, 128, 8) == 8
     assert _hpc(1, 64, 8, 32768, 128, 1) == 64
     assert _hpc(1, 64, 8, 32768, 128, 3) == 24          # ceil(8/3) = 3 groups per chunk
     # a small problem (2 CTAs per head) stays in one chunk by default
     assert _hpc(1, 4, 2, 300, 128, 0) == 4
+    # 8 query heads of 16 CTAs each (4096 rows): 148 SMs need 10 heads, so one chunk
+    assert _hpc(1, 8, 2, 4096, 128, 0) == 8
     # more chunks than groups: the smallest divisor m of G with groups*m >= want
     assert _hpc(1, 12, 1, 4096, 128, 5) == 2            # m = 6
     # never more than 64 chunks
