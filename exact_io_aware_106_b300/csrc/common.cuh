@@ -415,6 +415,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction (three-input max, sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
 // Pack two floats as 16-bit values, `lo` in the low half.
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {

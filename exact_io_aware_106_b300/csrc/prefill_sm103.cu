@@ -288,32 +288,36 @@ __device__ __forceinline__ bool tile_split(const Shape &sh, int q0, int t) {
 // p = 2^(s*c - m) for the NB scores of this thread's row, packed to 16 bits
 // and stored over the consumed scores (P_hi in columns [0, NB/2) of the S
 // tile; with SPLIT, the rounding residual p - P_hi in columns [NB/2, NB)).
-// Returns the row sum of p (fp32, eight independent partial sums).
+// Returns the row sum of p (fp32, eight independent partial sums).  The
+// score scaling and the sums run as packed pairs (fma/add .f32x2: one
+// instruction per two elements, each lane rounded as the scalar form).
 template <int NB, bool BF16, bool SPLIT>
 __device__ __forceinline__ float exp_pack_store(const float (&s)[NB], float c, float neg,
                                                 uint32_t tS) {
-    float acc[8];
+    float2 acc[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        acc[i] = 0.f;
+    for (int i = 0; i < 4; ++i)
+        acc[i] = make_float2(0.f, 0.f);
+    const float2 c2 = make_float2(c, c), n2 = make_float2(neg, neg);
 #pragma unroll
     for (int ch = 0; ch < NB / 32; ++ch) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(s[ch * 32 + 2 * i], c, neg));
-            const float p1 = ex2(fmaf(s[ch * 32 + 2 * i + 1], c, neg));
-            acc[(2 * i) & 7] += p0;
-            acc[(2 * i + 1) & 7] += p1;
-            hi[i] = pack2<BF16>(p0, p1);
+            const float2 x =
+                __ffma2_rn(make_float2(s[ch * 32 + 2 * i], s[ch * 32 + 2 * i + 1]), c2, n2);
+            const float2 p = make_float2(ex2(x.x), ex2(x.y));
+            acc[i & 3] = __fadd2_rn(acc[i & 3], p);
+            hi[i] = pack2<BF16>(p.x, p.y);
             if constexpr (SPLIT)
-                lo[i] = pack2<BF16>(p0 - lo16<BF16>(hi[i]), p1 - hi16<BF16>(hi[i]));
+                lo[i] = pack2<BF16>(p.x - lo16<BF16>(hi[i]), p.y - hi16<BF16>(hi[i]));
         }
         tmem_st16(tS + ch * 16, hi);
         if constexpr (SPLIT)
             tmem_st16(tS + NB / 2 + ch * 16, lo);
     }
-    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+           ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
 }
 
 // Widen one E4M3 V tile [ROWS][D] (panels of PW-byte rows, PW-byte swizzle)
@@ -678,16 +682,17 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                     if (k > lim)
                         s[k] = -INFINITY;
             }
-            // row max as a tree: eight independent chains, then 8 -> 1
+            // row max as a tree of three-input maxima: eight independent
+            // chains taking two scores per step, then 8 -> 1
             float mx8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                mx8[i] = s[i];
+                mx8[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-            for (int k = 8; k < BN; ++k)
-                mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            for (int k = 16; k < BN; k += 2)
+                mx8[(k >> 1) & 7] = max3(mx8[(k >> 1) & 7], s[k], s[k + 1]);
+            const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                                   fmaxf(max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_blk = mx * c;
             float m_use = m;
             if (m_blk > m + kRescaleThreshold || m == -INFINITY)
@@ -704,9 +709,15 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t u[32];
                     tmem_ld32(tO + ch * 32, u);
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 v = __fmul2_rn(
+                            make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])),
+                            a2);
+                        u[2 * i] = __float_as_uint(v.x);
+                        u[2 * i + 1] = __float_as_uint(v.y);
+                    }
                     tmem_st32(tO + ch * 32, u);
                 }
             }
@@ -1116,12 +1127,12 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
             float mx8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                mx8[i] = s[i];
+                mx8[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-            for (int k = 8; k < BN; ++k)
-                mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            for (int k = 16; k < BN; k += 2)
+                mx8[(k >> 1) & 7] = max3(mx8[(k >> 1) & 7], s[k], s[k + 1]);
+            const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                                   fmaxf(max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_blk = mx * c;
             float m_use = m;
             if (m_blk > m + pf::kRescaleThreshold || m == -INFINITY)
