@@ -14,13 +14,18 @@
 //   bwd_prep_kernel   D = rowsum(dO * O), one warp per row.
 //   bwd_kv_kernel     one CTA per (b, KV head, 128-key block): K and V stay
 //                     in shared memory; for every query head of the group
-//                     and every query block that sees the keys,
+//                     and every query block that sees the keys, in two
+//                     half-steps of 64 queries,
 //                       S^T = K Q^T, dP^T = V dO^T        (tcgen05, TMEM)
 //                       P^T, dS^T                          (4 warps, one key row each)
 //                       dV += P^T dO, dK += dS^T Q         (tcgen05, A = TMEM)
 //   bwd_q_kernel      one CTA per (b, head, 128-row query block): for every
-//                     key block it sees, S = Q K^T, dP = dO V^T, dS, and
+//                     64 keys it sees, S = Q K^T, dP = dO V^T, dS, and
 //                     dQ += dS K.
+// The score blocks of consecutive half-steps alternate between two tensor-
+// memory buffers: the tensor core computes the scores of half-step h+1 (and
+// after the second products of h, those of h+2) while the four softmax warps
+// turn half-step h's scores into P and dS, so neither waits for the other.
 // P and dS enter the second products in the inputs' 16-bit format; the
 // accumulators are fp32 in tensor memory.  Scores are in the log2 domain:
 // p = 2^(s c - lse log2 e), c = scale log2 e.
@@ -32,6 +37,7 @@ namespace attn {
 namespace bw {
 
 constexpr int BT = 128; // rows of a key block and of a query block
+constexpr int HS = 64;  // columns of a half-step (queries for dK/dV, keys for dQ)
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -44,12 +50,16 @@ struct Cfg {
     static constexpr int NS = 2;                     // stages of the streamed pair of tiles
     static constexpr int OFF_A = 0;                  // resident tile pair (K,V or Q,dO)
     static constexpr int OFF_S = OFF_A + 2 * TILE;   // NS stages of the streamed pair
-    static constexpr int OFF_ROW = OFF_S + NS * 2 * TILE; // per-step lse2 / D of 128 rows
-    static constexpr int OFF_BAR = OFF_ROW + 2 * BT * 4;
-    static constexpr int NBAR = 1 + 2 * NS + 2 + 2;  // afull, sfull/sempty[NS], mma_s, p_ready, done, drain
+    static constexpr int OFF_ROW = OFF_S + NS * 2 * TILE; // -lse2 / -D of 128 rows, 2 buffers
+    static constexpr int OFF_BAR = OFF_ROW + 2 * 2 * BT * 4;
+    // afull, sfull/sempty[NS], mma[2], pready[2], done, drain
+    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
-    static constexpr int S_COL = 0, DP_COL = BT, ACC0 = 2 * BT, ACC1 = 2 * BT + D;
+    // half-step buffer e: scores at 128 e, second product at 128 e + 64
+    __host__ __device__ static constexpr int S_COL(int e) { return e * BT; }
+    __host__ __device__ static constexpr int DP_COL(int e) { return e * BT + HS; }
+    static constexpr int ACC0 = 2 * BT, ACC1 = 2 * BT + D;
     static_assert(2 * BT + 2 * D <= 512, "tensor memory budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -116,28 +126,30 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *map, 
         tma_load_3d(dst + p * BT * 128, map, bar, p * 64, row, bh);
 }
 
-// Issues acc += A(tmem, 128 x 128 in 16-bit, K = 128) * B(smem tile,
-// MN-major: K = tile rows, N = D).
+// Issues acc += A(tmem, 128 rows x 64 in 16-bit, two per column) *
+// B(rows [64 e, 64 e + 64) of a 128-row smem tile, MN-major: K = tile rows,
+// N = D): one half-step's second product.
 template <int D>
-__device__ __forceinline__ void mma_tmem_a(uint32_t acc, uint32_t a_tmem, uint32_t b_tile,
-                                           uint32_t idesc, bool first) {
+__device__ __forceinline__ void mma_tmem_a_half(uint32_t acc, uint32_t a_tmem, uint32_t b_tile,
+                                                int e, uint32_t idesc, bool first) {
 #pragma unroll
-    for (int k = 0; k < BT / 16; ++k) {
-        const uint64_t bd = sdesc_sw128(b_tile + k * 16 * 128, BT * 128, 1024);
+    for (int k = 0; k < HS / 16; ++k) {
+        const uint64_t bd = sdesc_sw128(b_tile + (e * (HS / 16) + k) * 16 * 128, BT * 128, 1024);
         mma_ts(acc, a_tmem + k * 8, bd, idesc, (first && k == 0) ? 0u : 1u);
     }
 }
 
-// Issues acc = A(smem tile, K-major, 128 rows) * B(smem tile, K-major,
-// 128 rows)^T over K = D.
+// Issues acc = A(smem tile, K-major, 128 rows) * B(rows [64 e, 64 e + 64) of
+// a smem tile, K-major)^T over K = D: a 128 x 64 score block.
 template <int D>
-__device__ __forceinline__ void mma_ss_tiles(uint32_t acc, uint32_t a_tile, uint32_t b_tile,
-                                             uint32_t idesc) {
+__device__ __forceinline__ void mma_ss_half(uint32_t acc, uint32_t a_tile, uint32_t b_tile, int e,
+                                            uint32_t idesc) {
+    const uint32_t bh = b_tile + e * HS * 128; // 64 rows into every 128-byte panel
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k / 4) * (BT * 128) + (k % 4) * 32;
-        mma_ss(acc, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024),
-               idesc, k > 0 ? 1u : 0u);
+        mma_ss(acc, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(bh + off, 16, 1024), idesc,
+               k > 0 ? 1u : 0u);
     }
 }
 
@@ -178,7 +190,11 @@ __device__ __forceinline__ int key_blocks(const Shape &sh, int qb) {
 }
 
 // ========================================================================
-// dK, dV: one CTA per (b, KV head, key block)
+// dK, dV: one CTA per (b, KV head, key block).  Step t = (query head of the
+// group, query block); each step is two half-steps of 64 queries whose
+// scores live in the two tensor-memory buffers, so that S^T, dP^T of the
+// half-step two ahead are computed while the softmax warps work on the
+// current one.
 template <int D, bool BF16, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -195,29 +211,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sK = base_s + C::OFF_A, sV = sK + C::TILE;
     auto sQ = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE; };
     auto sDO = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE + C::TILE; };
-    float *s_lse2 = reinterpret_cast<float *>(base + C::OFF_ROW);
-    float *s_D = s_lse2 + BT;
+    // per step: -lse * log2(e) and -D of its 128 queries, double-buffered
+    float *s_row = reinterpret_cast<float *>(base + C::OFF_ROW);
     const uint32_t bar0 = base_s + C::OFF_BAR;
     const uint32_t b_afull = bar0;
     auto b_sfull = [&](int i) { return bar0 + 8u * (1 + i); };
     auto b_sempty = [&](int i) { return bar0 + 8u * (1 + C::NS + i); };
-    const uint32_t b_mma = bar0 + 8u * (1 + 2 * C::NS);    // S^T, dP^T of a step are in TMEM
-    const uint32_t b_pready = b_mma + 8u;                 // P^T, dS^T of a step are in TMEM
-    const uint32_t b_done = b_pready + 8u;
+    auto b_mma = [&](int e) { return bar0 + 8u * (1 + 2 * C::NS + e); };    // S^T, dP^T ready
+    auto b_pready = [&](int e) { return bar0 + 8u * (3 + 2 * C::NS + e); }; // P^T, dS^T ready
+    const uint32_t b_done = bar0 + 8u * (5 + 2 * C::NS);
     const uint32_t b_drain = b_done + 8u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // heaviest key blocks first (causal: early keys are seen by more queries)
-    const int per_bkv = sh.nkb;
     const int kb = static_cast<int>(blockIdx.x) / (sh.B * sh.Hkv);
     const int bkv = static_cast<int>(blockIdx.x) % (sh.B * sh.Hkv);
-    (void)per_bkv;
     const int b = bkv / sh.Hkv, hk = bkv % sh.Hkv;
     const int qb0 = first_qblock(sh, kb);
     const int nq_steps = sh.nqb - qb0;     // query blocks per query head
     const int nsteps = sh.G * nq_steps;    // (head, query block) steps
+    const int nhalf = 2 * nsteps;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -226,8 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_sfull(i), 1);
             mbar_init(b_sempty(i), 1);
         }
-        mbar_init(b_mma, 1);
-        mbar_init(b_pready, 4);
+        for (int e = 0; e < 2; ++e) {
+            mbar_init(b_mma(e), 1);
+            mbar_init(b_pready(e), 4);
+        }
         mbar_init(b_done, 1);
         mbar_init(b_drain, 1);
         fence_barrier_init();
@@ -268,32 +285,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16(BT, BT, BF16, false, false);
+            constexpr uint32_t idesc_s = idesc_f16(BT, HS, BF16, false, false);
             constexpr uint32_t idesc_acc = idesc_f16(BT, D, BF16, false, true);
+            // S^T = K Q_e^T, dP^T = V dO_e^T of half-step h into buffer h mod 2
+            auto issue_scores = [&](int h) {
+                const int st = (h >> 1) % C::NS, e = h & 1;
+                mma_ss_half<D>(tmem + C::S_COL(e), sK, sQ(st), e, idesc_s);
+                mma_ss_half<D>(tmem + C::DP_COL(e), sV, sDO(st), e, idesc_s);
+                tc_commit(b_mma(e));
+            };
             bool ok = mbar_wait(b_afull, 0, abort_flag, err);
-            for (int t = 0; ok && t <= nsteps; ++t) {
-                if (t > 0) {
-                    // second products of step t-1: P^T, dS^T are in TMEM
-                    const int sp = (t - 1) % C::NS;
-                    if (!mbar_wait(b_pready, (t - 1) & 1, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
+            if (ok && nsteps > 0) {
+                ok = mbar_wait(b_sfull(0), 0, abort_flag, err);
+                if (ok) {
                     tc_fence_after();
-                    mma_tmem_a<D>(tmem + C::ACC0, tmem + C::S_COL, sDO(sp), idesc_acc, t == 1);
-                    mma_tmem_a<D>(tmem + C::ACC1, tmem + C::DP_COL, sQ(sp), idesc_acc, t == 1);
-                    tc_commit(b_sempty(sp));
+                    issue_scores(0);
+                    issue_scores(1);
                 }
-                if (t < nsteps) {
-                    const int st = t % C::NS;
-                    if (!mbar_wait(b_sfull(st), (t / C::NS) & 1, abort_flag, err)) {
+            }
+            for (int h = 0; ok && h < nhalf; ++h) {
+                const int t = h >> 1, e = h & 1, st = t % C::NS;
+                if (!mbar_wait(b_pready(e), t & 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // dV += P^T dO_e, dK += dS^T Q_e (the half-step's 64 queries)
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::S_COL(e), sDO(st), e, idesc_acc,
+                                   h == 0);
+                mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL(e), sQ(st), e, idesc_acc,
+                                   h == 0);
+                if (e == 1)
+                    tc_commit(b_sempty(st)); // both halves of step t consumed
+                const int hn = h + 2;
+                if (hn < nhalf) {
+                    const int tn = hn >> 1;
+                    if (e == 0 &&
+                        !mbar_wait(b_sfull(tn % C::NS), (tn / C::NS) & 1, abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    mma_ss_tiles<D>(tmem + C::S_COL, sK, sQ(st), idesc_s);  // S^T = K Q^T
-                    mma_ss_tiles<D>(tmem + C::DP_COL, sV, sDO(st), idesc_s); // dP^T = V dO^T
-                    tc_commit(b_mma);
+                    // into the buffer the products above read (issued after them)
+                    issue_scores(hn);
                 }
             }
             if (ok)
@@ -306,55 +340,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = warp * 32 + lane; // key within the block
         const int key = kb * BT + j;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tS = tmem + lane_off + C::S_COL;
-        const uint32_t tP = tmem + lane_off + C::DP_COL;
         const int off = sh.n_kv - sh.n_q;
         const bool key_ok = key < sh.n_kv;
+        // query rows of step t (thread j fetches query j's statistics one
+        // step ahead, so the global loads are off the critical path)
+        auto fetch = [&](int t, float &nl, float &nd) {
+            nl = -INFINITY, nd = 0.f; // queries past n_q: p = 2^-inf = 0
+            if (t < nsteps) {
+                const int bh = b * sh.Hq + hk * sh.G + t / nq_steps;
+                const int q = (qb0 + t % nq_steps) * BT + j;
+                if (q < sh.n_q) {
+                    nl = -lse[static_cast<size_t>(bh) * sh.n_q + q] * kLog2e;
+                    nd = -Drow[static_cast<size_t>(bh) * sh.n_q + q];
+                }
+            }
+        };
+        float nl, nd;
+        fetch(0, nl, nd);
         bool ok = true;
-        for (int t = 0; t < nsteps; ++t) {
-            const int h = hk * sh.G + t / nq_steps;
+        for (int h = 0; h < nhalf; ++h) {
+            const int t = h >> 1, e = h & 1;
             const int qb = qb0 + t % nq_steps;
-            const int bh = b * sh.Hq + h;
-            // this step's per-query lse (log2 domain) and D, one row per thread
-            {
-                const int q = qb * BT + j;
-                const bool q_ok = q < sh.n_q;
-                asm volatile("bar.sync 1, 128;" ::: "memory"); // previous step's reads done
-                s_lse2[j] = q_ok ? lse[static_cast<size_t>(bh) * sh.n_q + q] * kLog2e : INFINITY;
-                s_D[j] = q_ok ? Drow[static_cast<size_t>(bh) * sh.n_q + q] : 0.f;
+            float *rl = s_row + (t & 1) * 2 * BT; // -lse2 of the step's 128 queries
+            float *rd = rl + BT;                  // -D
+            if (e == 0) {
+                // buffer t&1 was last read in step t-2; every warp has passed
+                // step t-1's barrier since, so it is free
+                rl[j] = nl;
+                rd[j] = nd;
                 asm volatile("bar.sync 1, 128;" ::: "memory");
+                fetch(t + 1, nl, nd);
             }
             // after a failed wait the warp keeps looping (and meeting the
-            // named barriers above) without touching tensor memory, so that
+            // named barrier above) without touching tensor memory, so that
             // its sibling warps never wait on it there
-            if (!ok || !mbar_wait_warp(b_mma, t & 1, abort_flag, err)) {
+            if (!ok || !mbar_wait_warp(b_mma(e), t & 1, abort_flag, err)) {
                 ok = false;
                 continue;
             }
             tc_fence_after();
-            // query i of this block sees this key iff key <= qb*BT + i + off
+            const uint32_t tS = tmem + lane_off + C::S_COL(e);
+            const uint32_t tP = tmem + lane_off + C::DP_COL(e);
+            // query i (of the step's block) sees this key iff key <= qb*BT + i + off
+            const int i0 = e * HS;
             const int i_min = key - off - qb * BT; // first visible query (causal)
-#pragma unroll 1
-            for (int ch = 0; ch < BT / 32; ++ch) {
+            const bool mask = !key_ok || (sh.causal && i_min > i0);
+            const float2 c2 = make_float2(sh.c, sh.c);
+#pragma unroll
+            for (int ch = 0; ch < HS / 32; ++ch) {
                 uint32_t us[32], ud[32];
                 tmem_ld32(tS + ch * 32, us);
                 tmem_ld32(tP + ch * 32, ud);
                 uint32_t pw[16], dw[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pv[2], dv[2];
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const int ib = i0 + ch * 32 + 4 * q4;
+                    const float4 l4 = *reinterpret_cast<const float4 *>(rl + ib);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(rd + ib);
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int i = ch * 32 + 2 * e + h2;
-                        const bool vis = key_ok && (!sh.causal || i >= i_min);
-                        const float p =
-                            vis ? ex2(fmaf(__uint_as_float(us[2 * e + h2]), sh.c, -s_lse2[i]))
-                                : 0.f;
-                        pv[h2] = p;
-                        dv[h2] = p * (__uint_as_float(ud[2 * e + h2]) - s_D[i]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int e2 = 4 * q4 + 2 * hh; // element pair within the chunk
+                        const float2 x = __ffma2_rn(
+                            make_float2(__uint_as_float(us[e2]), __uint_as_float(us[e2 + 1])), c2,
+                            hh ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+                        float2 p = make_float2(ex2(x.x), ex2(x.y));
+                        if (mask) {
+                            if (!key_ok || ib + 2 * hh < i_min)
+                                p.x = 0.f;
+                            if (!key_ok || ib + 2 * hh + 1 < i_min)
+                                p.y = 0.f;
+                        }
+                        const float2 g = __fadd2_rn(
+                            make_float2(__uint_as_float(ud[e2]), __uint_as_float(ud[e2 + 1])),
+                            hh ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
+                        const float2 ds = __fmul2_rn(p, g);
+                        pw[e2 / 2] = pack2<BF16>(p.x, p.y);
+                        dw[e2 / 2] = pack2<BF16>(ds.x, ds.y);
                     }
-                    pw[e] = pack2<BF16>(pv[0], pv[1]);
-                    dw[e] = pack2<BF16>(dv[0], dv[1]);
                 }
                 tmem_st16(tS + ch * 16, pw);
                 tmem_st16(tP + ch * 16, dw);
@@ -363,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(b_pready);
+                mbar_arrive(b_pready(e));
         }
         if (ok && nsteps > 0)
             ok = mbar_wait_warp(b_done, 0, abort_flag, err);
@@ -398,7 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ========================================================================
-// dQ: one CTA per (b, query head, query block)
+// dQ: one CTA per (b, query head, query block).  Step t = key block; each
+// step is two half-steps of 64 keys, double-buffered in tensor memory as in
+// the dK/dV kernel.  Half-steps past the last visible key are not computed.
 template <int D, bool BF16, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -418,20 +482,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_afull = bar0;
     auto b_sfull = [&](int i) { return bar0 + 8u * (1 + i); };
     auto b_sempty = [&](int i) { return bar0 + 8u * (1 + C::NS + i); };
-    const uint32_t b_mma = bar0 + 8u * (1 + 2 * C::NS);
-    const uint32_t b_pready = b_mma + 8u;
-    const uint32_t b_done = b_pready + 8u;
+    auto b_mma = [&](int e) { return bar0 + 8u * (1 + 2 * C::NS + e); };
+    auto b_pready = [&](int e) { return bar0 + 8u * (3 + 2 * C::NS + e); };
+    const uint32_t b_done = bar0 + 8u * (5 + 2 * C::NS);
     const uint32_t b_drain = b_done + 8u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int BH = sh.B * sh.Hq;
-    const int qb = sh.nqb - 1 - static_cast<int>(blockIdx.x) / BH; // heaviest first
-    const int bh = static_cast<int>(blockIdx.x) % BH;
+    const int nbh = sh.B * sh.Hq;
+    const int qb = sh.nqb - 1 - static_cast<int>(blockIdx.x) / nbh; // heaviest first
+    const int bh = static_cast<int>(blockIdx.x) % nbh;
     const int b = bh / sh.Hq, h = bh % sh.Hq;
     const int bkv = b * sh.Hkv + h / sh.G;
-    const int nsteps = key_blocks(sh, qb);
+    // 64-key half-steps up to the block's last visible key; 128-key stages
+    int keys = sh.n_kv;
+    if (sh.causal)
+        keys = min(keys, min(qb * BT + BT - 1, sh.n_q - 1) + (sh.n_kv - sh.n_q) + 1);
+    const int nhalf = (keys + HS - 1) / HS;
+    const int nsteps = (nhalf + 1) / 2;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -440,8 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_sfull(i), 1);
             mbar_init(b_sempty(i), 1);
         }
-        mbar_init(b_mma, 1);
-        mbar_init(b_pready, 4);
+        for (int e = 0; e < 2; ++e) {
+            mbar_init(b_mma(e), 1);
+            mbar_init(b_pready(e), 4);
+        }
         mbar_init(b_done, 1);
         mbar_init(b_drain, 1);
         fence_barrier_init();
@@ -479,30 +550,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16(BT, BT, BF16, false, false);
+            constexpr uint32_t idesc_s = idesc_f16(BT, HS, BF16, false, false);
             constexpr uint32_t idesc_acc = idesc_f16(BT, D, BF16, false, true);
+            // S = Q K_e^T, dP = dO V_e^T of half-step h into buffer h mod 2
+            auto issue_scores = [&](int h) {
+                const int st = (h >> 1) % C::NS, e = h & 1;
+                mma_ss_half<D>(tmem + C::S_COL(e), sQ, sK(st), e, idesc_s);
+                mma_ss_half<D>(tmem + C::DP_COL(e), sDO, sV(st), e, idesc_s);
+                tc_commit(b_mma(e));
+            };
             bool ok = mbar_wait(b_afull, 0, abort_flag, err);
-            for (int t = 0; ok && t <= nsteps; ++t) {
-                if (t > 0) {
-                    const int sp = (t - 1) % C::NS;
-                    if (!mbar_wait(b_pready, (t - 1) & 1, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
+            if (ok && nhalf > 0) {
+                ok = mbar_wait(b_sfull(0), 0, abort_flag, err);
+                if (ok) {
                     tc_fence_after();
-                    mma_tmem_a<D>(tmem + C::ACC0, tmem + C::DP_COL, sK(sp), idesc_acc, t == 1);
-                    tc_commit(b_sempty(sp));
+                    issue_scores(0);
+                    if (nhalf > 1)
+                        issue_scores(1);
                 }
-                if (t < nsteps) {
-                    const int st = t % C::NS;
-                    if (!mbar_wait(b_sfull(st), (t / C::NS) & 1, abort_flag, err)) {
+            }
+            for (int hs = 0; ok && hs < nhalf; ++hs) {
+                const int t = hs >> 1, e = hs & 1, st = t % C::NS;
+                if (!mbar_wait(b_pready(e), t & 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // dQ += dS K_e (the half-step's 64 keys)
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL(e), sK(st), e, idesc_acc,
+                                   hs == 0);
+                if (e == 1)
+                    tc_commit(b_sempty(st));
+                const int hn = hs + 2;
+                if (hn < nhalf) {
+                    const int tn = hn >> 1;
+                    if (e == 0 &&
+                        !mbar_wait(b_sfull(tn % C::NS), (tn / C::NS) & 1, abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    mma_ss_tiles<D>(tmem + C::S_COL, sQ, sK(st), idesc_s);   // S = Q K^T
-                    mma_ss_tiles<D>(tmem + C::DP_COL, sDO, sV(st), idesc_s); // dP = dO V^T
-                    tc_commit(b_mma);
+                    issue_scores(hn);
                 }
             }
             if (ok)
@@ -516,39 +604,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = qb * BT + i;
         const bool row_ok = row < sh.n_q;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tS = tmem + lane_off + C::S_COL;
-        const uint32_t tP = tmem + lane_off + C::DP_COL;
-        const float lse2 =
-            row_ok ? lse[static_cast<size_t>(bh) * sh.n_q + row] * kLog2e : INFINITY;
-        const float Dr = row_ok ? Drow[static_cast<size_t>(bh) * sh.n_q + row] : 0.f;
+        const float nl =
+            row_ok ? -lse[static_cast<size_t>(bh) * sh.n_q + row] * kLog2e : -INFINITY;
+        const float nd = row_ok ? -Drow[static_cast<size_t>(bh) * sh.n_q + row] : 0.f;
         const int lim = sh.causal ? row + (sh.n_kv - sh.n_q) : sh.n_kv - 1; // last visible key
         const int klim = min(lim, sh.n_kv - 1);
+        const float2 c2 = make_float2(sh.c, sh.c), l2 = make_float2(nl, nl),
+                     d2 = make_float2(nd, nd);
         bool ok = true;
-        for (int t = 0; t < nsteps; ++t) {
-            if (!mbar_wait_warp(b_mma, t & 1, abort_flag, err)) {
+        for (int hs = 0; hs < nhalf; ++hs) {
+            const int t = hs >> 1, e = hs & 1;
+            if (!mbar_wait_warp(b_mma(e), t & 1, abort_flag, err)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int kl = klim - t * BT; // last visible key within this block
-#pragma unroll 1
-            for (int ch = 0; ch < BT / 32; ++ch) {
+            const uint32_t tS = tmem + lane_off + C::S_COL(e);
+            const uint32_t tP = tmem + lane_off + C::DP_COL(e);
+            const int kl = klim - hs * HS; // last visible key within this half-step
+            const bool mask = kl < HS - 1;
+#pragma unroll
+            for (int ch = 0; ch < HS / 32; ++ch) {
                 uint32_t us[32], ud[32];
                 tmem_ld32(tS + ch * 32, us);
                 tmem_ld32(tP + ch * 32, ud);
                 uint32_t dw[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float dv[2];
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int k = ch * 32 + 2 * e + h2;
-                        const float p =
-                            (k <= kl) ? ex2(fmaf(__uint_as_float(us[2 * e + h2]), sh.c, -lse2))
-                                      : 0.f;
-                        dv[h2] = p * (__uint_as_float(ud[2 * e + h2]) - Dr);
+                for (int e2 = 0; e2 < 16; ++e2) {
+                    const int k = ch * 32 + 2 * e2;
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(us[2 * e2]), __uint_as_float(us[2 * e2 + 1])),
+                        c2, l2);
+                    float2 p = make_float2(ex2(x.x), ex2(x.y));
+                    if (mask) {
+                        if (k > kl)
+                            p.x = 0.f;
+                        if (k + 1 > kl)
+                            p.y = 0.f;
                     }
-                    dw[e] = pack2<BF16>(dv[0], dv[1]);
+                    const float2 g = __fadd2_rn(
+                        make_float2(__uint_as_float(ud[2 * e2]), __uint_as_float(ud[2 * e2 + 1])),
+                        d2);
+                    const float2 ds = __fmul2_rn(p, g);
+                    dw[e2] = pack2<BF16>(ds.x, ds.y);
                 }
                 tmem_st16(tP + ch * 16, dw);
             }
@@ -556,9 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(b_pready);
+                mbar_arrive(b_pready(e));
         }
-        if (ok && nsteps > 0)
+        if (ok && nhalf > 0)
             ok = mbar_wait_warp(b_done, 0, abort_flag, err);
         tc_fence_after();
         const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row) * D;
@@ -570,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float o[32];
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
-                    o[k] = (ok && nsteps > 0) ? __uint_as_float(u[k]) * sh.scale : 0.f;
+                    o[k] = (ok && nhalf > 0) ? __uint_as_float(u[k]) * sh.scale : 0.f;
                 store32<OUT>(dQ, orow + ch * 32, o);
             }
         }
