@@ -386,11 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i_min = key - off - qb * BT; // first visible query (causal)
             const bool mask = !key_ok || (sh.causal && i_min > i0);
             const float2 c2 = make_float2(sh.c, sh.c);
+            static_assert(HS == 64, "two 32-column chunks per half-step");
+            uint32_t us0[32], ud0[32], us1[32], ud1[32];
+            tmem_ld32x4(tS, us0, tP, ud0, tS + 32, us1, tP + 32, ud1);
 #pragma unroll
-            for (int ch = 0; ch < HS / 32; ++ch) {
-                uint32_t us[32], ud[32];
-                tmem_ld32(tS + ch * 32, us);
-                tmem_ld32(tP + ch * 32, ud);
+            for (int ch = 0; ch < 2; ++ch) {
+                const uint32_t(&us)[32] = ch ? us1 : us0;
+                const uint32_t(&ud)[32] = ch ? ud1 : ud0;
                 uint32_t pw[16], dw[16];
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
@@ -623,11 +625,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tP = tmem + lane_off + C::DP_COL(e);
             const int kl = klim - hs * HS; // last visible key within this half-step
             const bool mask = kl < HS - 1;
+            uint32_t us0[32], ud0[32], us1[32], ud1[32];
+            tmem_ld32x4(tS, us0, tP, ud0, tS + 32, us1, tP + 32, ud1);
 #pragma unroll
-            for (int ch = 0; ch < HS / 32; ++ch) {
-                uint32_t us[32], ud[32];
-                tmem_ld32(tS + ch * 32, us);
-                tmem_ld32(tP + ch * 32, ud);
+            for (int ch = 0; ch < 2; ++ch) {
+                const uint32_t(&us)[32] = ch ? us1 : us0;
+                const uint32_t(&ud)[32] = ch ? ud1 : ud0;
                 uint32_t dw[16];
 #pragma unroll
                 for (int e2 = 0; e2 < 16; ++e2) {

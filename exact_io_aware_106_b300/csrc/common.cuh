@@ -316,6 +316,31 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
                  : "r"(taddr)
                  : "memory");
 }
+// Four loads of 32 consecutive 32-bit columns each (thread i reads TMEM
+// lane base + i) under one completion wait, so their latencies overlap.
+__device__ __forceinline__ void tmem_ld32x4(uint32_t a0, uint32_t (&r0)[32], uint32_t a1,
+                                            uint32_t (&r1)[32], uint32_t a2,
+                                            uint32_t (&r2)[32], uint32_t a3,
+                                            uint32_t (&r3)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, "
+        "%19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, "
+        "%49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, "
+        "%81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, "
+        "%111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, "
+        "%125, %126, %127}, [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : ATTN_R32_OUT(r0), ATTN_R32_OUT(r1), ATTN_R32_OUT(r2), ATTN_R32_OUT(r3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+        : "memory");
+}
 // Thread i writes 32 consecutive columns of TMEM lane (lane base + i).
 // Completion is awaited separately with tmem_st_wait().
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
