@@ -251,6 +251,21 @@ def run_ours(args, rank, world):
         if ev:
             ev[3].record(stream)
 
+    # first call of each part, host wall time with synchronisation on both
+    # sides: lazy module load, tensor-map encoding and the run itself
+    first = {}
+    torch.cuda.synchronize(dev)
+    if do_pre:
+        t0 = time.perf_counter()
+        attn.prefill(Q, K, V, True, O=O, lse=lse, stream=stream)
+        torch.cuda.synchronize(dev)
+        first["prefill_ms"] = round((time.perf_counter() - t0) * 1e3, 3)
+    if do_dec:
+        t0 = time.perf_counter()
+        attn.decode(dd["q"], dd["Kc"], dd["Vc"], dd["block_table"], dd["seq_lens"],
+                    max_seq_len=DECODE.len_hi, O=Od, lse=lsed, workspace=ws, stream=stream)
+        torch.cuda.synchronize(dev)
+        first["decode_ms"] = round((time.perf_counter() - t0) * 1e3, 3)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -273,9 +288,11 @@ def run_ours(args, rank, world):
     n_launch = launches[0]
     if attn.last_error(stream) != attn.OK:
         raise RuntimeError("device error during the timed steps")
-    t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    per_pre = [e[0].elapsed_time(e[1]) for e in evs]
+    per_dec = [e[2].elapsed_time(e[3]) for e in evs]
+    t_pre = sum(per_pre) / 1e3
     t_app = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
-    t_dec = sum(e[2].elapsed_time(e[3]) for e in evs) / 1e3
+    t_dec = sum(per_dec) / 1e3
     t_step = sum(e[0].elapsed_time(e[3]) for e in evs) / 1e3
 
     F = prefill_flops(PREFILL)
@@ -294,6 +311,9 @@ def run_ours(args, rank, world):
         "t_app": t_app / nst,
         "roof_step": roof_step, "roof_pre": roof_pre, "roof_dec": roof_dec, "F": F, "Bd": Bd,
         "launches": n_launch, "clocks": clk.summary(), "wall": wall, "peaks": pk,
+        "first_call": first,
+        "pre_med_best": (statistics.median(per_pre), min(per_pre)),
+        "dec_med_best": (statistics.median(per_dec), min(per_dec)),
     }
 
     res["traffic"] = measured_traffic("prefill_sm103.cu", PREFILL.name)
@@ -369,9 +389,19 @@ def run_ours(args, rank, world):
 
 # ------------------------------------------------- single named workloads
 
+_FIRST_CALL = {}
+
+
 def _time_kernel(fn, stream, warmup, steps, flush):
     """Median and best device time of fn() over `steps` runs, L2 flushed
-    (a 256 MiB write) before every run, outside the timed events."""
+    (a 256 MiB write) before every run, outside the timed events.  The
+    first call's host wall time (synchronised on both sides: lazy module
+    load, tensor-map encoding and the run) is left in _FIRST_CALL["ms"]."""
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    fn()
+    torch.cuda.synchronize()
+    _FIRST_CALL["ms"] = round((time.perf_counter() - t0) * 1e3, 3)
     for _ in range(warmup):
         flush.zero_()
         fn()
@@ -410,6 +440,11 @@ def workload_lines(name: str, steps: int, warmup: int):
         jobs.append(("decode-tokens", (W.DECODE_TOKENS_WORKLOADS[name][0], base, name)))
     elif name in W.DECODE_WORKLOADS:
         jobs.append(("decode", W.DECODE_WORKLOADS[name]))
+    elif name.startswith(("sweep-decode-G", "sweep-prefill-G")):
+        # one cell of the G x d sweep, e.g. sweep-decode-G16-d64-e4m3
+        kind, g_, d_, kv = name.split("-")[1:]
+        G, d = int(g_[1:]), int(d_[1:])
+        jobs.append((kind, (W.sweep_decode if kind == "decode" else W.sweep_prefill)(G, d, kv)))
     elif name == "sweep":
         for kv in ("bf16", "e4m3"):
             for G in (1, 4, 8, 16):
@@ -438,6 +473,7 @@ def workload_lines(name: str, steps: int, warmup: int):
                 Bp = prefill_bytes(spec)
                 roof = max(F / (peak * 1e12), Bp / (pk["hbm_gbs"] * 1e9))
                 line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            first_call_ms=_FIRST_CALL.get("ms"),
                             tflops=round(F / med / 1e12, 2),
                             pct_roofline=round(100 * roof / med, 2),
                             peak_tflops=peak,
@@ -460,6 +496,7 @@ def workload_lines(name: str, steps: int, warmup: int):
                 F = 2.5 * prefill_flops(spec)
                 roof = F / (pk["bf16_tflops"] * 1e12)
                 line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            first_call_ms=_FIRST_CALL.get("ms"),
                             tflops=round(F / med / 1e12, 2),
                             pct_roofline=round(100 * roof / med, 2),
                             peak_tflops=pk["bf16_tflops"], peak_kind="measured burst bf16",
@@ -488,6 +525,7 @@ def workload_lines(name: str, steps: int, warmup: int):
                 roof = max(T * decode_flops(base, lens) / (pk["bf16_tflops"] * 1e12),
                            Bd / (pk["hbm_gbs"] * 1e9))
                 line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            first_call_ms=_FIRST_CALL.get("ms"),
                             gbs=round(Bd / med / 1e9, 1), bytes=Bd, new_tokens=T,
                             pct_roofline=round(100 * roof / med, 2),
                             peak_gbs=pk["hbm_gbs"], peak_kind="measured HBM copy")
@@ -511,6 +549,7 @@ def workload_lines(name: str, steps: int, warmup: int):
                       + 2 * spec.Hkv * spec.d * e * float(sum(int(L) for L in lens)))
                 roof = max(F / (pk["bf16_tflops"] * 1e12), Bp / (pk["hbm_gbs"] * 1e9))
                 line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            first_call_ms=_FIRST_CALL.get("ms"),
                             tflops=round(F / med / 1e12, 2),
                             pct_roofline=round(100 * roof / med, 2),
                             peak_tflops=pk["bf16_tflops"], peak_kind="measured burst bf16")
@@ -533,6 +572,7 @@ def workload_lines(name: str, steps: int, warmup: int):
                 roof = max(decode_flops(spec, lens) / (pk["bf16_tflops"] * 1e12),
                            Bd / (pk["hbm_gbs"] * 1e9))
                 line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
+                            first_call_ms=_FIRST_CALL.get("ms"),
                             gbs=round(Bd / med / 1e9, 1), bytes=Bd,
                             pct_roofline=round(100 * roof / med, 2),
                             peak_gbs=pk["hbm_gbs"], peak_kind="measured HBM copy")
@@ -645,7 +685,9 @@ def main():
                     help="override the number of decode sequences (profiling case)")
     ap.add_argument("--workload", default="",
                     help="time one named workload alone (single-head, gqa-4k, long-23k, "
-                         "long-32k, paged-decode) or every cell of 'sweep'; one line each")
+                         "long-32k, paged-decode, paged-prefill, spec-decode-4, "
+                         "bwd-<prefill workload>, one sweep cell such as "
+                         "sweep-decode-G16-d64-e4m3) or every cell of 'sweep'; one line each")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -705,7 +747,10 @@ def main():
             line["prefill"] = {
                 "tflops": round(pre_tflops, 2), "ms": round(res["t_pre"] * 1e3, 4),
                 "pct_roofline": round(100 * res["roof_pre"] / res["t_pre"], 2),
-                "pct_of_burst_peak": round(100 * pre_tflops / pk["bf16_tflops"], 2)}
+                "pct_of_burst_peak": round(100 * pre_tflops / pk["bf16_tflops"], 2),
+                "median_ms": round(res["pre_med_best"][0], 4),
+                "best_ms": round(res["pre_med_best"][1], 4),
+                "first_call_ms": res["first_call"].get("prefill_ms")}
             line["roofline"] = {
                 "bound": "tensor", "kernel": "prefill_kernel<128,bf16,bf16>",
                 "achieved": round(pre_tflops, 2), "peak": pk["bf16_tflops_sustained"],
@@ -717,7 +762,10 @@ def main():
             line["decode"] = {
                 "gbs": round(dec_gbs, 1), "ms": round(res["t_dec"] * 1e3, 4),
                 "pct_roofline": round(100 * res["roof_dec"] / res["t_dec"], 2),
-                "frac_of_8tbs_spec": round(dec_gbs / 8000.0, 4), "bytes": res["Bd"]}
+                "frac_of_8tbs_spec": round(dec_gbs / 8000.0, 4), "bytes": res["Bd"],
+                "median_ms": round(res["dec_med_best"][0], 4),
+                "best_ms": round(res["dec_med_best"][1], 4),
+                "first_call_ms": res["first_call"].get("decode_ms")}
             line["append"] = {"ms": round(res["t_app"] * 1e3, 4)}
             dec_roof = {
                 "bound": "hbm", "kernel": "decode_mma_kernel<128,bf16> + decode_combine_kernel",
