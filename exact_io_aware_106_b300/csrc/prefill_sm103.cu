@@ -24,7 +24,7 @@
 //               on the SFU, row sum, P packed to 16-bit back into tensor
 //               memory over the consumed scores, O rescaled in tensor memory
 //               when the reference max moves, final O / l and lse.
-//   warp 10     (E4M3 inputs only) widens each V tile to f16 on chip.
+//   warps 10-11 (E4M3 inputs only) widen each V tile to f16 on chip.
 // The two tiles ping-pong: while warpgroup 0 turns S_0 into P_0, the tensor
 // core computes O_1 += P_1 V_j and S_1 for the next block, and vice versa.
 //
@@ -74,7 +74,8 @@ struct Cfg {
     static constexpr int NK = (F8 || D == 64) ? 3 : 2;      // K stages
     static constexpr int NV = D == 64 ? 3 : 2;              // V stages
     static constexpr int NVS = F8 ? 2 : 0;                  // E4M3 V staging buffers
-    static constexpr int THREADS = F8 ? 352 : 320;
+    static constexpr int NCONV = F8 ? 2 : 0;                // V widening warps
+    static constexpr int THREADS = 320 + 32 * NCONV;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NT * Q_TILE_BYTES;
     static constexpr int OFF_V = OFF_K + NK * K_BYTES;
@@ -322,12 +323,14 @@ __device__ __forceinline__ float exp_pack_store(const float (&s)[NB], float c, f
 
 // Widen one E4M3 V tile [ROWS][D] (panels of PW-byte rows, PW-byte swizzle)
 // into the f16 operand layout (panels of 64 elements = 128-byte rows,
-// 128-byte swizzle) -- the layout 16-bit V tiles arrive in by TMA.
+// 128-byte swizzle) -- the layout 16-bit V tiles arrive in by TMA.  Warp
+// `part` of `nparts` converts every nparts-th group of 32 chunks.
 template <int D, int ROWS, int PW>
-__device__ __forceinline__ void widen_v_tile(uint32_t src, uint32_t dst, int lane) {
+__device__ __forceinline__ void widen_v_tile(uint32_t src, uint32_t dst, int lane, int part,
+                                             int nparts) {
     constexpr int CPR = D / 16; // 16-byte source chunks per row
 #pragma unroll 4
-    for (int i = lane; i < ROWS * CPR; i += 32) {
+    for (int i = part * 32 + lane; i < ROWS * CPR; i += 32 * nparts) {
         const int r = i / CPR, c = i % CPR;
         const uint4 v = lds_v4(src + (c * 16 / PW) * (ROWS * PW) +
                                swz_offset<PW>(r, (c * 16 % PW) >> 4));
@@ -411,12 +414,12 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             mbar_init(b_kempty(i), 1);
         }
         for (int i = 0; i < C::NV; ++i) {
-            mbar_init(b_vfull(i), 1);
+            mbar_init(b_vfull(i), F8 ? C::NCONV : 1);
             mbar_init(b_vempty(i), 1);
         }
         for (int i = 0; i < C::NVS; ++i) {
             mbar_init(b_vsfull(i), 1);
-            mbar_init(b_vsempty(i), 1);
+            mbar_init(b_vsempty(i), C::NCONV);
         }
         for (int t = 0; t < NT; ++t) {
             mbar_init(b_sfull(t), 1);
@@ -517,7 +520,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                 }
             }
         }
-    } else if (warp == kConvWarp) {
+    } else if (warp >= kConvWarp) {
         // ================================================= V widening (E4M3)
         if constexpr (F8) {
             for (int j = 0; j < nb_max; ++j) {
@@ -527,7 +530,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                 if (j >= C::NV &&
                     !mbar_wait_warp(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
                     break;
-                widen_v_tile<D, BN, C::PW>(sVS + ss * C::VS_BYTES, sV + vs * C::V_BYTES, lane);
+                widen_v_tile<D, BN, C::PW>(sVS + ss * C::VS_BYTES, sV + vs * C::V_BYTES, lane,
+                                           warp - kConvWarp, C::NCONV);
                 fence_proxy_async_smem(); // generic writes -> tensor-core reads
                 __syncwarp();
                 if (lane == 0) {
@@ -793,7 +797,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
 // two K and two V stages fit next to the Q tile.
 //   warp 4      TMA producer (Q once, K / V rings of 2 stages)
 //   warp 5      MMA issuer (one thread)
-//   warp 6      (E4M3 inputs only) widens each V tile to f16
+//   warps 6-9   (E4M3 inputs only) widen each V tile to f16, a quarter each
 //   warps 0-3   softmax, one thread per row; the epilogue
 // Tensor memory: S_0 [0,64), S_1 [64,128), O [128, 384).  A block that moves
 // the reference max rescales O only after the previous block's P V product
@@ -818,7 +822,8 @@ struct Cfg {
     static constexpr int V_BYTES = BN * D * 2;
     static constexpr int VS_BYTES = BN * D;
     static constexpr int NVS = F8 ? 2 : 0;
-    static constexpr int THREADS = F8 ? 224 : 192;
+    static constexpr int NCONV = F8 ? 4 : 0; // V widening warps
+    static constexpr int THREADS = 192 + 32 * NCONV;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + NK * K_BYTES;
@@ -899,12 +904,12 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
             mbar_init(b_kempty(i), 1);
         }
         for (int i = 0; i < NV; ++i) {
-            mbar_init(b_vfull(i), 1);
+            mbar_init(b_vfull(i), F8 ? C::NCONV : 1);
             mbar_init(b_vempty(i), 1);
         }
         for (int i = 0; i < C::NVS; ++i) {
             mbar_init(b_vsfull(i), 1);
-            mbar_init(b_vsempty(i), 1);
+            mbar_init(b_vsempty(i), C::NCONV);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_sfull(i), 1);
@@ -991,7 +996,7 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
                 }
             }
         }
-    } else if (warp == kConvWarp) {
+    } else if (warp >= kConvWarp) {
         // ================================================= V widening (E4M3)
         if constexpr (F8) {
             for (int j = 0; j < nb; ++j) {
@@ -1001,7 +1006,7 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
                 if (j >= NV && !mbar_wait_warp(b_vempty(vs), ((j / NV) - 1) & 1, abort_flag, err))
                     break;
                 pf::widen_v_tile<D, BN, C::PW>(sVS + ss * C::VS_BYTES, sV + vs * C::V_BYTES,
-                                               lane);
+                                               lane, warp - kConvWarp, C::NCONV);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
