@@ -241,7 +241,7 @@ attn_status decode_impl(const void *q, const void *Kcache, const void *Vcache,
         return ATTN_ERR_INVALID;
     if ((d != 64 && d != 128 && d != 256) ||
         (block_size != 16 && block_size != 32 && block_size != 64) ||
-        static_cast<long long>(Hq / Hkv) * T > 16)
+        static_cast<long long>(Hq / Hkv) * T > 64)
         return ATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(num_seqs) * Hq * T > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;

@@ -12,7 +12,9 @@
 //
 // Split-KV: one CTA per (split of tps tokens, KV head hk, sequence s).  The
 // G <= 16 query heads of the group are the rows of one 16-row warp-level
-// MMA tile (mma.sync m16n8k16, rows G..15 zero), so a 16-token unit costs
+// MMA tile (mma.sync m16n8k16, rows G..15 zero; with several new tokens per
+// sequence the G x n_new rows fill as many 16-row tiles as needed, one CTA
+// each), so a 16-token unit costs
 // D/8 MMAs for S = q K^T and D/8 (2 D/8 with the P residual) for u += P V
 // instead of ~2 G 16 D scalar FMAs: the consumer warps stay far ahead of
 // HBM.  A producer warp streams 16-token units of K and V by TMA into a
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
                       const int32_t *__restrict__ block_table,
                       const int32_t *__restrict__ seq_lens, const float *__restrict__ k_scale,
                       const float *__restrict__ v_scale, float2 *__restrict__ ws_ml,
-                      float *__restrict__ ws_u, int Hq, int G, int T, int block_size,
+                      float *__restrict__ ws_u, int Hq, int G, int T, int nrt, int block_size,
                       int max_blocks,
                       int num_blocks, int max_seq_len, int tps, int max_splits, float c,
                       unsigned *err) {
@@ -207,7 +209,10 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     __shared__ int s_abort;
     __shared__ int s_amax; // max |q| of the group as float bits (E4M3 caches)
 
-    const int split = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
+    // x = (split, row tile): the nrt row tiles of one split are adjacent, so
+    // the K/V they all stream is read from DRAM about once and from L2 after
+    const int split = blockIdx.x / nrt, rt = blockIdx.x % nrt;
+    const int hk = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int len = seq_lens[s];
     const bool len_ok = len >= (T > 1 ? T : 0) && len <= max_seq_len &&
@@ -223,11 +228,13 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     const int t1 = min(len, t0 + tps);
     const int nunits = (t1 - t0 + kUnit - 1) / kUnit;
     const int head0 = hk * G;
-    // rows of the MMA tile: r = g * T + i for head head0 + g and new token i
-    // (q [num_seqs, Hq, T, d], so a group's rows are contiguous)
-    const int R = G * T;
+    // rows of the group: r = g * T + i for head head0 + g and new token i
+    // (q [num_seqs, Hq, T, d], so a group's rows are contiguous); this CTA
+    // takes the 16-row tile [row0, row0 + 16) of them
+    const int row0 = 16 * rt;
+    const int R = min(16, G * T - row0);
     const uint16_t *qg = static_cast<const uint16_t *>(q_) +
-                         (static_cast<size_t>(s) * Hq + head0) * T * D;
+                         ((static_cast<size_t>(s) * Hq + head0) * T + row0) * D;
 
     if (threadIdx.x == 0) {
         s_flag = 0;
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
         if (threadIdx.x == 0)
             atomicOr(err, DERR_INDEX);
         for (int r = threadIdx.x; r < R; r += kThreads)
-            ws_ml[((static_cast<size_t>(s) * Hq + head0) * T + r) * max_splits + split] =
+            ws_ml[((static_cast<size_t>(s) * Hq + head0) * T + row0 + r) * max_splits + split] =
                 make_float2(0.f, -1.f); // l < 0 marks an unusable partial
         return;
     }
@@ -423,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
         }
         if (T > 1 && t0 + u * kUnit + kUnit - 1 > len - T) {
             // new token i sees cached token p iff p <= len - T + i (bottom-right)
-            const int lim0 = len - T + (g % T), lim1 = len - T + ((g + 8) % T);
+            const int lim0 = len - T + ((row0 + g) % T), lim1 = len - T + ((row0 + g + 8) % T);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int p = t0 + u * kUnit + (i >> 1) * 8 + 2 * t + (i & 1);
@@ -587,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
             U += sc * mrg_u[(w * 16 + r) * D + e];
         }
         const size_t o_idx =
-            ((static_cast<size_t>(s) * Hq + head0) * T + r) * max_splits + split;
+            ((static_cast<size_t>(s) * Hq + head0) * T + row0 + r) * max_splits + split;
         ws_u[o_idx * D + e] = U * vsc;
         if (e == 0)
             ws_ml[o_idx] = bad ? make_float2(0.f, -1.f) : make_float2(M, Lsum);
@@ -650,11 +657,12 @@ static cudaError_t launch_mma(const DecodeArgs &a, float2 *ws_ml, float *ws_u, i
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
     if (e != cudaSuccess)
         return e;
-    dim3 grid(max_splits, a.Hkv, a.num_seqs);
+    const int nrt = (a.Hq / a.Hkv * a.T + 15) / 16; // 16-row tiles per KV head
+    dim3 grid(max_splits * nrt, a.Hkv, a.num_seqs);
     kern<<<grid, dm::kThreads, Ly::SMEM, st>>>(
         mk, mv, a.q, a.block_table, a.seq_lens, a.k_scale, a.v_scale, ws_ml, ws_u, a.Hq,
-        a.Hq / a.Hkv, a.T, a.block_size, a.max_blocks, a.num_blocks, a.max_seq_len, tps, max_splits,
-        a.scale * 1.4426950408889634f, a.err);
+        a.Hq / a.Hkv, a.T, nrt, a.block_size, a.max_blocks, a.num_blocks, a.max_seq_len, tps,
+        max_splits, a.scale * 1.4426950408889634f, a.err);
     return cudaGetLastError();
 }
 
@@ -663,7 +671,8 @@ static cudaError_t launch_mma(const DecodeArgs &a, float2 *ws_ml, float *ws_u, i
 // CTAs -- longer splits amortise each CTA's set-up and merge.
 static int choose_tps(const DecodeArgs &a, int resident_per_sm) {
     int tps = decode_tokens_per_split(a.max_seq_len);
-    const long long pairs = static_cast<long long>(a.num_seqs) * a.Hkv;
+    const long long pairs = static_cast<long long>(a.num_seqs) * a.Hkv *
+                            ((a.Hq / a.Hkv * a.T + 15) / 16); // CTAs per split
     const long long slots = static_cast<long long>(sm_count()) * resident_per_sm;
     while (tps < 2048) {
         const long long splits = (a.max_seq_len + 2LL * tps - 1) / (2LL * tps);

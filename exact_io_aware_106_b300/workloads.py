@@ -95,6 +95,8 @@ PAGED_PREFILL_WORKLOADS = {
 # sequence (e.g. speculative drafts), G * 4 = 16 query rows per KV head
 DECODE_TOKENS_WORKLOADS = {
     "spec-decode-4": (4, None),
+    # 8 new tokens: G * 8 = 32 query rows per KV head, two 16-row tiles
+    "spec-decode-8": (8, None),
 }
 
 DECODE_WORKLOADS = {

@@ -175,8 +175,10 @@ ATTN_API size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d,
  *   O        [num_seqs, Hq, d] out_dtype;  lse [num_seqs, Hq] fp32 or NULL
  *   workspace: >= attn_decode_workspace_bytes(...) bytes, 256-byte aligned;
  *            its contents on entry do not matter and are overwritten.
- * block_size in {16, 32, 64}; d in {64, 128, 256}; Hq / Hkv <= 16; q, the
- * caches and the workspace 16-byte aligned (the workspace 256-byte).
+ * block_size in {16, 32, 64}; d in {64, 128, 256}; Hq / Hkv <= 64 (each 16
+ * query heads of a group are one CTA per split; the K/V of a split is read
+ * from DRAM once and by the other 16-row tiles from L2); q, the caches and
+ * the workspace 16-byte aligned (the workspace 256-byte).
  * A sequence of length 0 yields O = 0 and lse = -inf.  Two kernel launches
  * (split kernel, then combine).  The workspace must not be shared by
  * overlapping calls. */
@@ -197,7 +199,7 @@ ATTN_API attn_status attn_decode(const void *q, const void *Kcache, const void *
  * sees cached token p iff p <= seq_lens[s] - n_new + i (bottom-right).
  *   q   [num_seqs, Hq, n_new, d];  O [num_seqs, Hq, n_new, d];
  *   lse [num_seqs, Hq, n_new] or NULL
- * Everything else as attn_decode, with (Hq / Hkv) * n_new <= 16, every
+ * Everything else as attn_decode, with (Hq / Hkv) * n_new <= 64, every
  * seq_lens[s] >= n_new, and a workspace of at least
  * attn_decode_workspace_bytes(num_seqs * n_new, Hq, d, max_seq_len) bytes.
  * n_new = 1 is attn_decode.  Two kernel launches. */

@@ -108,7 +108,7 @@ def test_decode_host_validation(L):
     assert _decode(L, kvd=3, ks=None) == attn.ERR_INVALID              # fp8 without scales
     assert _decode(L, d=80) == attn.ERR_UNSUPPORTED
     assert _decode(L, bs=8, msl=64) == attn.ERR_UNSUPPORTED
-    assert _decode(L, Hq=34, Hkv=2) == attn.ERR_UNSUPPORTED            # G > 16
+    assert _decode(L, Hq=130, Hkv=2) == attn.ERR_UNSUPPORTED           # G > 64
     assert _decode(L, kvd=0) == attn.ERR_UNSUPPORTED                   # f16 cache, bf16 query
     assert _decode(L, ws=ctypes.c_void_p((1 << 20) + 16)) == attn.ERR_INVALID
 
@@ -121,7 +121,7 @@ def test_decode_tokens_host_validation(L):
                                     a["Hq"], a["Hkv"], a["d"], 16, 8, 32, a["msl"], 0.1, 1, 1, 1,
                                     None, None, FAKE, a["wsb"], None)
     assert call(T=0) == attn.ERR_INVALID
-    assert call(T=5) == attn.ERR_UNSUPPORTED                           # G * T = 20 > 16
+    assert call(T=17) == attn.ERR_UNSUPPORTED                          # G * T = 68 > 64
     assert call(T=4, msl=3) == attn.ERR_INVALID                        # shorter than its new tokens
     assert call(wsb=1024) == attn.ERR_INVALID                          # workspace too small
     assert L.attn_last_launch_count() == 0

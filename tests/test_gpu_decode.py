@@ -25,6 +25,9 @@ CASES = [
     (4, 8, 8, 128, 16, [5, 4096, 300, 1], "f16"),
     (2, 16, 8, 256, 16, [70, 9], "f16"),
     (6, 6, 2, 128, 16, [1, 2, 3, 250, 251, 1300], "bf16"),   # G = 3
+    (3, 32, 1, 128, 16, [1, 777, 3000], "bf16"),             # MQA, G = 32: two row tiles
+    (2, 40, 1, 64, 32, [100, 2500], "f16"),                  # G = 40: three tiles, last ragged
+    (2, 64, 1, 256, 16, [17, 1200], "bf16"),                 # G = 64: four tiles
 ]
 
 

@@ -19,6 +19,9 @@ CASES = [
     (3, 4, 4, 16, 64, [16, 100, 999], 32, "f16"),
     (2, 16, 2, 2, 256, [2, 5000], 16, "bf16"),
     (3, 6, 2, 5, 128, [5, 64, 77], 64, "bf16"),       # G = 3, T = 5: 15 rows
+    (3, 16, 2, 4, 128, [4, 333, 4000], 16, "bf16"),   # G = 8, T = 4: two 16-row tiles
+    (2, 4, 1, 5, 256, [5, 700], 16, "bf16"),          # G = 4, T = 5: 20 rows, ragged tile
+    (2, 16, 1, 4, 64, [4, 1000], 32, "f16"),          # G = 16, T = 4: four tiles
 ]
 
 
@@ -44,8 +47,9 @@ def test_decode_tokens_matches_paged_oracle(case):
         assert_lse(lse, lse_ref)
 
 
-def test_decode_tokens_e4m3_cache():
-    S, Hq, Hkv, T, d, lens, bs = 3, 8, 2, 3, 128, [3, 200, 1500], 16
+@pytest.mark.parametrize("Hq", [8, 16], ids=["12rows", "24rows"])
+def test_decode_tokens_e4m3_cache(Hq):
+    S, Hkv, T, d, lens, bs = 3, 2, 3, 128, [3, 200, 1500], 16
     spec = W.PagedPrefillSpec(S, Hq, Hkv, T, d, 1, max(lens), bs, True, "bf16", "f32")
     t = W.make_paged_prefill(spec, seed=8, lens=lens)
     kq, ks = W.quantize_e4m3_per_head(t["Kc"], 1)
