@@ -432,6 +432,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
     return r;
 }
 
+// Per-warpgroup register budget (all four warps of the warpgroup execute
+// it): dec gives registers back to the CTA's pool, inc waits until the pool
+// can grant the new count.  The counts must add up to the launch's
+// allocation or inc never returns.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------- numerics
 
 __device__ __forceinline__ float ex2(float x) {

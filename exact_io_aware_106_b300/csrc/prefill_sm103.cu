@@ -61,6 +61,18 @@ constexpr int kMmaWarp = 9;
 constexpr int kConvWarp = 10;
 constexpr int kSplitKeys = 512; // rows seeing fewer keys carry the P residual
 constexpr float kRescaleThreshold = 8.0f;
+// Registers per thread: 384 threads launch with 168 each (the most that three
+// warps per SM sub-partition allow); the producer / MMA / converter
+// warpgroup (warps 8-11) hands most of its share to the two softmax
+// warpgroups, whose 128-score rows would otherwise spill:
+// 256 x 208 + 128 x 88 = 384 x 168, and per SM sub-partition (warps k, k+4,
+// k+8) 208 + 208 + 88 = 3 x 168.
+constexpr int kThreadsAll = 384;
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsOther = 88;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther == kThreadsAll * kLaunchRegs,
+              "register split must add up to the launch allocation");
 
 template <int D, bool F8>
 struct Cfg {
@@ -75,7 +87,7 @@ struct Cfg {
     static constexpr int NV = D == 64 ? 3 : 2;              // V stages
     static constexpr int NVS = F8 ? 2 : 0;                  // E4M3 V staging buffers
     static constexpr int NCONV = F8 ? 2 : 0;                // V widening warps
-    static constexpr int THREADS = 320 + 32 * NCONV;
+    static constexpr int THREADS = kThreadsAll; // warps 10-11 idle for 16-bit inputs
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NT * Q_TILE_BYTES;
     static constexpr int OFF_V = OFF_K + NK * K_BYTES;
@@ -442,210 +454,225 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    if (warp == kProducerWarp && PAGED) {
-        // ================================================= paged producer
-        if (lane == 0) {
-            int ntiles = 0;
-            for (int t = 0; t < NT; ++t)
-                ntiles += nb[t] > 0;
-            mbar_arrive_expect_tx(b_qfull, ntiles * C::Q_TILE_BYTES);
-            for (int t = 0; t < NT; ++t)
-                if (nb[t] > 0)
-                    for (int p = 0; p < C::QK_PANELS; ++p)
-                        tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q, b_qfull,
-                                    p * 64, q0 + t * BM, bh);
-        }
-        paged_kv_producer<D, BN, C::NK, C::NV>(pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb_max, &tm_k,
-                                               &tm_v, sK, sV, b_kfull(0), b_kempty(0),
-                                               b_vfull(0), b_vempty(0), abort_flag, err, lane);
-        if (lane == 0 && *abort_flag)
-            mbar_wait_drain(b_qfull, 0);
-    } else if (warp == kProducerWarp) {
-        // ================================================= TMA producer
-        if (lane == 0) {
-            constexpr int XP = C::PW / C::EB; // elements per Q/K panel row
-            int ntiles = 0;
-            for (int t = 0; t < NT; ++t)
-                ntiles += nb[t] > 0;
-            mbar_arrive_expect_tx(b_qfull, ntiles * C::Q_TILE_BYTES);
-            for (int t = 0; t < NT; ++t)
-                if (nb[t] > 0)
-                    for (int p = 0; p < C::QK_PANELS; ++p)
-                        tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q, b_qfull,
-                                    p * XP, q0 + t * BM, bh);
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < nb_max; ++j) {
-                const int ks = j % C::NK;
-                if (j >= C::NK &&
-                    !mbar_wait(b_kempty(ks), ((j / C::NK) - 1) & 1, abort_flag, err))
-                    break;
-                mbar_arrive_expect_tx(b_kfull(ks), C::K_BYTES);
-                for (int p = 0; p < C::QK_PANELS; ++p)
-                    tma_load_3d(sK + ks * C::K_BYTES + p * BN * C::PW, &tm_k, b_kfull(ks),
-                                p * XP, j * BN, bkv);
-                k_issued = j + 1;
-                if constexpr (F8) {
-                    // E4M3 V into staging; the converter warp fills the V stage
-                    const int vs = j % C::NVS;
-                    if (j >= C::NVS &&
-                        !mbar_wait(b_vsempty(vs), ((j / C::NVS) - 1) & 1, abort_flag, err))
-                        break;
-                    mbar_arrive_expect_tx(b_vsfull(vs), C::VS_BYTES);
-                    for (int p = 0; p < C::QK_PANELS; ++p)
-                        tma_load_3d(sVS + vs * C::VS_BYTES + p * BN * C::PW, &tm_v,
-                                    b_vsfull(vs), p * XP, j * BN, bkv);
-                } else {
-                    const int vs = j % C::NV;
-                    if (j >= C::NV &&
-                        !mbar_wait(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
-                        break;
-                    mbar_arrive_expect_tx(b_vfull(vs), C::V_BYTES);
-                    for (int p = 0; p < D / 64; ++p)
-                        tma_load_3d(sV + vs * C::V_BYTES + p * BN * 128, &tm_v, b_vfull(vs),
-                                    p * 64, j * BN, bkv);
-                }
-                v_issued = j + 1;
+    // the roles of warps 8-11 run with few registers, the softmax
+    // warpgroups with many; each side finishes on its own (no code is shared
+    // across the two register budgets)
+    if (warp >= kProducerWarp) {
+        setmaxnreg_dec<kRegsOther>();
+        if (warp == kProducerWarp && PAGED) {
+            // ================================================= paged producer
+            if (lane == 0) {
+                int ntiles = 0;
+                for (int t = 0; t < NT; ++t)
+                    ntiles += nb[t] > 0;
+                mbar_arrive_expect_tx(b_qfull, ntiles * C::Q_TILE_BYTES);
+                for (int t = 0; t < NT; ++t)
+                    if (nb[t] > 0)
+                        for (int p = 0; p < C::QK_PANELS; ++p)
+                            tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q, b_qfull,
+                                        p * 64, q0 + t * BM, bh);
             }
-            if (*abort_flag) { // let in-flight copies land before the CTA exits
+            paged_kv_producer<D, BN, C::NK, C::NV>(pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb_max, &tm_k,
+                                                   &tm_v, sK, sV, b_kfull(0), b_kempty(0),
+                                                   b_vfull(0), b_vempty(0), abort_flag, err, lane);
+            if (lane == 0 && *abort_flag)
                 mbar_wait_drain(b_qfull, 0);
-                for (int u = max(0, k_issued - C::NK); u < k_issued; ++u)
-                    mbar_wait_drain(b_kfull(u % C::NK), (u / C::NK) & 1);
-                if constexpr (F8) {
-                    for (int u = max(0, v_issued - C::NVS); u < v_issued; ++u)
-                        mbar_wait_drain(b_vsfull(u % C::NVS), (u / C::NVS) & 1);
-                } else {
-                    for (int u = max(0, v_issued - C::NV); u < v_issued; ++u)
-                        mbar_wait_drain(b_vfull(u % C::NV), (u / C::NV) & 1);
+        } else if (warp == kProducerWarp) {
+            // ================================================= TMA producer
+            if (lane == 0) {
+                constexpr int XP = C::PW / C::EB; // elements per Q/K panel row
+                int ntiles = 0;
+                for (int t = 0; t < NT; ++t)
+                    ntiles += nb[t] > 0;
+                mbar_arrive_expect_tx(b_qfull, ntiles * C::Q_TILE_BYTES);
+                for (int t = 0; t < NT; ++t)
+                    if (nb[t] > 0)
+                        for (int p = 0; p < C::QK_PANELS; ++p)
+                            tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q, b_qfull,
+                                        p * XP, q0 + t * BM, bh);
+                int k_issued = 0, v_issued = 0;
+                for (int j = 0; j < nb_max; ++j) {
+                    const int ks = j % C::NK;
+                    if (j >= C::NK &&
+                        !mbar_wait(b_kempty(ks), ((j / C::NK) - 1) & 1, abort_flag, err))
+                        break;
+                    mbar_arrive_expect_tx(b_kfull(ks), C::K_BYTES);
+                    for (int p = 0; p < C::QK_PANELS; ++p)
+                        tma_load_3d(sK + ks * C::K_BYTES + p * BN * C::PW, &tm_k, b_kfull(ks),
+                                    p * XP, j * BN, bkv);
+                    k_issued = j + 1;
+                    if constexpr (F8) {
+                        // E4M3 V into staging; the converter warp fills the V stage
+                        const int vs = j % C::NVS;
+                        if (j >= C::NVS &&
+                            !mbar_wait(b_vsempty(vs), ((j / C::NVS) - 1) & 1, abort_flag, err))
+                            break;
+                        mbar_arrive_expect_tx(b_vsfull(vs), C::VS_BYTES);
+                        for (int p = 0; p < C::QK_PANELS; ++p)
+                            tma_load_3d(sVS + vs * C::VS_BYTES + p * BN * C::PW, &tm_v,
+                                        b_vsfull(vs), p * XP, j * BN, bkv);
+                    } else {
+                        const int vs = j % C::NV;
+                        if (j >= C::NV &&
+                            !mbar_wait(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
+                            break;
+                        mbar_arrive_expect_tx(b_vfull(vs), C::V_BYTES);
+                        for (int p = 0; p < D / 64; ++p)
+                            tma_load_3d(sV + vs * C::V_BYTES + p * BN * 128, &tm_v, b_vfull(vs),
+                                        p * 64, j * BN, bkv);
+                    }
+                    v_issued = j + 1;
+                }
+                if (*abort_flag) { // let in-flight copies land before the CTA exits
+                    mbar_wait_drain(b_qfull, 0);
+                    for (int u = max(0, k_issued - C::NK); u < k_issued; ++u)
+                        mbar_wait_drain(b_kfull(u % C::NK), (u / C::NK) & 1);
+                    if constexpr (F8) {
+                        for (int u = max(0, v_issued - C::NVS); u < v_issued; ++u)
+                            mbar_wait_drain(b_vsfull(u % C::NVS), (u / C::NVS) & 1);
+                    } else {
+                        for (int u = max(0, v_issued - C::NV); u < v_issued; ++u)
+                            mbar_wait_drain(b_vfull(u % C::NV), (u / C::NV) & 1);
+                    }
                 }
             }
-        }
-    } else if (warp >= kConvWarp) {
-        // ================================================= V widening (E4M3)
-        if constexpr (F8) {
-            for (int j = 0; j < nb_max; ++j) {
-                const int ss = j % C::NVS, vs = j % C::NV;
-                if (!mbar_wait_warp(b_vsfull(ss), (j / C::NVS) & 1, abort_flag, err))
-                    break;
-                if (j >= C::NV &&
-                    !mbar_wait_warp(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
-                    break;
-                widen_v_tile<D, BN, C::PW>(sVS + ss * C::VS_BYTES, sV + vs * C::V_BYTES, lane,
-                                           warp - kConvWarp, C::NCONV);
-                fence_proxy_async_smem(); // generic writes -> tensor-core reads
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(b_vsempty(ss));
-                    mbar_arrive(b_vfull(vs));
+        } else if (warp >= kConvWarp) {
+            // ================================================= V widening (E4M3)
+            if constexpr (F8) {
+                for (int j = 0; j < nb_max; ++j) {
+                    const int ss = j % C::NVS, vs = j % C::NV;
+                    if (!mbar_wait_warp(b_vsfull(ss), (j / C::NVS) & 1, abort_flag, err))
+                        break;
+                    if (j >= C::NV &&
+                        !mbar_wait_warp(b_vempty(vs), ((j / C::NV) - 1) & 1, abort_flag, err))
+                        break;
+                    widen_v_tile<D, BN, C::PW>(sVS + ss * C::VS_BYTES, sV + vs * C::V_BYTES, lane,
+                                               warp - kConvWarp, C::NCONV);
+                    fence_proxy_async_smem(); // generic writes -> tensor-core reads
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(b_vsempty(ss));
+                        mbar_arrive(b_vfull(vs));
+                    }
                 }
             }
-        }
-    } else if (warp == kMmaWarp) {
-        // ================================================= MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_f16(BM, BN, F8 ? false : BF16, false, false);
-            constexpr uint32_t idesc_pv = idesc_f16(BM, D, PB, false, true);
-            bool split[NT];
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-                split[t] = tile_split(sh, q0, t);
+        } else if (warp == kMmaWarp) {
+            // ================================================= MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idesc_qk = idesc_f16(BM, BN, F8 ? false : BF16, false, false);
+                constexpr uint32_t idesc_pv = idesc_f16(BM, D, PB, false, true);
+                bool split[NT];
+    #pragma unroll
+                for (int t = 0; t < NT; ++t)
+                    split[t] = tile_split(sh, q0, t);
 
-            auto issue_qk = [&](int t, int ks) {
-                const uint32_t qa = sQ + t * C::Q_TILE_BYTES;
-                const uint32_t kb = sK + ks * C::K_BYTES;
-#pragma unroll
-                for (int k = 0; k < D * C::EB / 32; ++k) { // 32-byte K steps
-                    const uint32_t byte = k * 32;
-                    const uint32_t offa = (byte / C::PW) * (BM * C::PW) + byte % C::PW;
-                    const uint32_t offb = (byte / C::PW) * (BN * C::PW) + byte % C::PW;
-                    const uint64_t ad = sdesc_kmajor(qa + offa, C::PW);
-                    const uint64_t bd = sdesc_kmajor(kb + offb, C::PW);
-                    if constexpr (F8)
-                        mma_ss_f8(tmem + C::S_COL(t), ad, bd, idesc_qk, k > 0 ? 1u : 0u);
-                    else
-                        mma_ss(tmem + C::S_COL(t), ad, bd, idesc_qk, k > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int t, int vs, bool first) {
-                const uint32_t vb = sV + vs * C::V_BYTES;
-#pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
-                    mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, bd, idesc_pv,
-                           (first && k == 0) ? 0u : 1u);
-                }
-                if (split[t]) {
-#pragma unroll
+                auto issue_qk = [&](int t, int ks) {
+                    const uint32_t qa = sQ + t * C::Q_TILE_BYTES;
+                    const uint32_t kb = sK + ks * C::K_BYTES;
+    #pragma unroll
+                    for (int k = 0; k < D * C::EB / 32; ++k) { // 32-byte K steps
+                        const uint32_t byte = k * 32;
+                        const uint32_t offa = (byte / C::PW) * (BM * C::PW) + byte % C::PW;
+                        const uint32_t offb = (byte / C::PW) * (BN * C::PW) + byte % C::PW;
+                        const uint64_t ad = sdesc_kmajor(qa + offa, C::PW);
+                        const uint64_t bd = sdesc_kmajor(kb + offb, C::PW);
+                        if constexpr (F8)
+                            mma_ss_f8(tmem + C::S_COL(t), ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+                        else
+                            mma_ss(tmem + C::S_COL(t), ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+                    }
+                };
+                auto issue_pv = [&](int t, int vs, bool first) {
+                    const uint32_t vb = sV + vs * C::V_BYTES;
+    #pragma unroll
                     for (int k = 0; k < BN / 16; ++k) {
                         const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
-                        mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + 64 + k * 8, bd, idesc_pv,
-                               1u);
+                        mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, bd, idesc_pv,
+                               (first && k == 0) ? 0u : 1u);
                     }
-                }
-            };
-
-            bool ok = mbar_wait(b_qfull, 0, abort_flag, err);
-            if (ok && nb_max > 0) {
-                ok = mbar_wait(b_kfull(0), 0, abort_flag, err);
-                if (ok) {
-                    tc_fence_after();
-                    for (int t = 0; t < NT; ++t)
-                        if (nb[t] > 0) {
-                            issue_qk(t, 0);
-                            tc_commit(b_sfull(t));
+                    if (split[t]) {
+    #pragma unroll
+                        for (int k = 0; k < BN / 16; ++k) {
+                            const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+                            mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + 64 + k * 8, bd, idesc_pv,
+                                   1u);
                         }
-                    tc_commit(b_kempty(0));
+                    }
+                };
+
+                bool ok = mbar_wait(b_qfull, 0, abort_flag, err);
+                if (ok && nb_max > 0) {
+                    ok = mbar_wait(b_kfull(0), 0, abort_flag, err);
+                    if (ok) {
+                        tc_fence_after();
+                        for (int t = 0; t < NT; ++t)
+                            if (nb[t] > 0) {
+                                issue_qk(t, 0);
+                                tc_commit(b_sfull(t));
+                            }
+                        tc_commit(b_kempty(0));
+                    }
                 }
-            }
-            for (int j = 0; ok && j < nb_max; ++j) {
-                const int vs = j % C::NV;
-                const int kn = j + 1, ks = kn % C::NK;
-                const bool need_k = kn < nb_max;
-                if (!mbar_wait(b_vfull(vs), (j / C::NV) & 1, abort_flag, err)) {
-                    ok = false;
-                    break;
-                }
-                if (need_k && !mbar_wait(b_kfull(ks), (kn / C::NK) & 1, abort_flag, err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (j < nb[0]) {
-                    if (!mbar_wait(b_pfull(0), j & 1, abort_flag, err)) {
+                for (int j = 0; ok && j < nb_max; ++j) {
+                    const int vs = j % C::NV;
+                    const int kn = j + 1, ks = kn % C::NK;
+                    const bool need_k = kn < nb_max;
+                    if (!mbar_wait(b_vfull(vs), (j / C::NV) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (need_k && !mbar_wait(b_kfull(ks), (kn / C::NK) & 1, abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_pv(0, vs, j == 0);
-                    if (kn < nb[0]) {
-                        issue_qk(0, ks);
-                        tc_commit(b_sfull(0));
+                    if (j < nb[0]) {
+                        if (!mbar_wait(b_pfull(0), j & 1, abort_flag, err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(0, vs, j == 0);
+                        if (kn < nb[0]) {
+                            issue_qk(0, ks);
+                            tc_commit(b_sfull(0));
+                        }
                     }
-                }
-                if (j < nb[1]) {
-                    if (!mbar_wait(b_pfull(1), j & 1, abort_flag, err)) {
-                        ok = false;
-                        break;
+                    if (j < nb[1]) {
+                        if (!mbar_wait(b_pfull(1), j & 1, abort_flag, err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(1, vs, j == 0);
                     }
-                    tc_fence_after();
-                    issue_pv(1, vs, j == 0);
+                    tc_commit(b_vempty(vs));
+                    if (j < nb[1] && kn < nb[1]) {
+                        issue_qk(1, ks);
+                        tc_commit(b_sfull(1));
+                    }
+                    if (need_k)
+                        tc_commit(b_kempty(ks));
                 }
-                tc_commit(b_vempty(vs));
-                if (j < nb[1] && kn < nb[1]) {
-                    issue_qk(1, ks);
-                    tc_commit(b_sfull(1));
-                }
-                if (need_k)
-                    tc_commit(b_kempty(ks));
+                if (ok)
+                    tc_commit(b_ofull);
+                // every MMA this thread issued must finish before tensor memory
+                // is released
+                tc_commit(b_drain);
+                mbar_wait_drain(b_drain, 0);
             }
-            if (ok)
-                tc_commit(b_ofull);
-            // every MMA this thread issued must finish before tensor memory
-            // is released
-            tc_commit(b_drain);
-            mbar_wait_drain(b_drain, 0);
         }
-    } else {
+        // ---- teardown: every tensor-memory access is done before release
+        tc_fence_before();
+        __syncthreads();
+        if (warp == kMmaWarp) {
+            tc_fence_after();
+            tmem_dealloc(tmem, C::TMEM_COLS);
+        }
+        return;
+    }
+    setmaxnreg_inc<kRegsSoftmax>();
+    {
         // ================================================= softmax warps
         const int t = warp >> 2;
         const int quarter = warp & 3;
@@ -777,13 +804,10 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         }
     }
 
-    // ---- teardown: every tensor-memory access is done before release
+    // ---- teardown of the softmax warps (tensor memory is released by the
+    // MMA warp once every warp has passed this barrier)
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
-    }
 }
 
 } // namespace pf
@@ -1298,6 +1322,17 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
     const pf::Shape sh = make_shape(a, pf::NT * pf::BM);
     const pf::Scales sc{a.q_scale, a.k_scale, a.v_scale};
     auto kern = pf::prefill_kernel<D, BF16, F8, PAGED, OUT>;
+    // the in-kernel register split adds up only if the kernel launches with
+    // exactly kLaunchRegs registers per thread; never launch it otherwise
+    static int regs = -1;
+    if (regs < 0) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
+            return cudaErrorInvalidDeviceFunction;
+        regs = fa.numRegs;
+    }
+    if (regs != pf::kLaunchRegs)
+        return cudaErrorInvalidConfiguration;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
