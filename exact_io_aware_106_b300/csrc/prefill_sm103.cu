@@ -817,27 +817,35 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
 // columns, more than the 512 an SM has, so one CTA owns one query tile and
 // the overlap comes from double-buffering S over consecutive key blocks:
 // while the softmax warpgroup turns S_(j mod 2) into P, the tensor core
-// computes O += P_(j-1) V_(j-1) and S_(j+1).  Key blocks are 64 wide so that
-// two K and two V stages fit next to the Q tile.
-//   warp 4      TMA producer (Q once, K / V rings of 2 stages)
+// computes O += P_(j-1) V_(j-1) and S_(j+1).  16-bit inputs use 128-key
+// blocks (S buffers of 128 columns, O at 256: 512 in all) with one K and one
+// V stage next to Q: 64-key blocks made every score MMA (M = 128, N = 64)
+// read 6 KB of shared-memory operands per 131k multiply-adds, more than the
+// SM's shared memory delivers, while N = 128 halves that per flop.  E4M3
+// inputs keep 64-key blocks (with ten warps a 128-score row would not fit
+// the registers) and two stages.
+//   warp 4      TMA producer: lane 0 Q once and the K stages, lane 1 the V
+//               stages, each waiting only for its own stage
 //   warp 5      MMA issuer (one thread)
 //   warps 6-9   (E4M3 inputs only) widen each V tile to f16, a quarter each
 //   warps 0-3   softmax, one thread per row; the epilogue
-// Tensor memory: S_0 [0,64), S_1 [64,128), O [128, 384).  A block that moves
+// Tensor memory: S_0 [0,BN), S_1 [BN,2BN), O [2BN, 2BN+256).  A block that moves
 // the reference max rescales O only after the previous block's P V product
 // has completed (barrier o_done, one phase per product).
 namespace pfw {
 
 constexpr int D = 256;
 constexpr int BM = 128;
-constexpr int BN = 64;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kConvWarp = 6;
-constexpr int NK = 2, NV = 2;
 
 template <bool F8>
 struct Cfg {
+    // 16-bit: 128-key blocks (N = 128 keeps the score products within the
+    // shared-memory operand bandwidth), one K and one V stage next to Q
+    static constexpr int BN = F8 ? 64 : 128;
+    static constexpr int NK = F8 ? 2 : 1, NV = F8 ? 2 : 1;
     static constexpr int EB = F8 ? 1 : 2;
     static constexpr int PW = 128;
     static constexpr int QK_PANELS = D * EB / PW;
@@ -860,10 +868,10 @@ struct Cfg {
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
-constexpr int S_COL0 = 0, O_COL = 2 * BN;
+constexpr int S_COL0 = 0;
 constexpr uint32_t TMEM_COLS = 512;
-static_assert(O_COL + D <= 512, "tensor memory budget");
 
+template <int BN>
 __device__ __forceinline__ int tile_blocks(const pf::Shape &sh, int r0) {
     const int nkb = (sh.n_kv + BN - 1) / BN;
     if (!sh.causal)
@@ -880,6 +888,8 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
                         float *__restrict__ lse, const pf::Shape sh_in, const pf::Scales sc,
                         const pf::Paged pg, unsigned *err) {
     using C = Cfg<F8>;
+    constexpr int BN = C::BN, NK = C::NK, NV = C::NV, O_COL = 2 * BN;
+    static_assert(O_COL + D <= 512, "tensor memory budget");
     static_assert(!(PAGED && F8), "paged prefill reads 16-bit caches");
     pf::Shape sh = sh_in;
     constexpr bool PB = F8 ? false : BF16;
@@ -918,7 +928,7 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
             return;
         sh.n_kv = len;
     }
-    const int nb = tile_blocks(sh, r0);
+    const int nb = tile_blocks<BN>(sh, r0);
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -972,12 +982,14 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
             mbar_wait_drain(b_qfull, 0);
     } else if (warp == kProducerWarp) {
         // ================================================= TMA producer
+        // lane 0 streams Q and K, lane 1 streams V: each waits only for its
+        // own stage, so a single-stage K never queues behind a V wait
+        constexpr int XP = C::PW / C::EB;
         if (lane == 0) {
-            constexpr int XP = C::PW / C::EB;
             mbar_arrive_expect_tx(b_qfull, C::Q_BYTES);
             for (int p = 0; p < C::QK_PANELS; ++p)
                 tma_load_3d(sQ + p * BM * C::PW, &tm_q, b_qfull, p * XP, r0, bh);
-            int k_issued = 0, v_issued = 0;
+            int k_issued = 0;
             for (int j = 0; j < nb; ++j) {
                 const int ks = j % NK;
                 if (j >= NK && !mbar_wait(b_kempty(ks), ((j / NK) - 1) & 1, abort_flag, err))
@@ -987,6 +999,15 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
                     tma_load_3d(sK + ks * C::K_BYTES + p * BN * C::PW, &tm_k, b_kfull(ks),
                                 p * XP, j * BN, bkv);
                 k_issued = j + 1;
+            }
+            if (*abort_flag) { // let in-flight copies land before the CTA exits
+                mbar_wait_drain(b_qfull, 0);
+                for (int u = max(0, k_issued - NK); u < k_issued; ++u)
+                    mbar_wait_drain(b_kfull(u % NK), (u / NK) & 1);
+            }
+        } else if (lane == 1) {
+            int v_issued = 0;
+            for (int j = 0; j < nb; ++j) {
                 if constexpr (F8) {
                     const int vs = j % C::NVS;
                     if (j >= C::NVS &&
@@ -1007,10 +1028,7 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
                 }
                 v_issued = j + 1;
             }
-            if (*abort_flag) { // let in-flight copies land before the CTA exits
-                mbar_wait_drain(b_qfull, 0);
-                for (int u = max(0, k_issued - NK); u < k_issued; ++u)
-                    mbar_wait_drain(b_kfull(u % NK), (u / NK) & 1);
+            if (*abort_flag) {
                 if constexpr (F8) {
                     for (int u = max(0, v_issued - C::NVS); u < v_issued; ++u)
                         mbar_wait_drain(b_vsfull(u % C::NVS), (u / C::NVS) & 1);
@@ -1139,7 +1157,10 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
             float s[BN];
             {
                 uint32_t u[BN];
-                tmem_ld64(tS, u);
+                if constexpr (BN == 128)
+                    tmem_ld128(tS, u);
+                else
+                    tmem_ld64(tS, u);
 #pragma unroll
                 for (int i = 0; i < BN; ++i)
                     s[i] = __uint_as_float(u[i]);
@@ -1350,7 +1371,7 @@ static cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t st) {
     using C = pfw::Cfg<F8>;
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, a.Q, pfw::D, a.n_q, a.B * a.Hq, BF16, F8, pfw::BM) ||
-        !make_kv_maps(&mk, &mv, a, pfw::D, BF16, F8, pfw::BN))
+        !make_kv_maps(&mk, &mv, a, pfw::D, BF16, F8, pfw::Cfg<F8>::BN))
         return cudaErrorInvalidValue;
     const pf::Shape sh = make_shape(a, pfw::BM);
     const pf::Scales sc{a.q_scale, a.k_scale, a.v_scale};
