@@ -108,10 +108,15 @@ constexpr int kMaxUnits = 256;  // units per CTA (tps <= 4096)
 constexpr int kSplitKeys = 512; // sequences shorter than this carry the P residual
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
-constexpr int min_ctas() { return D == 64 ? 4 : (D == 128 ? 3 : 2); }
+// resident CTAs per SM; with two 16-row tiles per CTA (NRT = 2, head size
+// 64 only) every consumer thread keeps twice the accumulators
+template <int D, int NRT = 1>
+constexpr int min_ctas() {
+    static_assert(NRT == 1 || D == 64, "two row tiles per CTA at head size 64 only");
+    return NRT == 1 ? (D == 64 ? 4 : (D == 128 ? 3 : 2)) : 3;
+}
 
-template <int D, bool KV8>
+template <int D, bool KV8, int NRT = 1>
 struct Lay {
     static constexpr int ROWB = KV8 ? D : 2 * D;          // bytes of one cache row
     static constexpr int PW = ROWB < 128 ? ROWB : 128;     // row bytes per panel = swizzle span
@@ -128,9 +133,10 @@ struct Lay {
     static constexpr int NST = KV8 ? (D == 64 ? 24 : (D == 128 ? 16 : 8))
                                    : (D == 64 ? 12 : (D == 128 ? 8 : 4));
     static_assert(NST % kNC == 0, "each stage must belong to one consumer warp");
-    static constexpr int MIN_CTAS = min_ctas<D>();
+    static constexpr int MIN_CTAS = min_ctas<D, NRT>();
     static constexpr int QROW = 2 * D + 16;                // padded q row (16-bit caches)
-    static constexpr int QBYTES = KV8 ? (D / 16) * 32 * 16 : 16 * QROW;
+    static constexpr int QBYTES1 = KV8 ? (D / 16) * 32 * 16 : 16 * QROW; // one row tile
+    static constexpr int QBYTES = NRT * QBYTES1;
     static constexpr int RING = NST * STAGE;
     static constexpr int MERGE_U = kNC * 16 * D * 4;
     static constexpr int MERGE = MERGE_U + kNC * 16 * 8;
@@ -183,18 +189,18 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
-template <int D, bool QBF16, bool KV8>
-__global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
+template <int D, bool QBF16, bool KV8, int NRT>
+__global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const void *__restrict__ q_,
                       const int32_t *__restrict__ block_table,
                       const int32_t *__restrict__ seq_lens, const float *__restrict__ k_scale,
                       const float *__restrict__ v_scale, float2 *__restrict__ ws_ml,
-                      float *__restrict__ ws_u, int Hq, int G, int T, int nrt, int block_size,
+                      float *__restrict__ ws_u, int Hq, int G, int T, int ngrp, int block_size,
                       int max_blocks,
                       int num_blocks, int max_seq_len, int tps, int max_splits, float c,
                       unsigned *err) {
-    using Ly = Lay<D, KV8>;
+    using Ly = Lay<D, KV8, NRT>;
     constexpr bool MB = KV8 ? false : QBF16; // operand format of the MMAs (bf16 or f16)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -207,11 +213,11 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     auto b_empty = [&](int i) { return bar0 + 8u * (Ly::NST + i); };
     __shared__ int s_flag; // 1 = bad index, 2 = aborted
     __shared__ int s_abort;
-    __shared__ int s_amax; // max |q| of the group as float bits (E4M3 caches)
+    __shared__ int s_amax[NRT]; // max |q| of each row tile as float bits (E4M3 caches)
 
-    // x = (split, row tile): the nrt row tiles of one split are adjacent, so
-    // the K/V they all stream is read from DRAM about once and from L2 after
-    const int split = blockIdx.x / nrt, rt = blockIdx.x % nrt;
+    // x = (split, group of NRT row tiles): the groups of one split are
+    // adjacent, so the K/V they all stream is read from DRAM about once
+    const int split = blockIdx.x / ngrp, grp = blockIdx.x % ngrp;
     const int hk = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int len = seq_lens[s];
@@ -230,16 +236,21 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     const int head0 = hk * G;
     // rows of the group: r = g * T + i for head head0 + g and new token i
     // (q [num_seqs, Hq, T, d], so a group's rows are contiguous); this CTA
-    // takes the 16-row tile [row0, row0 + 16) of them
-    const int row0 = 16 * rt;
-    const int R = min(16, G * T - row0);
+    // takes the NRT 16-row tiles [row0 + 16 rt, row0 + 16 rt + 16) of them
+    const int row0 = 16 * NRT * grp;
+    int R[NRT]; // real rows of each tile
+#pragma unroll
+    for (int rt = 0; rt < NRT; ++rt)
+        R[rt] = max(0, min(16, G * T - row0 - 16 * rt));
     const uint16_t *qg = static_cast<const uint16_t *>(q_) +
                          ((static_cast<size_t>(s) * Hq + head0) * T + row0) * D;
 
     if (threadIdx.x == 0) {
         s_flag = 0;
         s_abort = 0;
-        s_amax = 0;
+#pragma unroll
+        for (int rt = 0; rt < NRT; ++rt)
+            s_amax[rt] = 0;
     }
     __syncthreads();
     for (int u = threadIdx.x; u < nunits; u += kThreads) {
@@ -250,41 +261,53 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
         blk_ids[u] = phys;
     }
     if constexpr (!KV8) {
-        // the group's query rows, zero rows up to 16, padded rows
-        for (int i = threadIdx.x; i < 16 * (D / 8); i += kThreads) {
-            const int r = i / (D / 8), c8 = i % (D / 8);
+        // the tiles' query rows, zero rows up to 16 per tile, padded rows
+        for (int i = threadIdx.x; i < NRT * 16 * (D / 8); i += kThreads) {
+            const int r = i / (D / 8), c8 = i % (D / 8); // r = 16 rt + row in tile
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < R)
+            if ((r & 15) < R[r >> 4])
                 v = *reinterpret_cast<const uint4 *>(qg + static_cast<size_t>(r) * D + c8 * 8);
             *reinterpret_cast<uint4 *>(base + Ly::OFF_Q + r * Ly::QROW + c8 * 16) = v;
         }
     } else {
-        float amax = 0.f;
-        for (int i = threadIdx.x; i < R * D; i += kThreads) {
-            const float x = QBF16 ? __uint_as_float(static_cast<uint32_t>(qg[i]) << 16)
-                                  : __half2float(__ushort_as_half(qg[i]));
-            amax = fmaxf(amax, fabsf(x));
+#pragma unroll
+        for (int rt = 0; rt < NRT; ++rt) {
+            float amax = 0.f;
+            for (int i = threadIdx.x; i < R[rt] * D; i += kThreads) {
+                const uint16_t x16 = qg[static_cast<size_t>(16 * rt) * D + i];
+                const float x = QBF16 ? __uint_as_float(static_cast<uint32_t>(x16) << 16)
+                                      : __half2float(__ushort_as_half(x16));
+                amax = fmaxf(amax, fabsf(x));
+            }
+            if (amax > 0.f)
+                atomicMax(&s_amax[rt], __float_as_int(amax)); // non-negative floats order as ints
         }
-        if (amax > 0.f)
-            atomicMax(&s_amax, __float_as_int(amax)); // non-negative floats order as ints
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < Ly::NST; ++i) {
-            mbar_init(b_full(i), 1);  // producer arrive + tx bytes
-            mbar_init(b_empty(i), 1); // the consuming warp
+            mbar_init(b_full(i), 1);    // producer arrive + tx bytes
+            mbar_init(b_empty(i), 1);   // the consuming warp (it serves every row tile)
         }
         fence_barrier_init();
     }
     __syncthreads();
-    float qs = 1.0f; // power-of-two scale that keeps the f16 copy of q in range
+    // power-of-two scale that keeps the f16 copy of each tile's q in range
+    float qs[NRT];
+#pragma unroll
+    for (int rt = 0; rt < NRT; ++rt)
+        qs[rt] = 1.0f;
     if constexpr (KV8) {
-        const float amax = __int_as_float(s_amax);
-        if (amax > 0.f && isfinite(amax))
-            qs = exp2f(14.0f - floorf(log2f(amax)));
+#pragma unroll
+        for (int rt = 0; rt < NRT; ++rt) {
+            const float amax = __int_as_float(s_amax[rt]);
+            if (amax > 0.f && isfinite(amax))
+                qs[rt] = exp2f(14.0f - floorf(log2f(amax)));
+        }
         // q as f16 in the permuted fragment order: chunk ch, lane (g, t) gets
         // {(g, 4t..4t+1), (g+8, 4t..4t+1), (g, 4t+2..4t+3), (g+8, 4t+2..4t+3)}
-        for (int i = threadIdx.x; i < (D / 16) * 32; i += kThreads) {
-            const int ch = i >> 5, ln = i & 31, gg = ln >> 2, tt = ln & 3;
+        for (int i = threadIdx.x; i < NRT * (D / 16) * 32; i += kThreads) {
+            const int rt = i / ((D / 16) * 32), ii = i % ((D / 16) * 32);
+            const int ch = ii >> 5, ln = ii & 31, gg = ln >> 2, tt = ln & 3;
             uint32_t w[4];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {   // row gg + 8 h
@@ -292,18 +315,18 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
                 for (int k = 0; k < 2; ++k) { // elements 4t + 2k, 4t + 2k + 1
                     const int row = gg + 8 * h;
                     float x0 = 0.f, x1 = 0.f;
-                    if (row < R) {
+                    if (row < R[rt]) {
                         const int e = ch * 16 + 4 * tt + 2 * k;
-                        const uint16_t *src = qg + static_cast<size_t>(row) * D + e;
+                        const uint16_t *src = qg + static_cast<size_t>(16 * rt + row) * D + e;
                         x0 = QBF16 ? __uint_as_float(static_cast<uint32_t>(src[0]) << 16)
                                    : __half2float(__ushort_as_half(src[0]));
                         x1 = QBF16 ? __uint_as_float(static_cast<uint32_t>(src[1]) << 16)
                                    : __half2float(__ushort_as_half(src[1]));
                     }
-                    w[2 * k + h] = pack2<false>(x0 * qs, x1 * qs);
+                    w[2 * k + h] = pack2<false>(x0 * qs[rt], x1 * qs[rt]);
                 }
             }
-            *reinterpret_cast<uint4 *>(base + Ly::OFF_Q + i * 16) =
+            *reinterpret_cast<uint4 *>(base + Ly::OFF_Q + rt * Ly::QBYTES1 + ii * 16) =
                 make_uint4(w[0], w[1], w[2], w[3]);
         }
         __syncthreads();
@@ -311,9 +334,10 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     if (s_flag) {
         if (threadIdx.x == 0)
             atomicOr(err, DERR_INDEX);
-        for (int r = threadIdx.x; r < R; r += kThreads)
-            ws_ml[((static_cast<size_t>(s) * Hq + head0) * T + row0 + r) * max_splits + split] =
-                make_float2(0.f, -1.f); // l < 0 marks an unusable partial
+        for (int r = threadIdx.x; r < NRT * 16; r += kThreads)
+            if ((r & 15) < R[r >> 4])
+                ws_ml[((static_cast<size_t>(s) * Hq + head0) * T + row0 + r) * max_splits +
+                      split] = make_float2(0.f, -1.f); // l < 0 marks an unusable partial
         return;
     }
     volatile int *abort_flag = &s_abort;
@@ -354,13 +378,21 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     const int g = lane >> 2, t = lane & 3;
     const int mj = lane >> 3, mr = lane & 7; // ldmatrix: matrix index, row
     const bool split_p = len < kSplitKeys;
-    const float cq = KV8 ? c * k_scale[hk] / qs : c;
-
-    float o[D / 8][4];
+    float cq[NRT];
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n)
-        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    for (int rt = 0; rt < NRT; ++rt)
+        cq[rt] = KV8 ? c * k_scale[hk] / qs[rt] : c;
+
+    float o[NRT][D / 8][4];
+    float m[NRT][2], l[NRT][2];
+#pragma unroll
+    for (int rt = 0; rt < NRT; ++rt) {
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+            o[rt][n][0] = o[rt][n][1] = o[rt][n][2] = o[rt][n][3] = 0.f;
+        m[rt][0] = m[rt][1] = -INFINITY;
+        l[rt][0] = l[rt][1] = 0.f;
+    }
     bool ok = true;
 
     for (int u = warp; u < nunits; u += kNC) {
@@ -386,19 +418,29 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
             __syncwarp();
         }
 
-        // S = q K^T: 16 rows x 16 tokens as two 8-token column tiles
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        // S = q K^T: 16 rows x 16 tokens per tile as two 8-token column tiles;
+        // every K fragment serves all NRT row tiles
+        float s0[NRT][4], s1[NRT][4];
+#pragma unroll
+        for (int rt = 0; rt < NRT; ++rt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                s0[rt][i] = s1[rt][i] = 0.f;
         if constexpr (!KV8) {
             // matrices {t0-7,d0-7}, {t0-7,d8-15}, {t8-15,d0-7}, {t8-15,d8-15}
             const int k_tok = mr + (mj >> 1) * 8;
             const uint32_t q_lane = sQ + (mr + (mj & 1) * 8) * Ly::QROW + (mj >> 1) * 16;
 #pragma unroll
             for (int kc = 0; kc < D / 16; ++kc) {
-                uint32_t a[4], b[4];
-                ldsm_x4(a, q_lane + kc * 32);
+                uint32_t b[4];
                 ldsm_x4(b, kv_addr<D, KV8>(Ks, k_tok, (kc * 16 + (mj & 1) * 8) * 2));
-                mma16816<MB>(s0, a, b[0], b[1]);
-                mma16816<MB>(s1, a, b[2], b[3]);
+#pragma unroll
+                for (int rt = 0; rt < NRT; ++rt) {
+                    uint32_t a[4];
+                    ldsm_x4(a, q_lane + rt * 16 * Ly::QROW + kc * 32);
+                    mma16816<MB>(s0[rt], a, b[0], b[1]);
+                    mma16816<MB>(s1[rt], a, b[2], b[3]);
+                }
             }
         } else {
             // matrices {t0-7,c}, {t8-15,c}, {t0-7,c+1}, {t8-15,c+1} of 16-byte chunks
@@ -407,84 +449,101 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
             for (int cp = 0; cp < D / 32; ++cp) {
                 uint32_t b[4];
                 ldsm_x4(b, kv_addr<D, KV8>(Ks, k_tok, (2 * cp + (mj >> 1)) * 16));
-                const uint4 q0 = lds128(sQ + ((2 * cp) * 32 + lane) * 16);
-                const uint4 q1 = lds128(sQ + ((2 * cp + 1) * 32 + lane) * 16);
-                const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
-                const uint32_t a1[4] = {q1.x, q1.y, q1.z, q1.w};
-                mma16816<false>(s0, a0, e4m3x2_f16x2(b[0]), e4m3x2_f16x2(b[0] >> 16));
-                mma16816<false>(s1, a0, e4m3x2_f16x2(b[1]), e4m3x2_f16x2(b[1] >> 16));
-                mma16816<false>(s0, a1, e4m3x2_f16x2(b[2]), e4m3x2_f16x2(b[2] >> 16));
-                mma16816<false>(s1, a1, e4m3x2_f16x2(b[3]), e4m3x2_f16x2(b[3] >> 16));
+                const uint32_t kb00 = e4m3x2_f16x2(b[0]), kb01 = e4m3x2_f16x2(b[0] >> 16);
+                const uint32_t kb10 = e4m3x2_f16x2(b[1]), kb11 = e4m3x2_f16x2(b[1] >> 16);
+                const uint32_t kb20 = e4m3x2_f16x2(b[2]), kb21 = e4m3x2_f16x2(b[2] >> 16);
+                const uint32_t kb30 = e4m3x2_f16x2(b[3]), kb31 = e4m3x2_f16x2(b[3] >> 16);
+#pragma unroll
+                for (int rt = 0; rt < NRT; ++rt) {
+                    const uint32_t qt = sQ + rt * Ly::QBYTES1;
+                    const uint4 q0 = lds128(qt + ((2 * cp) * 32 + lane) * 16);
+                    const uint4 q1 = lds128(qt + ((2 * cp + 1) * 32 + lane) * 16);
+                    const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
+                    const uint32_t a1[4] = {q1.x, q1.y, q1.z, q1.w};
+                    mma16816<false>(s0[rt], a0, kb00, kb01);
+                    mma16816<false>(s1[rt], a0, kb10, kb11);
+                    mma16816<false>(s0[rt], a1, kb20, kb21);
+                    mma16816<false>(s1[rt], a1, kb30, kb31);
+                }
             }
         }
-        // log2-domain scores; row g: tokens 2t, 2t+1, 8+2t, 9+2t; row g+8 the same
-        float sc[8] = {s0[0] * cq, s0[1] * cq, s1[0] * cq, s1[1] * cq,
-                       s0[2] * cq, s0[3] * cq, s1[2] * cq, s1[3] * cq};
-        if (nvalid < kUnit) {
+        uint32_t pa[NRT][4], pl[NRT][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tok = (i >> 1) * 8 + 2 * t + (i & 1);
-                if (tok >= nvalid)
-                    sc[i] = sc[4 + i] = -INFINITY;
+        for (int rt = 0; rt < NRT; ++rt) {
+            // log2-domain scores; row g: tokens 2t, 2t+1, 8+2t, 9+2t; row g+8 the same
+            float sc[8] = {s0[rt][0] * cq[rt], s0[rt][1] * cq[rt], s1[rt][0] * cq[rt],
+                           s1[rt][1] * cq[rt], s0[rt][2] * cq[rt], s0[rt][3] * cq[rt],
+                           s1[rt][2] * cq[rt], s1[rt][3] * cq[rt]};
+            if (nvalid < kUnit) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = (i >> 1) * 8 + 2 * t + (i & 1);
+                    if (tok >= nvalid)
+                        sc[i] = sc[4 + i] = -INFINITY;
+                }
+            }
+            if (T > 1 && t0 + u * kUnit + kUnit - 1 > len - T) {
+                // new token i sees cached token p iff p <= len - T + i (bottom-right)
+                const int rb = row0 + 16 * rt;
+                const int lim0 = len - T + ((rb + g) % T), lim1 = len - T + ((rb + g + 8) % T);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int p = t0 + u * kUnit + (i >> 1) * 8 + 2 * t + (i & 1);
+                    if (p > lim0)
+                        sc[i] = -INFINITY;
+                    if (p > lim1)
+                        sc[4 + i] = -INFINITY;
+                }
+            }
+            float mx[2] = {max4(sc[0], sc[1], sc[2], sc[3]), max4(sc[4], sc[5], sc[6], sc[7])};
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+            }
+            float alpha[2], neg[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float mu = m[rt][r];
+                if (mx[r] > m[rt][r] + kRescaleThreshold || m[rt][r] == -INFINITY)
+                    mu = fmaxf(mx[r], m[rt][r]);
+                alpha[r] = (mu == m[rt][r]) ? 1.0f
+                                            : ((m[rt][r] == -INFINITY) ? 0.f : ex2(m[rt][r] - mu));
+                neg[r] = (mu == -INFINITY) ? 0.f : -mu;
+                m[rt][r] = mu;
+            }
+            float p[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                p[i] = ex2(sc[i] + neg[i >> 2]);
+            l[rt][0] = l[rt][0] * alpha[0] + ((p[0] + p[1]) + (p[2] + p[3]));
+            l[rt][1] = l[rt][1] * alpha[1] + ((p[4] + p[5]) + (p[6] + p[7]));
+            if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    o[rt][n][0] *= alpha[0];
+                    o[rt][n][1] *= alpha[0];
+                    o[rt][n][2] *= alpha[1];
+                    o[rt][n][3] *= alpha[1];
+                }
+            }
+            // P as the A operand: {(g, 2t..), (g+8, 2t..), (g, 8+2t..), (g+8, 8+2t..)}
+            pa[rt][0] = pack2<MB>(p[0], p[1]);
+            pa[rt][1] = pack2<MB>(p[4], p[5]);
+            pa[rt][2] = pack2<MB>(p[2], p[3]);
+            pa[rt][3] = pack2<MB>(p[6], p[7]);
+            if (split_p) {
+                // rounding residual of the 16-bit P, multiplied in as a second
+                // product so that short sequences do not see P's rounding
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int lo_i = (i & 1) * 4 + (i >> 1) * 2;
+                    pl[rt][i] = pack2<MB>(p[lo_i] - lo16<MB>(pa[rt][i]),
+                                          p[lo_i + 1] - hi16<MB>(pa[rt][i]));
+                }
             }
         }
-        if (T > 1 && t0 + u * kUnit + kUnit - 1 > len - T) {
-            // new token i sees cached token p iff p <= len - T + i (bottom-right)
-            const int lim0 = len - T + ((row0 + g) % T), lim1 = len - T + ((row0 + g + 8) % T);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int p = t0 + u * kUnit + (i >> 1) * 8 + 2 * t + (i & 1);
-                if (p > lim0)
-                    sc[i] = -INFINITY;
-                if (p > lim1)
-                    sc[4 + i] = -INFINITY;
-            }
-        }
-        float mx[2] = {max4(sc[0], sc[1], sc[2], sc[3]), max4(sc[4], sc[5], sc[6], sc[7])};
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        }
-        float alpha[2], neg[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            float mu = m[r];
-            if (mx[r] > m[r] + kRescaleThreshold || m[r] == -INFINITY)
-                mu = fmaxf(mx[r], m[r]);
-            alpha[r] = (mu == m[r]) ? 1.0f : ((m[r] == -INFINITY) ? 0.f : ex2(m[r] - mu));
-            neg[r] = (mu == -INFINITY) ? 0.f : -mu;
-            m[r] = mu;
-        }
-        float p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            p[i] = ex2(sc[i] + neg[i >> 2]);
-        l[0] = l[0] * alpha[0] + ((p[0] + p[1]) + (p[2] + p[3]));
-        l[1] = l[1] * alpha[1] + ((p[4] + p[5]) + (p[6] + p[7]));
-        if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
-#pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                o[n][0] *= alpha[0];
-                o[n][1] *= alpha[0];
-                o[n][2] *= alpha[1];
-                o[n][3] *= alpha[1];
-            }
-        }
-        // P as the A operand: {(g, 2t..), (g+8, 2t..), (g, 8+2t..), (g+8, 8+2t..)}
-        uint32_t pa[4] = {pack2<MB>(p[0], p[1]), pack2<MB>(p[4], p[5]), pack2<MB>(p[2], p[3]),
-                          pack2<MB>(p[6], p[7])};
-        uint32_t pl[4];
-        if (split_p) {
-            // rounding residual of the 16-bit P, multiplied in as a second
-            // product so that short sequences do not see P's rounding
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int lo_i = (i & 1) * 4 + (i >> 1) * 2;
-                pl[i] = pack2<MB>(p[lo_i] - lo16<MB>(pa[i]), p[lo_i + 1] - hi16<MB>(pa[i]));
-            }
-        }
-        // u += P V
+        // u += P V; every V fragment serves all NRT row tiles
         if constexpr (!KV8) {
             // V^T fragments by transposed ldmatrix, two d-tiles per load:
             // matrices {t0-7,d0-7}, {t8-15,d0-7}, {t0-7,d8-15}, {t8-15,d8-15}
@@ -493,11 +552,14 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
             for (int np = 0; np < D / 16; ++np) {
                 uint32_t b[4];
                 ldsm_x4_t(b, kv_addr<D, KV8>(Vs, v_tok, (np * 16 + (mj >> 1) * 8) * 2));
-                mma16816<MB>(o[2 * np], pa, b[0], b[1]);
-                mma16816<MB>(o[2 * np + 1], pa, b[2], b[3]);
-                if (split_p) {
-                    mma16816<MB>(o[2 * np], pl, b[0], b[1]);
-                    mma16816<MB>(o[2 * np + 1], pl, b[2], b[3]);
+#pragma unroll
+                for (int rt = 0; rt < NRT; ++rt) {
+                    mma16816<MB>(o[rt][2 * np], pa[rt], b[0], b[1]);
+                    mma16816<MB>(o[rt][2 * np + 1], pa[rt], b[2], b[3]);
+                    if (split_p) {
+                        mma16816<MB>(o[rt][2 * np], pl[rt], b[0], b[1]);
+                        mma16816<MB>(o[rt][2 * np + 1], pl[rt], b[2], b[3]);
+                    }
                 }
             }
         } else {
@@ -517,11 +579,14 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
                     const uint32_t ev1 = e4m3x2_f16x2(prmt(hi, 0x0020u));
                     const uint32_t od0 = e4m3x2_f16x2(prmt(lo, 0x0031u));
                     const uint32_t od1 = e4m3x2_f16x2(prmt(hi, 0x0031u));
-                    mma16816<false>(o[2 * ch], pa, ev0, ev1);
-                    mma16816<false>(o[2 * ch + 1], pa, od0, od1);
-                    if (split_p) {
-                        mma16816<false>(o[2 * ch], pl, ev0, ev1);
-                        mma16816<false>(o[2 * ch + 1], pl, od0, od1);
+#pragma unroll
+                    for (int rt = 0; rt < NRT; ++rt) {
+                        mma16816<false>(o[rt][2 * ch], pa[rt], ev0, ev1);
+                        mma16816<false>(o[rt][2 * ch + 1], pa[rt], od0, od1);
+                        if (split_p) {
+                            mma16816<false>(o[rt][2 * ch], pl[rt], ev0, ev1);
+                            mma16816<false>(o[rt][2 * ch + 1], pl[rt], od0, od1);
+                        }
                     }
                 }
             }
@@ -534,70 +599,80 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8>::MIN_CTAS)
     }
     // the four lanes of a quad hold partial row sums of the same rows
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-    }
+    for (int rt = 0; rt < NRT; ++rt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            l[rt][r] += __shfl_xor_sync(0xffffffffu, l[rt][r], 1);
+            l[rt][r] += __shfl_xor_sync(0xffffffffu, l[rt][r], 2);
+        }
     if (!ok)
         s_flag = 2;
 
-    // ---- merge the consumer warps' states (the ring is drained: every
-    // issued unit was consumed before its consumer reached this barrier)
-    asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
+    // ---- merge the consumer warps' states, one row tile at a time (the
+    // ring is drained: every issued unit was consumed before its consumer
+    // reached this barrier)
     float *mrg_u = reinterpret_cast<float *>(base);                  // [kNC][16][D]
     float2 *mrg_ml = reinterpret_cast<float2 *>(base + Ly::MERGE_U); // [kNC][16]
-    if constexpr (!KV8) {
-        // n-tile n, column 2t + e  <->  d = 8 n + 2 t + e
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            const int col = n * 8 + 2 * t;
-            if (g < R)
-                *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g) * D + col) =
-                    make_float2(o[n][0], o[n][1]);
-            if (g + 8 < R)
-                *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g + 8) * D + col) =
-                    make_float2(o[n][2], o[n][3]);
-        }
-    } else {
-        // chunk ch: even tile 2 ch holds d = 16 ch + 4t + {0, 2}, odd tile
-        // 2 ch + 1 holds d = 16 ch + 4t + {1, 3}
-#pragma unroll
-        for (int ch = 0; ch < D / 16; ++ch) {
-            const int col = ch * 16 + 4 * t;
-            if (g < R)
-                *reinterpret_cast<float4 *>(mrg_u + (warp * 16 + g) * D + col) =
-                    make_float4(o[2 * ch][0], o[2 * ch + 1][0], o[2 * ch][1], o[2 * ch + 1][1]);
-            if (g + 8 < R)
-                *reinterpret_cast<float4 *>(mrg_u + (warp * 16 + g + 8) * D + col) =
-                    make_float4(o[2 * ch][2], o[2 * ch + 1][2], o[2 * ch][3], o[2 * ch + 1][3]);
-        }
-    }
-    if (t == 0) {
-        mrg_ml[warp * 16 + g] = make_float2(m[0], l[0]);
-        mrg_ml[warp * 16 + g + 8] = make_float2(m[1], l[1]);
-    }
-    asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
-    const bool bad = s_flag != 0;
     const float vsc = KV8 ? v_scale[hk] : 1.0f;
-    for (int idx = threadIdx.x; idx < R * D; idx += kNC * 32) {
-        const int r = idx / D, e = idx % D;
-        float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kNC; ++w)
-            M = fmaxf(M, mrg_ml[w * 16 + r].x);
-        float Lsum = 0.f, U = 0.f;
+    for (int rt = 0; rt < NRT; ++rt) {
+        asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
+        const int Rt = R[rt];
+        if constexpr (!KV8) {
+            // n-tile n, column 2t + e  <->  d = 8 n + 2 t + e
 #pragma unroll
-        for (int w = 0; w < kNC; ++w) {
-            const float2 ml = mrg_ml[w * 16 + r];
-            const float sc = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
-            Lsum += sc * ml.y;
-            U += sc * mrg_u[(w * 16 + r) * D + e];
+            for (int n = 0; n < D / 8; ++n) {
+                const int col = n * 8 + 2 * t;
+                if (g < Rt)
+                    *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g) * D + col) =
+                        make_float2(o[rt][n][0], o[rt][n][1]);
+                if (g + 8 < Rt)
+                    *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g + 8) * D + col) =
+                        make_float2(o[rt][n][2], o[rt][n][3]);
+            }
+        } else {
+            // chunk ch: even tile 2 ch holds d = 16 ch + 4t + {0, 2}, odd tile
+            // 2 ch + 1 holds d = 16 ch + 4t + {1, 3}
+#pragma unroll
+            for (int ch = 0; ch < D / 16; ++ch) {
+                const int col = ch * 16 + 4 * t;
+                if (g < Rt)
+                    *reinterpret_cast<float4 *>(mrg_u + (warp * 16 + g) * D + col) =
+                        make_float4(o[rt][2 * ch][0], o[rt][2 * ch + 1][0], o[rt][2 * ch][1],
+                                    o[rt][2 * ch + 1][1]);
+                if (g + 8 < Rt)
+                    *reinterpret_cast<float4 *>(mrg_u + (warp * 16 + g + 8) * D + col) =
+                        make_float4(o[rt][2 * ch][2], o[rt][2 * ch + 1][2], o[rt][2 * ch][3],
+                                    o[rt][2 * ch + 1][3]);
+            }
         }
-        const size_t o_idx =
-            ((static_cast<size_t>(s) * Hq + head0) * T + row0 + r) * max_splits + split;
-        ws_u[o_idx * D + e] = U * vsc;
-        if (e == 0)
-            ws_ml[o_idx] = bad ? make_float2(0.f, -1.f) : make_float2(M, Lsum);
+        if (t == 0) {
+            mrg_ml[warp * 16 + g] = make_float2(m[rt][0], l[rt][0]);
+            mrg_ml[warp * 16 + g + 8] = make_float2(m[rt][1], l[rt][1]);
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
+        const bool bad = s_flag != 0;
+        for (int idx = threadIdx.x; idx < Rt * D; idx += kNC * 32) {
+            const int r = idx / D, e = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kNC; ++w)
+                M = fmaxf(M, mrg_ml[w * 16 + r].x);
+            float Lsum = 0.f, U = 0.f;
+#pragma unroll
+            for (int w = 0; w < kNC; ++w) {
+                const float2 ml = mrg_ml[w * 16 + r];
+                const float sc = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+                Lsum += sc * ml.y;
+                U += sc * mrg_u[(w * 16 + r) * D + e];
+            }
+            const size_t o_idx =
+                ((static_cast<size_t>(s) * Hq + head0) * T + row0 + 16 * rt + r) * max_splits +
+                split;
+            ws_u[o_idx * D + e] = U * vsc;
+            if (e == 0)
+                ws_ml[o_idx] = bad ? make_float2(0.f, -1.f) : make_float2(M, Lsum);
+        }
     }
 }
 
@@ -635,10 +710,22 @@ static cudaError_t launch_combine(const DecodeArgs &a, const float2 *ws_ml, cons
     return cudaGetLastError();
 }
 
-template <int D, bool QBF16, bool KV8>
+// 16-row tiles of a KV head's query rows (G x n_new of them)
+static int decode_row_tiles(const DecodeArgs &a) { return (a.Hq / a.Hkv * a.T + 15) / 16; }
+
+// Row tiles per CTA: two at head size 64 when they pair up, so that each
+// K/V copy and fragment serves both (MQA G = 32 at d = 64: 0.125 -> 0.096
+// ms); at d = 128 the doubled accumulators leave room for one CTA per SM and
+// separate CTAs per tile are faster.
+template <int D>
+static int decode_tiles_per_cta(const DecodeArgs &a) {
+    return (D == 64 && decode_row_tiles(a) % 2 == 0) ? 2 : 1;
+}
+
+template <int D, bool QBF16, bool KV8, int NRT>
 static cudaError_t launch_mma(const DecodeArgs &a, float2 *ws_ml, float *ws_u, int tps,
                               int max_splits, cudaStream_t st) {
-    using Ly = dm::Lay<D, KV8>;
+    using Ly = dm::Lay<D, KV8, NRT>;
     // cache [num_blocks, Hkv, block_size, D] viewed as {D, Hkv * block_size, num_blocks}
     const uint64_t esz = KV8 ? 1 : 2;
     const uint64_t dims[3] = {static_cast<uint64_t>(D),
@@ -652,16 +739,16 @@ static cudaError_t launch_mma(const DecodeArgs &a, float2 *ws_ml, float *ws_u, i
     if (!make_tmap_3d(&mk, a.Kc, el, dims, strides, box, Ly::PW) ||
         !make_tmap_3d(&mv, a.Vc, el, dims, strides, box, Ly::PW))
         return cudaErrorInvalidValue;
-    auto kern = dm::decode_mma_kernel<D, QBF16, KV8>;
+    auto kern = dm::decode_mma_kernel<D, QBF16, KV8, NRT>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
     if (e != cudaSuccess)
         return e;
-    const int nrt = (a.Hq / a.Hkv * a.T + 15) / 16; // 16-row tiles per KV head
-    dim3 grid(max_splits * nrt, a.Hkv, a.num_seqs);
+    const int ngrp = decode_row_tiles(a) / NRT; // CTAs per (split, KV head, sequence)
+    dim3 grid(max_splits * ngrp, a.Hkv, a.num_seqs);
     kern<<<grid, dm::kThreads, Ly::SMEM, st>>>(
         mk, mv, a.q, a.block_table, a.seq_lens, a.k_scale, a.v_scale, ws_ml, ws_u, a.Hq,
-        a.Hq / a.Hkv, a.T, nrt, a.block_size, a.max_blocks, a.num_blocks, a.max_seq_len, tps,
+        a.Hq / a.Hkv, a.T, ngrp, a.block_size, a.max_blocks, a.num_blocks, a.max_seq_len, tps,
         max_splits, a.scale * 1.4426950408889634f, a.err);
     return cudaGetLastError();
 }
@@ -669,10 +756,10 @@ static cudaError_t launch_mma(const DecodeArgs &a, float2 *ws_ml, float *ws_u, i
 // Tokens per split for one call: at least the workspace's split length (so
 // the partials fit), doubled while the grid still has at least four waves of
 // CTAs -- longer splits amortise each CTA's set-up and merge.
-static int choose_tps(const DecodeArgs &a, int resident_per_sm) {
+static int choose_tps(const DecodeArgs &a, int resident_per_sm, int tiles_per_cta) {
     int tps = decode_tokens_per_split(a.max_seq_len);
     const long long pairs = static_cast<long long>(a.num_seqs) * a.Hkv *
-                            ((a.Hq / a.Hkv * a.T + 15) / 16); // CTAs per split
+                            (decode_row_tiles(a) / tiles_per_cta); // CTAs per split
     const long long slots = static_cast<long long>(sm_count()) * resident_per_sm;
     while (tps < 2048) {
         const long long splits = (a.max_seq_len + 2LL * tps - 1) / (2LL * tps);
@@ -685,19 +772,30 @@ static int choose_tps(const DecodeArgs &a, int resident_per_sm) {
 
 template <int D>
 static cudaError_t decode_d(const DecodeArgs &a, cudaStream_t st) {
-    const int tps = choose_tps(a, dm::min_ctas<D>());
+    const int nrt = decode_tiles_per_cta<D>(a);
+    int resident = dm::min_ctas<D, 1>();
+    if constexpr (D == 64)
+        resident = nrt == 2 ? dm::min_ctas<D, 2>() : resident;
+    const int tps = choose_tps(a, resident, nrt);
     const int max_splits = max(1, (a.max_seq_len + tps - 1) / tps);
     const size_t n = static_cast<size_t>(a.num_seqs) * a.Hq * a.T * max_splits;
     size_t ml_bytes = (n * sizeof(float2) + 255) & ~static_cast<size_t>(255);
     float2 *ws_ml = static_cast<float2 *>(a.workspace);
     float *ws_u = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + ml_bytes);
     cudaError_t e;
-    if (a.kv_e4m3)
-        e = a.q_bf16 ? launch_mma<D, true, true>(a, ws_ml, ws_u, tps, max_splits, st)
-                     : launch_mma<D, false, true>(a, ws_ml, ws_u, tps, max_splits, st);
+    auto run = [&](auto nrt_c) -> cudaError_t {
+        constexpr int NRT = decltype(nrt_c)::value;
+        if (a.kv_e4m3)
+            return a.q_bf16 ? launch_mma<D, true, true, NRT>(a, ws_ml, ws_u, tps, max_splits, st)
+                            : launch_mma<D, false, true, NRT>(a, ws_ml, ws_u, tps, max_splits,
+                                                               st);
+        return a.q_bf16 ? launch_mma<D, true, false, NRT>(a, ws_ml, ws_u, tps, max_splits, st)
+                        : launch_mma<D, false, false, NRT>(a, ws_ml, ws_u, tps, max_splits, st);
+    };
+    if constexpr (D == 64)
+        e = nrt == 2 ? run(std::integral_constant<int, 2>{}) : run(std::integral_constant<int, 1>{});
     else
-        e = a.q_bf16 ? launch_mma<D, true, false>(a, ws_ml, ws_u, tps, max_splits, st)
-                     : launch_mma<D, false, false>(a, ws_ml, ws_u, tps, max_splits, st);
+        e = run(std::integral_constant<int, 1>{});
     if (e != cudaSuccess)
         return e;
     switch (a.out_dtype) {

@@ -26,6 +26,7 @@ CASES = [
     (2, 16, 8, 256, 16, [70, 9], "f16"),
     (6, 6, 2, 128, 16, [1, 2, 3, 250, 251, 1300], "bf16"),   # G = 3
     (3, 32, 1, 128, 16, [1, 777, 3000], "bf16"),             # MQA, G = 32: two row tiles
+    (3, 32, 1, 64, 16, [1, 777, 3000], "bf16"),              # d = 64, G = 32: one CTA, two tiles
     (2, 40, 1, 64, 32, [100, 2500], "f16"),                  # G = 40: three tiles, last ragged
     (2, 64, 1, 256, 16, [17, 1200], "bf16"),                 # G = 64: four tiles
 ]
@@ -49,8 +50,8 @@ def test_decode_small(case):
         assert_lse(lse, lse_ref)
 
 
-@pytest.mark.parametrize("d", [64, 128, 256])
-@pytest.mark.parametrize("G", [1, 4, 8, 16])
+@pytest.mark.parametrize("d,G", [(d, G) for d in (64, 128, 256) for G in (1, 4, 8, 16)] +
+                         [(64, 32)])  # d = 64, G = 32: one CTA serving two row tiles
 def test_decode_e4m3(d, G):
     spec = W.DecodeSpec(3, 2 * G, 2, d, 1, 2000, 16, "bf16", "e4m3", "bf16")
     t = W.make_decode(spec, seed=2, lens=[2000, 1500, 37], keep_unquantised=True)
