@@ -14,18 +14,20 @@
 //   bwd_prep_kernel   D = rowsum(dO * O), one warp per row.
 //   bwd_kv_kernel     one CTA per (b, KV head, 128-key block): K and V stay
 //                     in shared memory; for every query head of the group
-//                     and every query block that sees the keys, in two
-//                     half-steps of 64 queries,
+//                     and every query block that sees the keys,
 //                       S^T = K Q^T, dP^T = V dO^T        (tcgen05, TMEM)
 //                       P^T, dS^T                          (4 warps, one key row each)
 //                       dV += P^T dO, dK += dS^T Q         (tcgen05, A = TMEM)
 //   bwd_q_kernel      one CTA per (b, head, 128-row query block): for every
-//                     64 keys it sees, S = Q K^T, dP = dO V^T, dS, and
+//                     key block it sees, S = Q K^T, dP = dO V^T, dS, and
 //                     dQ += dS K.
-// The score blocks of consecutive half-steps alternate between two tensor-
-// memory buffers: the tensor core computes the scores of half-step h+1 (and
-// after the second products of h, those of h+2) while the four softmax warps
-// turn half-step h's scores into P and dS, so neither waits for the other.
+// Every score product is a full 128 x 128 block (N = 128: a tcgen05.mma with
+// N = 64 runs at two thirds of the tensor core's rate).  The softmax warps
+// work on a step's block in two halves of 64 columns and signal after each.
+// Per step the tensor core runs, in order: half 0's second products, the
+// next step's S (once half 1 has read the scores), half 1's second products,
+// the next step's dP.  The warps take the exponentials of half 0 while dP is
+// computed and do half 1 while half 0's products run.
 // P and dS enter the second products in the inputs' 16-bit format; the
 // accumulators are fp32 in tensor memory.  Scores are in the log2 domain:
 // p = 2^(s c - lse log2 e), c = scale log2 e.
@@ -37,7 +39,7 @@ namespace attn {
 namespace bw {
 
 constexpr int BT = 128; // rows of a key block and of a query block
-constexpr int HS = 64;  // columns of a half-step (queries for dK/dV, keys for dQ)
+constexpr int HS = 64;  // columns of a softmax half (queries for dK/dV, keys for dQ)
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -52,13 +54,15 @@ struct Cfg {
     static constexpr int OFF_S = OFF_A + 2 * TILE;   // NS stages of the streamed pair
     static constexpr int OFF_ROW = OFF_S + NS * 2 * TILE; // -lse2 / -D of 128 rows, 2 buffers
     static constexpr int OFF_BAR = OFF_ROW + 2 * 2 * BT * 4;
-    // afull, sfull/sempty[NS], mma[2], pready[2], done, drain
+    // afull, sfull/sempty[NS], sready, dpready, pready[2], done, drain
     static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
-    // half-step buffer e: scores at 128 e, second product at 128 e + 64
-    __host__ __device__ static constexpr int S_COL(int e) { return e * BT; }
-    __host__ __device__ static constexpr int DP_COL(int e) { return e * BT + HS; }
+    // a step's 128 x 128 scores at S_COL, the second product at DP_COL.
+    // Softmax half e reads columns [64 e, 64 e + 64) of each and writes its
+    // 16-bit results (two per column) over the dP columns it has read, so the
+    // score columns are free for the next step once both halves are read.
+    static constexpr int S_COL = 0, DP_COL = BT;
     static constexpr int ACC0 = 2 * BT, ACC1 = 2 * BT + D;
     static_assert(2 * BT + 2 * D <= 512, "tensor memory budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -128,7 +132,7 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *map, 
 
 // Issues acc += A(tmem, 128 rows x 64 in 16-bit, two per column) *
 // B(rows [64 e, 64 e + 64) of a 128-row smem tile, MN-major: K = tile rows,
-// N = D): one half-step's second product.
+// N = D): the second product of one softmax half.
 template <int D>
 __device__ __forceinline__ void mma_tmem_a_half(uint32_t acc, uint32_t a_tmem, uint32_t b_tile,
                                                 int e, uint32_t idesc, bool first) {
@@ -139,17 +143,16 @@ __device__ __forceinline__ void mma_tmem_a_half(uint32_t acc, uint32_t a_tmem, u
     }
 }
 
-// Issues acc = A(smem tile, K-major, 128 rows) * B(rows [64 e, 64 e + 64) of
-// a smem tile, K-major)^T over K = D: a 128 x 64 score block.
+// Issues acc = A(smem tile, K-major, 128 rows) * B(smem tile, K-major, 128
+// rows)^T over K = D: a 128 x 128 score block.
 template <int D>
-__device__ __forceinline__ void mma_ss_half(uint32_t acc, uint32_t a_tile, uint32_t b_tile, int e,
-                                            uint32_t idesc) {
-    const uint32_t bh = b_tile + e * HS * 128; // 64 rows into every 128-byte panel
+__device__ __forceinline__ void mma_ss_block(uint32_t acc, uint32_t a_tile, uint32_t b_tile,
+                                             uint32_t idesc) {
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k / 4) * (BT * 128) + (k % 4) * 32;
-        mma_ss(acc, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(bh + off, 16, 1024), idesc,
-               k > 0 ? 1u : 0u);
+        mma_ss(acc, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024),
+               idesc, k > 0 ? 1u : 0u);
     }
 }
 
@@ -191,10 +194,9 @@ __device__ __forceinline__ int key_blocks(const Shape &sh, int qb) {
 
 // ========================================================================
 // dK, dV: one CTA per (b, KV head, key block).  Step t = (query head of the
-// group, query block); each step is two half-steps of 64 queries whose
-// scores live in the two tensor-memory buffers, so that S^T, dP^T of the
-// half-step two ahead are computed while the softmax warps work on the
-// current one.
+// group, query block): S^T, dP^T of the step's 128 queries, then dV, dK fed
+// half by half as the softmax warps finish each 64 queries (P^T of half e at
+// dP^T columns [64 e, 64 e + 32), dS^T at [64 e + 32, 64 e + 64)).
 template <int D, bool BF16, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -217,8 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_afull = bar0;
     auto b_sfull = [&](int i) { return bar0 + 8u * (1 + i); };
     auto b_sempty = [&](int i) { return bar0 + 8u * (1 + C::NS + i); };
-    auto b_mma = [&](int e) { return bar0 + 8u * (1 + 2 * C::NS + e); };    // S^T, dP^T ready
-    auto b_pready = [&](int e) { return bar0 + 8u * (3 + 2 * C::NS + e); }; // P^T, dS^T ready
+    const uint32_t b_s = bar0 + 8u * (1 + 2 * C::NS); // scores ready
+    const uint32_t b_dp = b_s + 8u;                   // second product ready
+    auto b_pready = [&](int e) { return bar0 + 8u * (3 + 2 * C::NS + e); }; // half e packed
     const uint32_t b_done = bar0 + 8u * (5 + 2 * C::NS);
     const uint32_t b_drain = b_done + 8u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
@@ -232,7 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qb0 = first_qblock(sh, kb);
     const int nq_steps = sh.nqb - qb0;     // query blocks per query head
     const int nsteps = sh.G * nq_steps;    // (head, query block) steps
-    const int nhalf = 2 * nsteps;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -241,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_sfull(i), 1);
             mbar_init(b_sempty(i), 1);
         }
-        for (int e = 0; e < 2; ++e) {
-            mbar_init(b_mma(e), 1);
+        mbar_init(b_s, 1);
+        mbar_init(b_dp, 1);
+        for (int e = 0; e < 2; ++e)
             mbar_init(b_pready(e), 4);
-        }
         mbar_init(b_done, 1);
         mbar_init(b_drain, 1);
         fence_barrier_init();
@@ -285,49 +287,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16(BT, HS, BF16, false, false);
+            constexpr uint32_t idesc_s = idesc_f16(BT, BT, BF16, false, false);
             constexpr uint32_t idesc_acc = idesc_f16(BT, D, BF16, false, true);
-            // S^T = K Q_e^T, dP^T = V dO_e^T of half-step h into buffer h mod 2
-            auto issue_scores = [&](int h) {
-                const int st = (h >> 1) % C::NS, e = h & 1;
-                mma_ss_half<D>(tmem + C::S_COL(e), sK, sQ(st), e, idesc_s);
-                mma_ss_half<D>(tmem + C::DP_COL(e), sV, sDO(st), e, idesc_s);
-                tc_commit(b_mma(e));
-            };
             bool ok = mbar_wait(b_afull, 0, abort_flag, err);
-            if (ok && nsteps > 0) {
+            if (ok && nsteps > 0)
                 ok = mbar_wait(b_sfull(0), 0, abort_flag, err);
-                if (ok) {
-                    tc_fence_after();
-                    issue_scores(0);
-                    issue_scores(1);
-                }
+            if (ok && nsteps > 0) {
+                tc_fence_after();
+                mma_ss_block<D>(tmem + C::S_COL, sK, sQ(0), idesc_s);
+                tc_commit(b_s);
+                mma_ss_block<D>(tmem + C::DP_COL, sV, sDO(0), idesc_s);
+                tc_commit(b_dp);
             }
-            for (int h = 0; ok && h < nhalf; ++h) {
-                const int t = h >> 1, e = h & 1, st = t % C::NS;
-                if (!mbar_wait(b_pready(e), t & 1, abort_flag, err)) {
+            for (int t = 0; ok && t < nsteps; ++t) {
+                const int st = t % C::NS, sn = (t + 1) % C::NS;
+                const bool next = t + 1 < nsteps;
+                if (!mbar_wait(b_pready(0), t & 1, abort_flag, err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // dV += P^T dO_e, dK += dS^T Q_e (the half-step's 64 queries)
-                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::S_COL(e), sDO(st), e, idesc_acc,
-                                   h == 0);
-                mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL(e), sQ(st), e, idesc_acc,
-                                   h == 0);
-                if (e == 1)
-                    tc_commit(b_sempty(st)); // both halves of step t consumed
-                const int hn = h + 2;
-                if (hn < nhalf) {
-                    const int tn = hn >> 1;
-                    if (e == 0 &&
-                        !mbar_wait(b_sfull(tn % C::NS), (tn / C::NS) & 1, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // into the buffer the products above read (issued after them)
-                    issue_scores(hn);
+                // dV += P^T dO, dK += dS^T Q over queries 0-63
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL, sDO(st), 0, idesc_acc,
+                                   t == 0);
+                mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL + 32, sQ(st), 0, idesc_acc,
+                                   t == 0);
+                if (!mbar_wait(b_pready(1), t & 1, abort_flag, err) ||
+                    (next && !mbar_wait(b_sfull(sn), ((t + 1) / C::NS) & 1, abort_flag, err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (next) {
+                    // both halves have read the scores: step t+1's may replace them
+                    mma_ss_block<D>(tmem + C::S_COL, sK, sQ(sn), idesc_s);
+                    tc_commit(b_s);
+                }
+                // the same over queries 64-127
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL + 64, sDO(st), 1, idesc_acc,
+                                   false);
+                mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL + 96, sQ(st), 1, idesc_acc,
+                                   false);
+                tc_commit(b_sempty(st)); // step t's stage consumed
+                if (next) {
+                    // after half 1's products, which read these columns (the
+                    // tensor core runs in issue order)
+                    mma_ss_block<D>(tmem + C::DP_COL, sV, sDO(sn), idesc_s);
+                    tc_commit(b_dp);
                 }
             }
             if (ok)
@@ -358,76 +364,99 @@ __global__ void __launch_bounds__(kThreads, 1)
         float nl, nd;
         fetch(0, nl, nd);
         bool ok = true;
-        for (int h = 0; h < nhalf; ++h) {
-            const int t = h >> 1, e = h & 1;
+        const uint32_t tS = tmem + lane_off + C::S_COL;
+        const uint32_t tP = tmem + lane_off + C::DP_COL;
+        const float2 c2 = make_float2(sh.c, sh.c);
+        for (int t = 0; t < nsteps; ++t) {
             const int qb = qb0 + t % nq_steps;
             float *rl = s_row + (t & 1) * 2 * BT; // -lse2 of the step's 128 queries
             float *rd = rl + BT;                  // -D
-            if (e == 0) {
-                // buffer t&1 was last read in step t-2; every warp has passed
-                // step t-1's barrier since, so it is free
-                rl[j] = nl;
-                rd[j] = nd;
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                fetch(t + 1, nl, nd);
-            }
+            // buffer t&1 was last read in step t-2; every warp has passed
+            // step t-1's barrier since, so it is free
+            rl[j] = nl;
+            rd[j] = nd;
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            fetch(t + 1, nl, nd);
             // after a failed wait the warp keeps looping (and meeting the
             // named barrier above) without touching tensor memory, so that
             // its sibling warps never wait on it there
-            if (!ok || !mbar_wait_warp(b_mma(e), t & 1, abort_flag, err)) {
+            if (!ok || !mbar_wait_warp(b_s, t & 1, abort_flag, err)) {
                 ok = false;
                 continue;
             }
             tc_fence_after();
-            const uint32_t tS = tmem + lane_off + C::S_COL(e);
-            const uint32_t tP = tmem + lane_off + C::DP_COL(e);
             // query i (of the step's block) sees this key iff key <= qb*BT + i + off
-            const int i0 = e * HS;
             const int i_min = key - off - qb * BT; // first visible query (causal)
-            const bool mask = !key_ok || (sh.causal && i_min > i0);
-            const float2 c2 = make_float2(sh.c, sh.c);
-            static_assert(HS == 64, "two 32-column chunks per half-step");
-            uint32_t us0[32], ud0[32], us1[32], ud1[32];
-            tmem_ld32x4(tS, us0, tP, ud0, tS + 32, us1, tP + 32, ud1);
+            // p of queries [i0, i0 + 64) from 64 score columns, with -lse2 from rl
+            auto probs = [&](const uint32_t(&us)[64], int i0, float2(&p)[32]) {
+                const bool mask = !key_ok || (sh.causal && i_min > i0);
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const uint32_t(&us)[32] = ch ? us1 : us0;
-                const uint32_t(&ud)[32] = ch ? ud1 : ud0;
-                uint32_t pw[16], dw[16];
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const int ib = i0 + ch * 32 + 4 * q4;
-                    const float4 l4 = *reinterpret_cast<const float4 *>(rl + ib);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(rd + ib);
+                for (int q4 = 0; q4 < 16; ++q4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(rl + i0 + 4 * q4);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        const int e2 = 4 * q4 + 2 * hh; // element pair within the chunk
+                        const int w = 2 * q4 + hh; // element pair
                         const float2 x = __ffma2_rn(
-                            make_float2(__uint_as_float(us[e2]), __uint_as_float(us[e2 + 1])), c2,
-                            hh ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
-                        float2 p = make_float2(ex2(x.x), ex2(x.y));
+                            make_float2(__uint_as_float(us[2 * w]), __uint_as_float(us[2 * w + 1])),
+                            c2, hh ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+                        p[w] = make_float2(ex2(x.x), ex2(x.y));
                         if (mask) {
-                            if (!key_ok || ib + 2 * hh < i_min)
-                                p.x = 0.f;
-                            if (!key_ok || ib + 2 * hh + 1 < i_min)
-                                p.y = 0.f;
+                            if (!key_ok || i0 + 2 * w < i_min)
+                                p[w].x = 0.f;
+                            if (!key_ok || i0 + 2 * w + 1 < i_min)
+                                p[w].y = 0.f;
                         }
-                        const float2 g = __fadd2_rn(
-                            make_float2(__uint_as_float(ud[e2]), __uint_as_float(ud[e2 + 1])),
-                            hh ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
-                        const float2 ds = __fmul2_rn(p, g);
-                        pw[e2 / 2] = pack2<BF16>(p.x, p.y);
-                        dw[e2 / 2] = pack2<BF16>(ds.x, ds.y);
                     }
                 }
-                tmem_st16(tS + ch * 16, pw);
-                tmem_st16(tP + ch * 16, dw);
+            };
+            // dS = P (dP - D); P and dS packed over the 64 dP columns read
+            auto grads = [&](const float2(&p)[32], const uint32_t(&ud)[64], int i0) {
+                uint32_t pw[32], dw[32];
+#pragma unroll
+                for (int q4 = 0; q4 < 16; ++q4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(rd + i0 + 4 * q4);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int w = 2 * q4 + hh;
+                        const float2 g = __fadd2_rn(
+                            make_float2(__uint_as_float(ud[2 * w]), __uint_as_float(ud[2 * w + 1])),
+                            hh ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
+                        const float2 ds = __fmul2_rn(p[w], g);
+                        pw[w] = pack2<BF16>(p[w].x, p[w].y);
+                        dw[w] = pack2<BF16>(ds.x, ds.y);
+                    }
+                }
+                tmem_st32(tP + i0, pw);
+                tmem_st32(tP + i0 + 32, dw);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+            };
+            {
+                // half 0: exponentials while the tensor core computes dP^T
+                uint32_t us[64], ud[64];
+                float2 p[32];
+                tmem_ld64(tS, us);
+                probs(us, 0, p);
+                if (!mbar_wait_warp(b_dp, t & 1, abort_flag, err)) {
+                    ok = false;
+                    continue;
+                }
+                tc_fence_after();
+                tmem_ld64(tP, ud);
+                grads(p, ud, 0);
+                if (lane == 0)
+                    mbar_arrive(b_pready(0));
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(b_pready(e));
+            {
+                uint32_t us[64], ud[64];
+                float2 p[32];
+                tmem_ld64x2(tS + HS, us, tP + HS, ud);
+                probs(us, HS, p);
+                grads(p, ud, HS);
+                if (lane == 0)
+                    mbar_arrive(b_pready(1));
+            }
         }
         if (ok && nsteps > 0)
             ok = mbar_wait_warp(b_done, 0, abort_flag, err);
@@ -462,9 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ========================================================================
-// dQ: one CTA per (b, query head, query block).  Step t = key block; each
-// step is two half-steps of 64 keys, double-buffered in tensor memory as in
-// the dK/dV kernel.  Half-steps past the last visible key are not computed.
+// dQ: one CTA per (b, query head, query block).  Step t = key block: S, dP
+// of its 128 keys, then dQ fed half by half as the softmax warps finish each
+// 64 keys (dS of half e at dP columns [64 e, 64 e + 32)).  Key blocks past
+// the last visible key are not computed.
 template <int D, bool BF16, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -484,8 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_afull = bar0;
     auto b_sfull = [&](int i) { return bar0 + 8u * (1 + i); };
     auto b_sempty = [&](int i) { return bar0 + 8u * (1 + C::NS + i); };
-    auto b_mma = [&](int e) { return bar0 + 8u * (1 + 2 * C::NS + e); };
-    auto b_pready = [&](int e) { return bar0 + 8u * (3 + 2 * C::NS + e); };
+    const uint32_t b_s = bar0 + 8u * (1 + 2 * C::NS); // scores ready
+    const uint32_t b_dp = b_s + 8u;                   // second product ready
+    auto b_pready = [&](int e) { return bar0 + 8u * (3 + 2 * C::NS + e); }; // half e packed
     const uint32_t b_done = bar0 + 8u * (5 + 2 * C::NS);
     const uint32_t b_drain = b_done + 8u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
@@ -497,12 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = static_cast<int>(blockIdx.x) % nbh;
     const int b = bh / sh.Hq, h = bh % sh.Hq;
     const int bkv = b * sh.Hkv + h / sh.G;
-    // 64-key half-steps up to the block's last visible key; 128-key stages
+    // key blocks up to the query block's last visible key
     int keys = sh.n_kv;
     if (sh.causal)
         keys = min(keys, min(qb * BT + BT - 1, sh.n_q - 1) + (sh.n_kv - sh.n_q) + 1);
-    const int nhalf = (keys + HS - 1) / HS;
-    const int nsteps = (nhalf + 1) / 2;
+    const int nsteps = (keys + BT - 1) / BT;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -511,10 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_sfull(i), 1);
             mbar_init(b_sempty(i), 1);
         }
-        for (int e = 0; e < 2; ++e) {
-            mbar_init(b_mma(e), 1);
+        mbar_init(b_s, 1);
+        mbar_init(b_dp, 1);
+        for (int e = 0; e < 2; ++e)
             mbar_init(b_pready(e), 4);
-        }
         mbar_init(b_done, 1);
         mbar_init(b_drain, 1);
         fence_barrier_init();
@@ -552,47 +582,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16(BT, HS, BF16, false, false);
+            constexpr uint32_t idesc_s = idesc_f16(BT, BT, BF16, false, false);
             constexpr uint32_t idesc_acc = idesc_f16(BT, D, BF16, false, true);
-            // S = Q K_e^T, dP = dO V_e^T of half-step h into buffer h mod 2
-            auto issue_scores = [&](int h) {
-                const int st = (h >> 1) % C::NS, e = h & 1;
-                mma_ss_half<D>(tmem + C::S_COL(e), sQ, sK(st), e, idesc_s);
-                mma_ss_half<D>(tmem + C::DP_COL(e), sDO, sV(st), e, idesc_s);
-                tc_commit(b_mma(e));
-            };
             bool ok = mbar_wait(b_afull, 0, abort_flag, err);
-            if (ok && nhalf > 0) {
+            if (ok && nsteps > 0)
                 ok = mbar_wait(b_sfull(0), 0, abort_flag, err);
-                if (ok) {
-                    tc_fence_after();
-                    issue_scores(0);
-                    if (nhalf > 1)
-                        issue_scores(1);
-                }
+            if (ok && nsteps > 0) {
+                tc_fence_after();
+                mma_ss_block<D>(tmem + C::S_COL, sQ, sK(0), idesc_s);
+                tc_commit(b_s);
+                mma_ss_block<D>(tmem + C::DP_COL, sDO, sV(0), idesc_s);
+                tc_commit(b_dp);
             }
-            for (int hs = 0; ok && hs < nhalf; ++hs) {
-                const int t = hs >> 1, e = hs & 1, st = t % C::NS;
-                if (!mbar_wait(b_pready(e), t & 1, abort_flag, err)) {
+            for (int t = 0; ok && t < nsteps; ++t) {
+                const int st = t % C::NS, sn = (t + 1) % C::NS;
+                const bool next = t + 1 < nsteps;
+                if (!mbar_wait(b_pready(0), t & 1, abort_flag, err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // dQ += dS K_e (the half-step's 64 keys)
-                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL(e), sK(st), e, idesc_acc,
-                                   hs == 0);
-                if (e == 1)
-                    tc_commit(b_sempty(st));
-                const int hn = hs + 2;
-                if (hn < nhalf) {
-                    const int tn = hn >> 1;
-                    if (e == 0 &&
-                        !mbar_wait(b_sfull(tn % C::NS), (tn / C::NS) & 1, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_scores(hn);
+                // dQ += dS K over keys 0-63 of the block
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL, sK(st), 0, idesc_acc,
+                                   t == 0);
+                if (!mbar_wait(b_pready(1), t & 1, abort_flag, err) ||
+                    (next && !mbar_wait(b_sfull(sn), ((t + 1) / C::NS) & 1, abort_flag, err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (next) {
+                    // both halves have read the scores: step t+1's may replace them
+                    mma_ss_block<D>(tmem + C::S_COL, sQ, sK(sn), idesc_s);
+                    tc_commit(b_s);
+                }
+                // the same over keys 64-127
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL + 64, sK(st), 1, idesc_acc,
+                                   false);
+                tc_commit(b_sempty(st)); // step t's stage consumed
+                if (next) {
+                    // after half 1's products, which read these columns (the
+                    // tensor core runs in issue order)
+                    mma_ss_block<D>(tmem + C::DP_COL, sDO, sV(sn), idesc_s);
+                    tc_commit(b_dp);
                 }
             }
             if (ok)
@@ -614,52 +646,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 c2 = make_float2(sh.c, sh.c), l2 = make_float2(nl, nl),
                      d2 = make_float2(nd, nd);
         bool ok = true;
-        for (int hs = 0; hs < nhalf; ++hs) {
-            const int t = hs >> 1, e = hs & 1;
-            if (!mbar_wait_warp(b_mma(e), t & 1, abort_flag, err)) {
+        const uint32_t tS = tmem + lane_off + C::S_COL;
+        const uint32_t tP = tmem + lane_off + C::DP_COL;
+        // p of keys [64 e, 64 e + 64) of step t from 64 score columns
+        auto probs = [&](const uint32_t(&us)[64], int t, int e, float2(&p)[32]) {
+            const int kl = klim - (t * BT + e * HS); // last visible key within the half
+            const bool mask = kl < HS - 1;
+#pragma unroll
+            for (int w = 0; w < 32; ++w) {
+                const float2 x = __ffma2_rn(
+                    make_float2(__uint_as_float(us[2 * w]), __uint_as_float(us[2 * w + 1])), c2,
+                    l2);
+                p[w] = make_float2(ex2(x.x), ex2(x.y));
+                if (mask) {
+                    if (2 * w > kl)
+                        p[w].x = 0.f;
+                    if (2 * w + 1 > kl)
+                        p[w].y = 0.f;
+                }
+            }
+        };
+        // dS = P (dP - D), packed over the first 32 of the 64 dP columns read
+        auto grads = [&](const float2(&p)[32], const uint32_t(&ud)[64], int e) {
+            uint32_t dw[32];
+#pragma unroll
+            for (int w = 0; w < 32; ++w) {
+                const float2 g = __fadd2_rn(
+                    make_float2(__uint_as_float(ud[2 * w]), __uint_as_float(ud[2 * w + 1])), d2);
+                const float2 ds = __fmul2_rn(p[w], g);
+                dw[w] = pack2<BF16>(ds.x, ds.y);
+            }
+            tmem_st32(tP + e * HS, dw);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+        };
+        for (int t = 0; t < nsteps; ++t) {
+            if (!mbar_wait_warp(b_s, t & 1, abort_flag, err)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t tS = tmem + lane_off + C::S_COL(e);
-            const uint32_t tP = tmem + lane_off + C::DP_COL(e);
-            const int kl = klim - hs * HS; // last visible key within this half-step
-            const bool mask = kl < HS - 1;
-            uint32_t us0[32], ud0[32], us1[32], ud1[32];
-            tmem_ld32x4(tS, us0, tP, ud0, tS + 32, us1, tP + 32, ud1);
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const uint32_t(&us)[32] = ch ? us1 : us0;
-                const uint32_t(&ud)[32] = ch ? ud1 : ud0;
-                uint32_t dw[16];
-#pragma unroll
-                for (int e2 = 0; e2 < 16; ++e2) {
-                    const int k = ch * 32 + 2 * e2;
-                    const float2 x = __ffma2_rn(
-                        make_float2(__uint_as_float(us[2 * e2]), __uint_as_float(us[2 * e2 + 1])),
-                        c2, l2);
-                    float2 p = make_float2(ex2(x.x), ex2(x.y));
-                    if (mask) {
-                        if (k > kl)
-                            p.x = 0.f;
-                        if (k + 1 > kl)
-                            p.y = 0.f;
-                    }
-                    const float2 g = __fadd2_rn(
-                        make_float2(__uint_as_float(ud[2 * e2]), __uint_as_float(ud[2 * e2 + 1])),
-                        d2);
-                    const float2 ds = __fmul2_rn(p, g);
-                    dw[e2] = pack2<BF16>(ds.x, ds.y);
+            {
+                // half 0: exponentials while the tensor core computes dP
+                uint32_t us[64], ud[64];
+                float2 p[32];
+                tmem_ld64(tS, us);
+                probs(us, t, 0, p);
+                if (!mbar_wait_warp(b_dp, t & 1, abort_flag, err)) {
+                    ok = false;
+                    break;
                 }
-                tmem_st16(tP + ch * 16, dw);
+                tc_fence_after();
+                tmem_ld64(tP, ud);
+                grads(p, ud, 0);
+                if (lane == 0)
+                    mbar_arrive(b_pready(0));
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(b_pready(e));
+            {
+                uint32_t us[64], ud[64];
+                float2 p[32];
+                tmem_ld64x2(tS + HS, us, tP + HS, ud);
+                probs(us, t, 1, p);
+                grads(p, ud, 1);
+                if (lane == 0)
+                    mbar_arrive(b_pready(1));
+            }
         }
-        if (ok && nhalf > 0)
+        if (ok && nsteps > 0)
             ok = mbar_wait_warp(b_done, 0, abort_flag, err);
         tc_fence_after();
         const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row) * D;
@@ -671,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float o[32];
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
-                    o[k] = (ok && nhalf > 0) ? __uint_as_float(u[k]) * sh.scale : 0.f;
+                    o[k] = (ok && nsteps > 0) ? __uint_as_float(u[k]) * sh.scale : 0.f;
                 store32<OUT>(dQ, orow + ch * 32, o);
             }
         }
