@@ -16,18 +16,19 @@
 //                     in shared memory; for every query head of the group
 //                     and every query block that sees the keys,
 //                       S^T = K Q^T, dP^T = V dO^T        (tcgen05, TMEM)
-//                       P^T, dS^T                          (4 warps, one key row each)
+//                       P^T, dS^T                          (8 warps, two per key row)
 //                       dV += P^T dO, dK += dS^T Q         (tcgen05, A = TMEM)
 //   bwd_q_kernel      one CTA per (b, head, 128-row query block): for every
 //                     key block it sees, S = Q K^T, dP = dO V^T, dS, and
 //                     dQ += dS K.
 // Every score product is a full 128 x 128 block (N = 128: a tcgen05.mma with
-// N = 64 runs at two thirds of the tensor core's rate).  The softmax warps
-// work on a step's block in two halves of 64 columns and signal after each.
-// Per step the tensor core runs, in order: half 0's second products, the
-// next step's S (once half 1 has read the scores), half 1's second products,
-// the next step's dP.  The warps take the exponentials of half 0 while dP is
-// computed and do half 1 while half 0's products run.
+// N = 64 runs at two thirds of the tensor core's rate).  Per step t the
+// tensor core runs, in order: dP(t), S(t+1), the second products of
+// softmax half 0 of step t, those of half 1, then dP(t+1).  The softmax
+// warps load S(t+1) into registers as soon as it lands (freeing its columns
+// for S(t+2)) and take its exponentials while prod1(t) and dP(t+1) run;
+// they form half 0's dS while S(t+2) runs and half 1's while half 0's
+// products run, so the tensor core does not wait on them.
 // P and dS enter the second products in the inputs' 16-bit format; the
 // accumulators are fp32 in tensor memory.  Scores are in the log2 domain:
 // p = 2^(s c - lse log2 e), c = scale log2 e.
@@ -40,32 +41,42 @@ namespace bw {
 
 constexpr int BT = 128; // rows of a key block and of a query block
 constexpr int HS = 64;  // columns of a softmax half (queries for dK/dV, keys for dQ)
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kSoftmaxWarps = 8; // two per TMEM lane quarter
+constexpr int kThreads = 32 * kSoftmaxWarps + 64;
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct Cfg {
     static constexpr int TILE = BT * D * 2;          // one 128-row 16-bit tile
     static constexpr int PANELS = D / 64;
-    static constexpr int NS = 2;                     // stages of the streamed pair of tiles
+    // Two streamed tiles per step, each in its own ring: X feeds the step's
+    // score product (Q for dK/dV, K for dQ), Y the second product (dO, V).
+    // S(t+1) is issued right after dP(t), so X is the ring that needs depth.
+    static constexpr int NX = D == 128 ? 3 : 4;
+    static constexpr int NY = D == 128 ? 2 : 4;
     static constexpr int OFF_A = 0;                  // resident tile pair (K,V or Q,dO)
-    static constexpr int OFF_S = OFF_A + 2 * TILE;   // NS stages of the streamed pair
-    static constexpr int OFF_ROW = OFF_S + NS * 2 * TILE; // -lse2 / -D of 128 rows, 2 buffers
+    static constexpr int OFF_X = OFF_A + 2 * TILE;
+    static constexpr int OFF_Y = OFF_X + NX * TILE;
+    static constexpr int OFF_ROW = OFF_Y + NY * TILE; // -lse2 / -D of 128 rows, 2 buffers
     static constexpr int OFF_BAR = OFF_ROW + 2 * 2 * BT * 4;
-    // afull, sfull/sempty[NS], sready, dpready, pready[2], done, drain
-    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2;
+    // afull, xfull/xempty[NX], yfull/yempty[NY], sready, dpready, sfree,
+    // pready[2], done, drain
+    static constexpr int NBAR = 1 + 2 * NX + 2 * NY + 3 + 2 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 64 + 1024;
+    static constexpr int SMEM_USED = OFF_MISC + 64;  // from the 1024-aligned base
+    // room to align the base; at d = 128 the rings leave less than 1024
+    // bytes, and a kernel whose base needs more padding reports DERR_INDEX
+    static constexpr int SMEM = SMEM_USED + 1024 < 227 * 1024 ? SMEM_USED + 1024 : 227 * 1024;
     // a step's 128 x 128 scores at S_COL, the second product at DP_COL.
-    // Softmax half e reads columns [64 e, 64 e + 64) of each and writes its
-    // 16-bit results (two per column) over the dP columns it has read, so the
-    // score columns are free for the next step once both halves are read.
+    // The softmax warps load all their score columns at once (which frees
+    // them for the next step's scores) and write their 16-bit results (two
+    // per column) over the dP columns they have read.
     static constexpr int S_COL = 0, DP_COL = BT;
     static constexpr int ACC0 = 2 * BT, ACC1 = 2 * BT + D;
     static_assert(2 * BT + 2 * D <= 512, "tensor memory budget");
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(SMEM_USED + 128 <= SMEM, "shared memory budget");
 };
 
 struct Shape {
@@ -130,16 +141,18 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *map, 
         tma_load_3d(dst + p * BT * 128, map, bar, p * 64, row, bh);
 }
 
-// Issues acc += A(tmem, 128 rows x 64 in 16-bit, two per column) *
-// B(rows [64 e, 64 e + 64) of a 128-row smem tile, MN-major: K = tile rows,
-// N = D): the second product of one softmax half.
+// Issues acc += A(tmem, 128 rows x 64 in 16-bit) * B(rows [64 e, 64 e + 64)
+// of a 128-row smem tile, MN-major: K = tile rows, N = D): the second
+// product of one softmax half.  A holds two per column, written by the two
+// warps of a row quarter: elements [0, 32) at columns [0, 16) of a_half,
+// elements [32, 64) at columns [32, 48).
 template <int D>
-__device__ __forceinline__ void mma_tmem_a_half(uint32_t acc, uint32_t a_tmem, uint32_t b_tile,
+__device__ __forceinline__ void mma_tmem_a_half(uint32_t acc, uint32_t a_half, uint32_t b_tile,
                                                 int e, uint32_t idesc, bool first) {
 #pragma unroll
     for (int k = 0; k < HS / 16; ++k) {
         const uint64_t bd = sdesc_sw128(b_tile + (e * (HS / 16) + k) * 16 * 128, BT * 128, 1024);
-        mma_ts(acc, a_tmem + k * 8, bd, idesc, (first && k == 0) ? 0u : 1u);
+        mma_ts(acc, a_half + (k >> 1) * 32 + (k & 1) * 8, bd, idesc, (first && k == 0) ? 0u : 1u);
     }
 }
 
@@ -195,8 +208,8 @@ __device__ __forceinline__ int key_blocks(const Shape &sh, int qb) {
 // ========================================================================
 // dK, dV: one CTA per (b, KV head, key block).  Step t = (query head of the
 // group, query block): S^T, dP^T of the step's 128 queries, then dV, dK fed
-// half by half as the softmax warps finish each 64 queries (P^T of half e at
-// dP^T columns [64 e, 64 e + 32), dS^T at [64 e + 32, 64 e + 64)).
+// half by half as the softmax warps finish each 64 queries (P^T of queries
+// [64 e + 32 c, +32) at dP^T columns [64 e + 32 c, +16), dS^T at the next 16).
 template <int D, bool BF16, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -211,22 +224,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_s - raw_s);
     const uint32_t sK = base_s + C::OFF_A, sV = sK + C::TILE;
-    auto sQ = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE; };
-    auto sDO = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE + C::TILE; };
+    auto sQ = [&](int st) { return base_s + C::OFF_X + st * C::TILE; };  // ring X
+    auto sDO = [&](int st) { return base_s + C::OFF_Y + st * C::TILE; }; // ring Y
     // per step: -lse * log2(e) and -D of its 128 queries, double-buffered
     float *s_row = reinterpret_cast<float *>(base + C::OFF_ROW);
     const uint32_t bar0 = base_s + C::OFF_BAR;
     const uint32_t b_afull = bar0;
-    auto b_sfull = [&](int i) { return bar0 + 8u * (1 + i); };
-    auto b_sempty = [&](int i) { return bar0 + 8u * (1 + C::NS + i); };
-    const uint32_t b_s = bar0 + 8u * (1 + 2 * C::NS); // scores ready
+    auto b_xfull = [&](int i) { return bar0 + 8u * (1 + i); };
+    auto b_xempty = [&](int i) { return bar0 + 8u * (1 + C::NX + i); };
+    auto b_yfull = [&](int i) { return bar0 + 8u * (1 + 2 * C::NX + i); };
+    auto b_yempty = [&](int i) { return bar0 + 8u * (1 + 2 * C::NX + C::NY + i); };
+    const uint32_t b_s = bar0 + 8u * (1 + 2 * C::NX + 2 * C::NY); // scores ready
     const uint32_t b_dp = b_s + 8u;                   // second product ready
-    auto b_pready = [&](int e) { return bar0 + 8u * (3 + 2 * C::NS + e); }; // half e packed
-    const uint32_t b_done = bar0 + 8u * (5 + 2 * C::NS);
+    const uint32_t b_sfree = b_s + 16u;               // scores loaded by the softmax warps
+    auto b_pready = [&](int e) { return b_s + 8u * (3 + e); }; // half e packed
+    const uint32_t b_done = b_s + 40u;
     const uint32_t b_drain = b_done + 8u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
 
+    if (base_s - raw_s + C::SMEM_USED > static_cast<uint32_t>(C::SMEM)) {
+        if (threadIdx.x == 0)
+            atomicOr(err, DERR_INDEX); // the base needed more alignment padding than reserved
+        return;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // heaviest key blocks first (causal: early keys are seen by more queries)
     const int kb = static_cast<int>(blockIdx.x) / (sh.B * sh.Hkv);
@@ -239,14 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(b_afull, 1);
-        for (int i = 0; i < C::NS; ++i) {
-            mbar_init(b_sfull(i), 1);
-            mbar_init(b_sempty(i), 1);
+        for (int i = 0; i < C::NX; ++i) {
+            mbar_init(b_xfull(i), 1);
+            mbar_init(b_xempty(i), 1);
+        }
+        for (int i = 0; i < C::NY; ++i) {
+            mbar_init(b_yfull(i), 1);
+            mbar_init(b_yempty(i), 1);
         }
         mbar_init(b_s, 1);
         mbar_init(b_dp, 1);
+        mbar_init(b_sfree, kSoftmaxWarps);
         for (int e = 0; e < 2; ++e)
-            mbar_init(b_pready(e), 4);
+            mbar_init(b_pready(e), kSoftmaxWarps);
         mbar_init(b_done, 1);
         mbar_init(b_drain, 1);
         fence_barrier_init();
@@ -261,28 +287,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kProducerWarp) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(b_afull, 2 * C::TILE);
-            load_tile<D>(sK, &tm_k, b_afull, kb * BT, bkv);
-            load_tile<D>(sV, &tm_v, b_afull, kb * BT, bkv);
+        // lane 0: K, V, then the Q ring; lane 1: the dO ring (each ring runs
+        // at its own pace)
+        if (lane < 2) {
+            const bool is_x = lane == 0;
+            const int n = is_x ? C::NX : C::NY;
+            if (is_x) {
+                mbar_arrive_expect_tx(b_afull, 2 * C::TILE);
+                load_tile<D>(sK, &tm_k, b_afull, kb * BT, bkv);
+                load_tile<D>(sV, &tm_v, b_afull, kb * BT, bkv);
+            }
             int issued = 0;
             for (int t = 0; t < nsteps; ++t) {
-                const int st = t % C::NS;
-                if (t >= C::NS &&
-                    !mbar_wait(b_sempty(st), ((t / C::NS) - 1) & 1, abort_flag, err))
+                const int st = t % n;
+                if (t >= n && !mbar_wait(is_x ? b_xempty(st) : b_yempty(st), ((t / n) - 1) & 1,
+                                         abort_flag, err))
                     break;
                 const int h = hk * sh.G + t / nq_steps;
                 const int qb = qb0 + t % nq_steps;
                 const int bh = b * sh.Hq + h;
-                mbar_arrive_expect_tx(b_sfull(st), 2 * C::TILE);
-                load_tile<D>(sQ(st), &tm_q, b_sfull(st), qb * BT, bh);
-                load_tile<D>(sDO(st), &tm_do, b_sfull(st), qb * BT, bh);
+                const uint32_t full = is_x ? b_xfull(st) : b_yfull(st);
+                mbar_arrive_expect_tx(full, C::TILE);
+                load_tile<D>(is_x ? sQ(st) : sDO(st), is_x ? &tm_q : &tm_do, full, qb * BT, bh);
                 issued = t + 1;
             }
             if (*abort_flag) {
-                mbar_wait_drain(b_afull, 0);
-                for (int u = max(0, issued - C::NS); u < issued; ++u)
-                    mbar_wait_drain(b_sfull(u % C::NS), (u / C::NS) & 1);
+                if (is_x)
+                    mbar_wait_drain(b_afull, 0);
+                for (int u = max(0, issued - n); u < issued; ++u)
+                    mbar_wait_drain(is_x ? b_xfull(u % n) : b_yfull(u % n), (u / n) & 1);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -291,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_acc = idesc_f16(BT, D, BF16, false, true);
             bool ok = mbar_wait(b_afull, 0, abort_flag, err);
             if (ok && nsteps > 0)
-                ok = mbar_wait(b_sfull(0), 0, abort_flag, err);
+                ok = mbar_wait(b_xfull(0), 0, abort_flag, err) &&
+                     mbar_wait(b_yfull(0), 0, abort_flag, err);
             if (ok && nsteps > 0) {
                 tc_fence_after();
                 mma_ss_block<D>(tmem + C::S_COL, sK, sQ(0), idesc_s);
@@ -300,39 +334,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(b_dp);
             }
             for (int t = 0; ok && t < nsteps; ++t) {
-                const int st = t % C::NS, sn = (t + 1) % C::NS;
+                const int xt = t % C::NX, yt = t % C::NY;
+                const int xn = (t + 1) % C::NX, yn = (t + 1) % C::NY;
                 const bool next = t + 1 < nsteps;
+                if (next) {
+                    if (!mbar_wait(b_xfull(xn), ((t + 1) / C::NX) & 1, abort_flag, err) ||
+                        !mbar_wait(b_sfree, t & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // the softmax warps hold step t's scores in registers
+                    mma_ss_block<D>(tmem + C::S_COL, sK, sQ(xn), idesc_s);
+                    tc_commit(b_s);
+                }
                 if (!mbar_wait(b_pready(0), t & 1, abort_flag, err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 // dV += P^T dO, dK += dS^T Q over queries 0-63
-                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL, sDO(st), 0, idesc_acc,
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL, sDO(yt), 0, idesc_acc,
                                    t == 0);
-                mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL + 32, sQ(st), 0, idesc_acc,
+                mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL + 16, sQ(xt), 0, idesc_acc,
                                    t == 0);
-                if (!mbar_wait(b_pready(1), t & 1, abort_flag, err) ||
-                    (next && !mbar_wait(b_sfull(sn), ((t + 1) / C::NS) & 1, abort_flag, err))) {
+                if (!mbar_wait(b_pready(1), t & 1, abort_flag, err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (next) {
-                    // both halves have read the scores: step t+1's may replace them
-                    mma_ss_block<D>(tmem + C::S_COL, sK, sQ(sn), idesc_s);
-                    tc_commit(b_s);
-                }
                 // the same over queries 64-127
-                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL + 64, sDO(st), 1, idesc_acc,
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL + 64, sDO(yt), 1, idesc_acc,
                                    false);
-                mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL + 96, sQ(st), 1, idesc_acc,
+                mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL + 80, sQ(xt), 1, idesc_acc,
                                    false);
-                tc_commit(b_sempty(st)); // step t's stage consumed
+                tc_commit(b_xempty(xt)); // step t's Q and dO consumed
+                tc_commit(b_yempty(yt));
                 if (next) {
+                    if (!mbar_wait(b_yfull(yn), ((t + 1) / C::NY) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     // after half 1's products, which read these columns (the
                     // tensor core runs in issue order)
-                    mma_ss_block<D>(tmem + C::DP_COL, sV, sDO(sn), idesc_s);
+                    mma_ss_block<D>(tmem + C::DP_COL, sV, sDO(yn), idesc_s);
                     tc_commit(b_dp);
                 }
             }
@@ -342,27 +388,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_drain(b_drain, 0);
         }
     } else {
-        // ---- warps 0-3: one key row each
-        const int j = warp * 32 + lane; // key within the block
+        // ---- warps 0-7: one key row each, two warps per TMEM lane quarter;
+        // warp half c takes queries [32 c, 32 c + 32) of each softmax half
+        const int quarter = warp & 3, cpart = warp >> 2;
+        const int j = quarter * 32 + lane; // key within the block
         const int key = kb * BT + j;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int off = sh.n_kv - sh.n_q;
         const bool key_ok = key < sh.n_kv;
-        // query rows of step t (thread j fetches query j's statistics one
-        // step ahead, so the global loads are off the critical path)
-        auto fetch = [&](int t, float &nl, float &nd) {
-            nl = -INFINITY, nd = 0.f; // queries past n_q: p = 2^-inf = 0
+        // a statistic of query j of step t, fetched one step ahead so the
+        // global loads are off the critical path: -lse log2(e) by warps 0-3,
+        // -D by warps 4-7 (queries past n_q: p = 2^-inf = 0)
+        auto fetch = [&](int t) {
+            float v = cpart ? 0.f : -INFINITY;
             if (t < nsteps) {
-                const int bh = b * sh.Hq + hk * sh.G + t / nq_steps;
+                const size_t bh = static_cast<size_t>(b) * sh.Hq + hk * sh.G + t / nq_steps;
                 const int q = (qb0 + t % nq_steps) * BT + j;
-                if (q < sh.n_q) {
-                    nl = -lse[static_cast<size_t>(bh) * sh.n_q + q] * kLog2e;
-                    nd = -Drow[static_cast<size_t>(bh) * sh.n_q + q];
-                }
+                if (q < sh.n_q)
+                    v = cpart ? -Drow[bh * sh.n_q + q] : -lse[bh * sh.n_q + q] * kLog2e;
             }
+            return v;
         };
-        float nl, nd;
-        fetch(0, nl, nd);
+        float nv = fetch(0);
         bool ok = true;
         const uint32_t tS = tmem + lane_off + C::S_COL;
         const uint32_t tP = tmem + lane_off + C::DP_COL;
@@ -373,10 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float *rd = rl + BT;                  // -D
             // buffer t&1 was last read in step t-2; every warp has passed
             // step t-1's barrier since, so it is free
-            rl[j] = nl;
-            rd[j] = nd;
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            fetch(t + 1, nl, nd);
+            (cpart ? rd : rl)[j] = nv;
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftmaxWarps) : "memory");
+            nv = fetch(t + 1);
             // after a failed wait the warp keeps looping (and meeting the
             // named barrier above) without touching tensor memory, so that
             // its sibling warps never wait on it there
@@ -387,73 +433,77 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // query i (of the step's block) sees this key iff key <= qb*BT + i + off
             const int i_min = key - off - qb * BT; // first visible query (causal)
-            // p of queries [i0, i0 + 64) from 64 score columns, with -lse2 from rl
-            auto probs = [&](const uint32_t(&us)[64], int i0, float2(&p)[32]) {
-                const bool mask = !key_ok || (sh.causal && i_min > i0);
+            // p of queries [i0, i0 + 32) from their 32 score columns
+            auto probs = [&](const uint32_t(&us)[32], int i0, float2(&p)[16]) {
+                const float4 *l4 = reinterpret_cast<const float4 *>(rl + i0);
 #pragma unroll
-                for (int q4 = 0; q4 < 16; ++q4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(rl + i0 + 4 * q4);
+                for (int w = 0; w < 16; ++w) {
+                    const float4 l = l4[w / 2];
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(us[2 * w]), __uint_as_float(us[2 * w + 1])),
+                        c2, (w & 1) ? make_float2(l.z, l.w) : make_float2(l.x, l.y));
+                    p[w] = make_float2(ex2(x.x), ex2(x.y));
+                }
+                if (!key_ok || (sh.causal && i_min > i0)) {
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int w = 2 * q4 + hh; // element pair
-                        const float2 x = __ffma2_rn(
-                            make_float2(__uint_as_float(us[2 * w]), __uint_as_float(us[2 * w + 1])),
-                            c2, hh ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
-                        p[w] = make_float2(ex2(x.x), ex2(x.y));
-                        if (mask) {
-                            if (!key_ok || i0 + 2 * w < i_min)
-                                p[w].x = 0.f;
-                            if (!key_ok || i0 + 2 * w + 1 < i_min)
-                                p[w].y = 0.f;
-                        }
+                    for (int w = 0; w < 16; ++w) {
+                        if (!key_ok || i0 + 2 * w < i_min)
+                            p[w].x = 0.f;
+                        if (!key_ok || i0 + 2 * w + 1 < i_min)
+                            p[w].y = 0.f;
                     }
                 }
             };
-            // dS = P (dP - D); P and dS packed over the 64 dP columns read
-            auto grads = [&](const float2(&p)[32], const uint32_t(&ud)[64], int i0) {
-                uint32_t pw[32], dw[32];
+            // dS = P (dP - D); P packed over dP columns [i0, i0 + 16), dS over
+            // [i0 + 16, i0 + 32): the columns this warp has just read
+            auto grads = [&](const float2(&p)[16], const uint32_t(&ud)[32], int i0) {
+                const float4 *d4 = reinterpret_cast<const float4 *>(rd + i0);
+                uint32_t pw[16], dw[16];
 #pragma unroll
-                for (int q4 = 0; q4 < 16; ++q4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(rd + i0 + 4 * q4);
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int w = 2 * q4 + hh;
-                        const float2 g = __fadd2_rn(
-                            make_float2(__uint_as_float(ud[2 * w]), __uint_as_float(ud[2 * w + 1])),
-                            hh ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
-                        const float2 ds = __fmul2_rn(p[w], g);
-                        pw[w] = pack2<BF16>(p[w].x, p[w].y);
-                        dw[w] = pack2<BF16>(ds.x, ds.y);
-                    }
+                for (int w = 0; w < 16; ++w) {
+                    const float4 d = d4[w / 2];
+                    const float2 g = __fadd2_rn(
+                        make_float2(__uint_as_float(ud[2 * w]), __uint_as_float(ud[2 * w + 1])),
+                        (w & 1) ? make_float2(d.z, d.w) : make_float2(d.x, d.y));
+                    const float2 ds = __fmul2_rn(p[w], g);
+                    pw[w] = pack2<BF16>(p[w].x, p[w].y);
+                    dw[w] = pack2<BF16>(ds.x, ds.y);
                 }
-                tmem_st32(tP + i0, pw);
-                tmem_st32(tP + i0 + 32, dw);
+                tmem_st16(tP + i0, pw);
+                tmem_st16(tP + i0 + 16, dw);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
             };
+            // this warp's queries of the two halves: [32 c, +32) and [64 + 32 c, +32)
+            const int i0 = 32 * cpart, i1 = HS + 32 * cpart;
+            float2 p0[16], p1[16];
             {
-                // half 0: exponentials while the tensor core computes dP^T
-                uint32_t us[64], ud[64];
-                float2 p[32];
-                tmem_ld64(tS, us);
-                probs(us, 0, p);
-                if (!mbar_wait_warp(b_dp, t & 1, abort_flag, err)) {
-                    ok = false;
-                    continue;
-                }
-                tc_fence_after();
-                tmem_ld64(tP, ud);
-                grads(p, ud, 0);
+                uint32_t us0[32], us1[32];
+                tmem_ld32x2(tS + i0, us0, tS + i1, us1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(b_sfree); // the next step's S^T may overwrite them
+                probs(us0, i0, p0);
+                probs(us1, i1, p1);
+            }
+            if (!mbar_wait_warp(b_dp, t & 1, abort_flag, err)) {
+                ok = false;
+                continue;
+            }
+            tc_fence_after();
+            {
+                uint32_t ud[32];
+                tmem_ld32(tP + i0, ud);
+                grads(p0, ud, i0);
                 if (lane == 0)
                     mbar_arrive(b_pready(0));
             }
             {
-                uint32_t us[64], ud[64];
-                float2 p[32];
-                tmem_ld64x2(tS + HS, us, tP + HS, ud);
-                probs(us, HS, p);
-                grads(p, ud, HS);
+                uint32_t ud[32];
+                tmem_ld32(tP + i1, ud);
+                grads(p1, ud, i1);
                 if (lane == 0)
                     mbar_arrive(b_pready(1));
             }
@@ -465,19 +515,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // executes them; only the stores depend on the row being real
         const size_t orow = (static_cast<size_t>(bkv) * sh.n_kv + key) * D;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t uv[32], uk[32];
-            tmem_ld32(tmem + lane_off + C::ACC0 + ch * 32, uv);
-            tmem_ld32(tmem + lane_off + C::ACC1 + ch * 32, uk);
+        for (int c = cpart; c < 2 * (D / 32); c += 2) {
+            // chunks [0, D/32) of dV, then of dK (scaled)
+            const bool is_k = c >= D / 32;
+            const int ch = is_k ? c - D / 32 : c;
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_off + (is_k ? C::ACC1 : C::ACC0) + ch * 32, u);
             if (key_ok) {
-                float ov[32], ok_[32];
+                const float f = is_k ? sh.scale : 1.f;
+                float o[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    ov[i] = (ok && nsteps > 0) ? __uint_as_float(uv[i]) : 0.f;
-                    ok_[i] = (ok && nsteps > 0) ? __uint_as_float(uk[i]) * sh.scale : 0.f;
-                }
-                store32<OUT>(dV, orow + ch * 32, ov);
-                store32<OUT>(dK, orow + ch * 32, ok_);
+                for (int i = 0; i < 32; ++i)
+                    o[i] = (ok && nsteps > 0) ? __uint_as_float(u[i]) * f : 0.f;
+                store32<OUT>(is_k ? dK : dV, orow + ch * 32, o);
             }
         }
     }
@@ -493,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ========================================================================
 // dQ: one CTA per (b, query head, query block).  Step t = key block: S, dP
 // of its 128 keys, then dQ fed half by half as the softmax warps finish each
-// 64 keys (dS of half e at dP columns [64 e, 64 e + 32)).  Key blocks past
-// the last visible key are not computed.
+// 64 keys (dS of keys [64 e + 32 c, +32) at dP columns [64 e + 32 c, +16)).
+// Key blocks past the last visible key are not computed.
 template <int D, bool BF16, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -508,20 +558,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_s - raw_s);
     const uint32_t sQ = base_s + C::OFF_A, sDO = sQ + C::TILE;
-    auto sK = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE; };
-    auto sV = [&](int st) { return base_s + C::OFF_S + st * 2 * C::TILE + C::TILE; };
+    auto sK = [&](int st) { return base_s + C::OFF_X + st * C::TILE; }; // ring X
+    auto sV = [&](int st) { return base_s + C::OFF_Y + st * C::TILE; }; // ring Y
     const uint32_t bar0 = base_s + C::OFF_BAR;
     const uint32_t b_afull = bar0;
-    auto b_sfull = [&](int i) { return bar0 + 8u * (1 + i); };
-    auto b_sempty = [&](int i) { return bar0 + 8u * (1 + C::NS + i); };
-    const uint32_t b_s = bar0 + 8u * (1 + 2 * C::NS); // scores ready
+    auto b_xfull = [&](int i) { return bar0 + 8u * (1 + i); };
+    auto b_xempty = [&](int i) { return bar0 + 8u * (1 + C::NX + i); };
+    auto b_yfull = [&](int i) { return bar0 + 8u * (1 + 2 * C::NX + i); };
+    auto b_yempty = [&](int i) { return bar0 + 8u * (1 + 2 * C::NX + C::NY + i); };
+    const uint32_t b_s = bar0 + 8u * (1 + 2 * C::NX + 2 * C::NY); // scores ready
     const uint32_t b_dp = b_s + 8u;                   // second product ready
-    auto b_pready = [&](int e) { return bar0 + 8u * (3 + 2 * C::NS + e); }; // half e packed
-    const uint32_t b_done = bar0 + 8u * (5 + 2 * C::NS);
+    const uint32_t b_sfree = b_s + 16u;               // scores loaded by the softmax warps
+    auto b_pready = [&](int e) { return b_s + 8u * (3 + e); }; // half e packed
+    const uint32_t b_done = b_s + 40u;
     const uint32_t b_drain = b_done + 8u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
 
+    if (base_s - raw_s + C::SMEM_USED > static_cast<uint32_t>(C::SMEM)) {
+        if (threadIdx.x == 0)
+            atomicOr(err, DERR_INDEX); // the base needed more alignment padding than reserved
+        return;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbh = sh.B * sh.Hq;
     const int qb = sh.nqb - 1 - static_cast<int>(blockIdx.x) / nbh; // heaviest first
@@ -537,14 +595,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(b_afull, 1);
-        for (int i = 0; i < C::NS; ++i) {
-            mbar_init(b_sfull(i), 1);
-            mbar_init(b_sempty(i), 1);
+        for (int i = 0; i < C::NX; ++i) {
+            mbar_init(b_xfull(i), 1);
+            mbar_init(b_xempty(i), 1);
+        }
+        for (int i = 0; i < C::NY; ++i) {
+            mbar_init(b_yfull(i), 1);
+            mbar_init(b_yempty(i), 1);
         }
         mbar_init(b_s, 1);
         mbar_init(b_dp, 1);
+        mbar_init(b_sfree, kSoftmaxWarps);
         for (int e = 0; e < 2; ++e)
-            mbar_init(b_pready(e), 4);
+            mbar_init(b_pready(e), kSoftmaxWarps);
         mbar_init(b_done, 1);
         mbar_init(b_drain, 1);
         fence_barrier_init();
@@ -559,25 +622,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kProducerWarp) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(b_afull, 2 * C::TILE);
-            load_tile<D>(sQ, &tm_q, b_afull, qb * BT, bh);
-            load_tile<D>(sDO, &tm_do, b_afull, qb * BT, bh);
+        // lane 0: Q, dO, then the K ring; lane 1: the V ring
+        if (lane < 2) {
+            const bool is_x = lane == 0;
+            const int n = is_x ? C::NX : C::NY;
+            if (is_x) {
+                mbar_arrive_expect_tx(b_afull, 2 * C::TILE);
+                load_tile<D>(sQ, &tm_q, b_afull, qb * BT, bh);
+                load_tile<D>(sDO, &tm_do, b_afull, qb * BT, bh);
+            }
             int issued = 0;
             for (int t = 0; t < nsteps; ++t) {
-                const int st = t % C::NS;
-                if (t >= C::NS &&
-                    !mbar_wait(b_sempty(st), ((t / C::NS) - 1) & 1, abort_flag, err))
+                const int st = t % n;
+                if (t >= n && !mbar_wait(is_x ? b_xempty(st) : b_yempty(st), ((t / n) - 1) & 1,
+                                         abort_flag, err))
                     break;
-                mbar_arrive_expect_tx(b_sfull(st), 2 * C::TILE);
-                load_tile<D>(sK(st), &tm_k, b_sfull(st), t * BT, bkv);
-                load_tile<D>(sV(st), &tm_v, b_sfull(st), t * BT, bkv);
+                const uint32_t full = is_x ? b_xfull(st) : b_yfull(st);
+                mbar_arrive_expect_tx(full, C::TILE);
+                load_tile<D>(is_x ? sK(st) : sV(st), is_x ? &tm_k : &tm_v, full, t * BT, bkv);
                 issued = t + 1;
             }
             if (*abort_flag) {
-                mbar_wait_drain(b_afull, 0);
-                for (int u = max(0, issued - C::NS); u < issued; ++u)
-                    mbar_wait_drain(b_sfull(u % C::NS), (u / C::NS) & 1);
+                if (is_x)
+                    mbar_wait_drain(b_afull, 0);
+                for (int u = max(0, issued - n); u < issued; ++u)
+                    mbar_wait_drain(is_x ? b_xfull(u % n) : b_yfull(u % n), (u / n) & 1);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -586,45 +655,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_acc = idesc_f16(BT, D, BF16, false, true);
             bool ok = mbar_wait(b_afull, 0, abort_flag, err);
             if (ok && nsteps > 0)
-                ok = mbar_wait(b_sfull(0), 0, abort_flag, err);
+                ok = mbar_wait(b_xfull(0), 0, abort_flag, err) &&
+                     mbar_wait(b_yfull(0), 0, abort_flag, err);
             if (ok && nsteps > 0) {
                 tc_fence_after();
                 mma_ss_block<D>(tmem + C::S_COL, sQ, sK(0), idesc_s);
                 tc_commit(b_s);
                 mma_ss_block<D>(tmem + C::DP_COL, sDO, sV(0), idesc_s);
                 tc_commit(b_dp);
+                tc_commit(b_yempty(0)); // V is read by dP alone
             }
             for (int t = 0; ok && t < nsteps; ++t) {
-                const int st = t % C::NS, sn = (t + 1) % C::NS;
+                const int xt = t % C::NX, yt = t % C::NY;
+                const int xn = (t + 1) % C::NX, yn = (t + 1) % C::NY;
                 const bool next = t + 1 < nsteps;
+                if (next) {
+                    if (!mbar_wait(b_xfull(xn), ((t + 1) / C::NX) & 1, abort_flag, err) ||
+                        !mbar_wait(b_sfree, t & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // the softmax warps hold step t's scores in registers
+                    mma_ss_block<D>(tmem + C::S_COL, sQ, sK(xn), idesc_s);
+                    tc_commit(b_s);
+                }
                 if (!mbar_wait(b_pready(0), t & 1, abort_flag, err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 // dQ += dS K over keys 0-63 of the block
-                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL, sK(st), 0, idesc_acc,
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL, sK(xt), 0, idesc_acc,
                                    t == 0);
-                if (!mbar_wait(b_pready(1), t & 1, abort_flag, err) ||
-                    (next && !mbar_wait(b_sfull(sn), ((t + 1) / C::NS) & 1, abort_flag, err))) {
+                if (!mbar_wait(b_pready(1), t & 1, abort_flag, err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (next) {
-                    // both halves have read the scores: step t+1's may replace them
-                    mma_ss_block<D>(tmem + C::S_COL, sQ, sK(sn), idesc_s);
-                    tc_commit(b_s);
-                }
                 // the same over keys 64-127
-                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL + 64, sK(st), 1, idesc_acc,
+                mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL + 64, sK(xt), 1, idesc_acc,
                                    false);
-                tc_commit(b_sempty(st)); // step t's stage consumed
+                tc_commit(b_xempty(xt)); // step t's K consumed
                 if (next) {
+                    if (!mbar_wait(b_yfull(yn), ((t + 1) / C::NY) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     // after half 1's products, which read these columns (the
                     // tensor core runs in issue order)
-                    mma_ss_block<D>(tmem + C::DP_COL, sDO, sV(sn), idesc_s);
+                    mma_ss_block<D>(tmem + C::DP_COL, sDO, sV(yn), idesc_s);
                     tc_commit(b_dp);
+                    tc_commit(b_yempty(yn)); // V is read by dP alone
                 }
             }
             if (ok)
@@ -633,11 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_drain(b_drain, 0);
         }
     } else {
-        // ---- warps 0-3: one query row each
-        const int i = warp * 32 + lane;
+        // ---- warps 0-7: one query row each, two warps per TMEM lane
+        // quarter; warp half c takes keys [32 c, 32 c + 32) of each softmax half
+        const int quarter = warp & 3, cpart = warp >> 2;
+        const int i = quarter * 32 + lane;
         const int row = qb * BT + i;
         const bool row_ok = row < sh.n_q;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const float nl =
             row_ok ? -lse[static_cast<size_t>(bh) * sh.n_q + row] * kLog2e : -INFINITY;
         const float nd = row_ok ? -Drow[static_cast<size_t>(bh) * sh.n_q + row] : 0.f;
@@ -648,17 +733,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         const uint32_t tS = tmem + lane_off + C::S_COL;
         const uint32_t tP = tmem + lane_off + C::DP_COL;
-        // p of keys [64 e, 64 e + 64) of step t from 64 score columns
-        auto probs = [&](const uint32_t(&us)[64], int t, int e, float2(&p)[32]) {
-            const int kl = klim - (t * BT + e * HS); // last visible key within the half
-            const bool mask = kl < HS - 1;
+        // p of keys [k0, k0 + 32) of step t from their 32 score columns
+        auto probs = [&](const uint32_t(&us)[32], int t, int k0, float2(&p)[16]) {
 #pragma unroll
-            for (int w = 0; w < 32; ++w) {
+            for (int w = 0; w < 16; ++w) {
                 const float2 x = __ffma2_rn(
                     make_float2(__uint_as_float(us[2 * w]), __uint_as_float(us[2 * w + 1])), c2,
                     l2);
                 p[w] = make_float2(ex2(x.x), ex2(x.y));
-                if (mask) {
+            }
+            const int kl = klim - (t * BT + k0); // last visible key among the 32
+            if (kl < 31) {
+#pragma unroll
+                for (int w = 0; w < 16; ++w) {
                     if (2 * w > kl)
                         p[w].x = 0.f;
                     if (2 * w + 1 > kl)
@@ -666,17 +753,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         };
-        // dS = P (dP - D), packed over the first 32 of the 64 dP columns read
-        auto grads = [&](const float2(&p)[32], const uint32_t(&ud)[64], int e) {
-            uint32_t dw[32];
+        // dS = P (dP - D), packed over dP columns [k0, k0 + 16): columns this
+        // warp has just read
+        auto grads = [&](const float2(&p)[16], const uint32_t(&ud)[32], int k0) {
+            uint32_t dw[16];
 #pragma unroll
-            for (int w = 0; w < 32; ++w) {
+            for (int w = 0; w < 16; ++w) {
                 const float2 g = __fadd2_rn(
                     make_float2(__uint_as_float(ud[2 * w]), __uint_as_float(ud[2 * w + 1])), d2);
                 const float2 ds = __fmul2_rn(p[w], g);
                 dw[w] = pack2<BF16>(ds.x, ds.y);
             }
-            tmem_st32(tP + e * HS, dw);
+            tmem_st16(tP + k0, dw);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -687,28 +775,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            // this warp's keys of the two halves: [32 c, +32) and [64 + 32 c, +32)
+            const int k0 = 32 * cpart, k1 = HS + 32 * cpart;
+            float2 p0[16], p1[16];
             {
-                // half 0: exponentials while the tensor core computes dP
-                uint32_t us[64], ud[64];
-                float2 p[32];
-                tmem_ld64(tS, us);
-                probs(us, t, 0, p);
-                if (!mbar_wait_warp(b_dp, t & 1, abort_flag, err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_ld64(tP, ud);
-                grads(p, ud, 0);
+                uint32_t us0[32], us1[32];
+                tmem_ld32x2(tS + k0, us0, tS + k1, us1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(b_sfree); // the next step's S may overwrite them
+                probs(us0, t, k0, p0);
+                probs(us1, t, k1, p1);
+            }
+            if (!mbar_wait_warp(b_dp, t & 1, abort_flag, err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            {
+                uint32_t ud[32];
+                tmem_ld32(tP + k0, ud);
+                grads(p0, ud, k0);
                 if (lane == 0)
                     mbar_arrive(b_pready(0));
             }
             {
-                uint32_t us[64], ud[64];
-                float2 p[32];
-                tmem_ld64x2(tS + HS, us, tP + HS, ud);
-                probs(us, t, 1, p);
-                grads(p, ud, 1);
+                uint32_t ud[32];
+                tmem_ld32(tP + k1, ud);
+                grads(p1, ud, k1);
                 if (lane == 0)
                     mbar_arrive(b_pready(1));
             }
@@ -718,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row) * D;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
+        for (int ch = cpart; ch < D / 32; ch += 2) {
             uint32_t u[32];
             tmem_ld32(tmem + lane_off + C::ACC0 + ch * 32, u); // warp-wide
             if (row_ok) {
