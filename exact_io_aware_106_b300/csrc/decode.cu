@@ -108,39 +108,46 @@ constexpr int kMaxUnits = 256;  // units per CTA (tps <= 4096)
 constexpr int kSplitKeys = 512; // sequences shorter than this carry the P residual
 constexpr float kRescaleThreshold = 8.0f;
 
-// resident CTAs per SM; with two 16-row tiles per CTA (NRT = 2, head size
-// 64 only) every consumer thread keeps twice the accumulators
-template <int D, int NRT = 1>
+// resident CTAs per SM.  A CTA serves NRT x NG 16-row tiles: its kNC
+// consumer warps form NG groups of kNC / NG, each group takes NRT tiles and
+// every warp keeps NRT tiles' accumulators (NRT = 2 at head size 64 only,
+// where they fit; NG = 2 at head sizes 128 and 256, where the two groups
+// share each K/V copy instead)
+template <int D, int NRT = 1, int NG = 1>
 constexpr int min_ctas() {
-    static_assert(NRT == 1 || D == 64, "two row tiles per CTA at head size 64 only");
+    static_assert(NRT == 1 || D == 64, "two row tiles per warp at head size 64 only");
+    static_assert(NG == 1 || (D >= 128 && NRT == 1), "two consumer groups at head size >= 128");
     return NRT == 1 ? (D == 64 ? 4 : (D == 128 ? 3 : 2)) : 3;
 }
 
-template <int D, bool KV8, int NRT = 1>
+template <int D, bool KV8, int NRT = 1, int NG = 1>
 struct Lay {
+    static constexpr int GW = kNC / NG;  // consumer warps per group
+    static constexpr int NTC = NRT * NG; // row tiles per CTA
     static constexpr int ROWB = KV8 ? D : 2 * D;          // bytes of one cache row
     static constexpr int PW = ROWB < 128 ? ROWB : 128;     // row bytes per panel = swizzle span
     static constexpr int PANELS = ROWB / PW;
     static constexpr int PANEL_BYTES = kUnit * PW;         // one TMA box
     static constexpr int HALF = PANELS * PANEL_BYTES;      // K (or V) of one unit
     static constexpr int STAGE = 2 * HALF;
-    // Unit u lives in stage u % NST and is consumed by warp u % kNC.  With
-    // NST a multiple of kNC a stage is only ever consumed by one warp, so
-    // that warp has itself waited for the stage's previous phase before it
-    // waits (by parity) for the next one; otherwise a warp could wait on a
-    // stage whose previous fill, for another warp, has not landed yet, and
-    // the parity test would pass one phase early.
+    // Unit u lives in stage u % NST and is consumed by warp u % GW of every
+    // group.  With NST a multiple of GW a stage is only ever consumed by the
+    // same warp of each group, so that warp has itself waited for the
+    // stage's previous phase before it waits (by parity) for the next one;
+    // otherwise a warp could wait on a stage whose previous fill, for another
+    // warp, has not landed yet, and the parity test would pass one phase
+    // early.
     static constexpr int NST = KV8 ? (D == 64 ? 24 : (D == 128 ? 16 : 8))
                                    : (D == 64 ? 12 : (D == 128 ? 8 : 4));
-    static_assert(NST % kNC == 0, "each stage must belong to one consumer warp");
-    static constexpr int MIN_CTAS = min_ctas<D, NRT>();
+    static_assert(NST % GW == 0, "each stage must belong to one consumer warp per group");
+    static constexpr int MIN_CTAS = min_ctas<D, NRT, NG>();
     static constexpr int QROW = 2 * D + 16;                // padded q row (16-bit caches)
     static constexpr int QBYTES1 = KV8 ? (D / 16) * 32 * 16 : 16 * QROW; // one row tile
-    static constexpr int QBYTES = NRT * QBYTES1;
+    static constexpr int QBYTES = NTC * QBYTES1;
     static constexpr int RING = NST * STAGE;
-    static constexpr int MERGE_U = kNC * 16 * D * 4;
-    static constexpr int MERGE = MERGE_U + kNC * 16 * 8;
-    static constexpr int OFF_Q = RING > MERGE ? RING : MERGE;
+    static constexpr int MERGE_U = GW * 16 * D * 4;
+    static constexpr int MERGE = MERGE_U + GW * 16 * 8; // one group's merge area
+    static constexpr int OFF_Q = RING > NG * MERGE ? RING : NG * MERGE;
     static constexpr int OFF_BLK = OFF_Q + QBYTES;
     static constexpr int OFF_BAR = OFF_BLK + kMaxUnits * 4;
     static constexpr int SMEM = OFF_BAR + 2 * NST * 8 + 16 + 1024; // + alignment slack
@@ -189,8 +196,8 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
-template <int D, bool QBF16, bool KV8, int NRT>
-__global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
+template <int D, bool QBF16, bool KV8, int NRT, int NG>
+__global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT, NG>::MIN_CTAS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const void *__restrict__ q_,
                       const int32_t *__restrict__ block_table,
@@ -200,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
                       int max_blocks,
                       int num_blocks, int max_seq_len, int tps, int max_splits, float c,
                       unsigned *err) {
-    using Ly = Lay<D, KV8, NRT>;
+    using Ly = Lay<D, KV8, NRT, NG>;
+    constexpr int NTC = Ly::NTC, GW = Ly::GW;
     constexpr bool MB = KV8 ? false : QBF16; // operand format of the MMAs (bf16 or f16)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -213,9 +221,9 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
     auto b_empty = [&](int i) { return bar0 + 8u * (Ly::NST + i); };
     __shared__ int s_flag; // 1 = bad index, 2 = aborted
     __shared__ int s_abort;
-    __shared__ int s_amax[NRT]; // max |q| of each row tile as float bits (E4M3 caches)
+    __shared__ int s_amax[NTC]; // max |q| of each row tile as float bits (E4M3 caches)
 
-    // x = (split, group of NRT row tiles): the groups of one split are
+    // x = (split, group of NTC row tiles): the groups of one split are
     // adjacent, so the K/V they all stream is read from DRAM about once
     const int split = blockIdx.x / ngrp, grp = blockIdx.x % ngrp;
     const int hk = blockIdx.y, s = blockIdx.z;
@@ -236,11 +244,11 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
     const int head0 = hk * G;
     // rows of the group: r = g * T + i for head head0 + g and new token i
     // (q [num_seqs, Hq, T, d], so a group's rows are contiguous); this CTA
-    // takes the NRT 16-row tiles [row0 + 16 rt, row0 + 16 rt + 16) of them
-    const int row0 = 16 * NRT * grp;
-    int R[NRT]; // real rows of each tile
+    // takes the NTC 16-row tiles [row0 + 16 rt, row0 + 16 rt + 16) of them
+    const int row0 = 16 * NTC * grp;
+    int R[NTC]; // real rows of each tile
 #pragma unroll
-    for (int rt = 0; rt < NRT; ++rt)
+    for (int rt = 0; rt < NTC; ++rt)
         R[rt] = max(0, min(16, G * T - row0 - 16 * rt));
     const uint16_t *qg = static_cast<const uint16_t *>(q_) +
                          ((static_cast<size_t>(s) * Hq + head0) * T + row0) * D;
@@ -249,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
         s_flag = 0;
         s_abort = 0;
 #pragma unroll
-        for (int rt = 0; rt < NRT; ++rt)
+        for (int rt = 0; rt < NTC; ++rt)
             s_amax[rt] = 0;
     }
     __syncthreads();
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
     }
     if constexpr (!KV8) {
         // the tiles' query rows, zero rows up to 16 per tile, padded rows
-        for (int i = threadIdx.x; i < NRT * 16 * (D / 8); i += kThreads) {
+        for (int i = threadIdx.x; i < NTC * 16 * (D / 8); i += kThreads) {
             const int r = i / (D / 8), c8 = i % (D / 8); // r = 16 rt + row in tile
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if ((r & 15) < R[r >> 4])
@@ -271,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
         }
     } else {
 #pragma unroll
-        for (int rt = 0; rt < NRT; ++rt) {
+        for (int rt = 0; rt < NTC; ++rt) {
             float amax = 0.f;
             for (int i = threadIdx.x; i < R[rt] * D; i += kThreads) {
                 const uint16_t x16 = qg[static_cast<size_t>(16 * rt) * D + i];
@@ -286,26 +294,26 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
     if (threadIdx.x == 0) {
         for (int i = 0; i < Ly::NST; ++i) {
             mbar_init(b_full(i), 1);    // producer arrive + tx bytes
-            mbar_init(b_empty(i), 1);   // the consuming warp (it serves every row tile)
+            mbar_init(b_empty(i), NG);  // one consuming warp per group
         }
         fence_barrier_init();
     }
     __syncthreads();
     // power-of-two scale that keeps the f16 copy of each tile's q in range
-    float qs[NRT];
+    float qs[NTC];
 #pragma unroll
-    for (int rt = 0; rt < NRT; ++rt)
+    for (int rt = 0; rt < NTC; ++rt)
         qs[rt] = 1.0f;
     if constexpr (KV8) {
 #pragma unroll
-        for (int rt = 0; rt < NRT; ++rt) {
+        for (int rt = 0; rt < NTC; ++rt) {
             const float amax = __int_as_float(s_amax[rt]);
             if (amax > 0.f && isfinite(amax))
                 qs[rt] = exp2f(14.0f - floorf(log2f(amax)));
         }
         // q as f16 in the permuted fragment order: chunk ch, lane (g, t) gets
         // {(g, 4t..4t+1), (g+8, 4t..4t+1), (g, 4t+2..4t+3), (g+8, 4t+2..4t+3)}
-        for (int i = threadIdx.x; i < NRT * (D / 16) * 32; i += kThreads) {
+        for (int i = threadIdx.x; i < NTC * (D / 16) * 32; i += kThreads) {
             const int rt = i / ((D / 16) * 32), ii = i % ((D / 16) * 32);
             const int ch = ii >> 5, ln = ii & 31, gg = ln >> 2, tt = ln & 3;
             uint32_t w[4];
@@ -334,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
     if (s_flag) {
         if (threadIdx.x == 0)
             atomicOr(err, DERR_INDEX);
-        for (int r = threadIdx.x; r < NRT * 16; r += kThreads)
+        for (int r = threadIdx.x; r < NTC * 16; r += kThreads)
             if ((r & 15) < R[r >> 4])
                 ws_ml[((static_cast<size_t>(s) * Hq + head0) * T + row0 + r) * max_splits +
                       split] = make_float2(0.f, -1.f); // l < 0 marks an unusable partial
@@ -375,13 +383,17 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
     }
 
     // ---------------------------------------------------- consumer warps
+    // group gi (warps GW gi .. GW gi + GW - 1) takes the row tiles
+    // [NRT gi, NRT gi + NRT) of the CTA; warp wl of a group the units
+    // wl, wl + GW, ...  (every group streams every unit)
+    const int gi = warp / GW, wl = warp % GW, rt0 = gi * NRT;
     const int g = lane >> 2, t = lane & 3;
     const int mj = lane >> 3, mr = lane & 7; // ldmatrix: matrix index, row
     const bool split_p = len < kSplitKeys;
     float cq[NRT];
 #pragma unroll
     for (int rt = 0; rt < NRT; ++rt)
-        cq[rt] = KV8 ? c * k_scale[hk] / qs[rt] : c;
+        cq[rt] = KV8 ? c * k_scale[hk] / qs[rt0 + rt] : c;
 
     float o[NRT][D / 8][4];
     float m[NRT][2], l[NRT][2];
@@ -395,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
     }
     bool ok = true;
 
-    for (int u = warp; u < nunits; u += kNC) {
+    for (int u = wl; u < nunits; u += GW) {
         const int st = u % Ly::NST;
         if (!mbar_wait_warp(b_full(st), (u / Ly::NST) & 1, abort_flag, err)) {
             ok = false;
@@ -437,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
 #pragma unroll
                 for (int rt = 0; rt < NRT; ++rt) {
                     uint32_t a[4];
-                    ldsm_x4(a, q_lane + rt * 16 * Ly::QROW + kc * 32);
+                    ldsm_x4(a, q_lane + (rt0 + rt) * 16 * Ly::QROW + kc * 32);
                     mma16816<MB>(s0[rt], a, b[0], b[1]);
                     mma16816<MB>(s1[rt], a, b[2], b[3]);
                 }
@@ -455,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
                 const uint32_t kb30 = e4m3x2_f16x2(b[3]), kb31 = e4m3x2_f16x2(b[3] >> 16);
 #pragma unroll
                 for (int rt = 0; rt < NRT; ++rt) {
-                    const uint32_t qt = sQ + rt * Ly::QBYTES1;
+                    const uint32_t qt = sQ + (rt0 + rt) * Ly::QBYTES1;
                     const uint4 q0 = lds128(qt + ((2 * cp) * 32 + lane) * 16);
                     const uint4 q1 = lds128(qt + ((2 * cp + 1) * 32 + lane) * 16);
                     const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
@@ -484,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
             }
             if (T > 1 && t0 + u * kUnit + kUnit - 1 > len - T) {
                 // new token i sees cached token p iff p <= len - T + i (bottom-right)
-                const int rb = row0 + 16 * rt;
+                const int rb = row0 + 16 * (rt0 + rt);
                 const int lim0 = len - T + ((rb + g) % T), lim1 = len - T + ((rb + g + 8) % T);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -608,26 +620,30 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
     if (!ok)
         s_flag = 2;
 
-    // ---- merge the consumer warps' states, one row tile at a time (the
-    // ring is drained: every issued unit was consumed before its consumer
-    // reached this barrier)
-    float *mrg_u = reinterpret_cast<float *>(base);                  // [kNC][16][D]
-    float2 *mrg_ml = reinterpret_cast<float2 *>(base + Ly::MERGE_U); // [kNC][16]
+    // ---- merge each group's warp states, one row tile at a time, in the
+    // group's own area over the ring.  The ring is drained once every
+    // consumer warp of every group has reached the first barrier (every
+    // issued unit was consumed before its consumers got there).
+    asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
+    float *mrg_u = reinterpret_cast<float *>(base + gi * Ly::MERGE);                  // [GW][16][D]
+    float2 *mrg_ml = reinterpret_cast<float2 *>(base + gi * Ly::MERGE + Ly::MERGE_U); // [GW][16]
     const float vsc = KV8 ? v_scale[hk] : 1.0f;
+    const int gtid = threadIdx.x - gi * GW * 32; // thread within the group
 #pragma unroll
     for (int rt = 0; rt < NRT; ++rt) {
-        asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
-        const int Rt = R[rt];
+        if (rt > 0) // the previous tile's merge reads are done
+            asm volatile("bar.sync %0, %1;" ::"r"(2 + gi), "r"(GW * 32) : "memory");
+        const int Rt = R[rt0 + rt];
         if constexpr (!KV8) {
             // n-tile n, column 2t + e  <->  d = 8 n + 2 t + e
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) {
                 const int col = n * 8 + 2 * t;
                 if (g < Rt)
-                    *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g) * D + col) =
+                    *reinterpret_cast<float2 *>(mrg_u + (wl * 16 + g) * D + col) =
                         make_float2(o[rt][n][0], o[rt][n][1]);
                 if (g + 8 < Rt)
-                    *reinterpret_cast<float2 *>(mrg_u + (warp * 16 + g + 8) * D + col) =
+                    *reinterpret_cast<float2 *>(mrg_u + (wl * 16 + g + 8) * D + col) =
                         make_float2(o[rt][n][2], o[rt][n][3]);
             }
         } else {
@@ -637,37 +653,37 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT>::MIN_CTAS)
             for (int ch = 0; ch < D / 16; ++ch) {
                 const int col = ch * 16 + 4 * t;
                 if (g < Rt)
-                    *reinterpret_cast<float4 *>(mrg_u + (warp * 16 + g) * D + col) =
+                    *reinterpret_cast<float4 *>(mrg_u + (wl * 16 + g) * D + col) =
                         make_float4(o[rt][2 * ch][0], o[rt][2 * ch + 1][0], o[rt][2 * ch][1],
                                     o[rt][2 * ch + 1][1]);
                 if (g + 8 < Rt)
-                    *reinterpret_cast<float4 *>(mrg_u + (warp * 16 + g + 8) * D + col) =
+                    *reinterpret_cast<float4 *>(mrg_u + (wl * 16 + g + 8) * D + col) =
                         make_float4(o[rt][2 * ch][2], o[rt][2 * ch + 1][2], o[rt][2 * ch][3],
                                     o[rt][2 * ch + 1][3]);
             }
         }
         if (t == 0) {
-            mrg_ml[warp * 16 + g] = make_float2(m[rt][0], l[rt][0]);
-            mrg_ml[warp * 16 + g + 8] = make_float2(m[rt][1], l[rt][1]);
+            mrg_ml[wl * 16 + g] = make_float2(m[rt][0], l[rt][0]);
+            mrg_ml[wl * 16 + g + 8] = make_float2(m[rt][1], l[rt][1]);
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kNC * 32) : "memory");
+        asm volatile("bar.sync %0, %1;" ::"r"(2 + gi), "r"(GW * 32) : "memory");
         const bool bad = s_flag != 0;
-        for (int idx = threadIdx.x; idx < Rt * D; idx += kNC * 32) {
+        for (int idx = gtid; idx < Rt * D; idx += GW * 32) {
             const int r = idx / D, e = idx % D;
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kNC; ++w)
+            for (int w = 0; w < GW; ++w)
                 M = fmaxf(M, mrg_ml[w * 16 + r].x);
             float Lsum = 0.f, U = 0.f;
 #pragma unroll
-            for (int w = 0; w < kNC; ++w) {
+            for (int w = 0; w < GW; ++w) {
                 const float2 ml = mrg_ml[w * 16 + r];
                 const float sc = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
                 Lsum += sc * ml.y;
                 U += sc * mrg_u[(w * 16 + r) * D + e];
             }
             const size_t o_idx =
-                ((static_cast<size_t>(s) * Hq + head0) * T + row0 + 16 * rt + r) * max_splits +
+                ((static_cast<size_t>(s) * Hq + head0) * T + row0 + 16 * (rt0 + rt) + r) * max_splits +
                 split;
             ws_u[o_idx * D + e] = U * vsc;
             if (e == 0)
@@ -713,19 +729,21 @@ static cudaError_t launch_combine(const DecodeArgs &a, const float2 *ws_ml, cons
 // 16-row tiles of a KV head's query rows (G x n_new of them)
 static int decode_row_tiles(const DecodeArgs &a) { return (a.Hq / a.Hkv * a.T + 15) / 16; }
 
-// Row tiles per CTA: two at head size 64 when they pair up, so that each
-// K/V copy and fragment serves both (MQA G = 32 at d = 64: 0.125 -> 0.096
-// ms); at d = 128 the doubled accumulators leave room for one CTA per SM and
-// separate CTAs per tile are faster.
+// Row tiles per CTA: two when they pair up, so that each K/V copy serves
+// both.  At head size 64 one warp takes both tiles (each K/V fragment serves
+// both; MQA G = 32: 0.125 -> 0.096 ms); at 128 and 256 the doubled
+// accumulators would leave room for one CTA per SM (measured slower at
+// 128), so the consumer warps split into two groups of two, one per tile,
+// sharing the copy (spec-decode-8 at 128: 1.127 -> 0.757 ms).
 template <int D>
 static int decode_tiles_per_cta(const DecodeArgs &a) {
-    return (D == 64 && decode_row_tiles(a) % 2 == 0) ? 2 : 1;
+    return decode_row_tiles(a) % 2 == 0 ? 2 : 1;
 }
 
-template <int D, bool QBF16, bool KV8, int NRT>
+template <int D, bool QBF16, bool KV8, int NRT, int NG>
 static cudaError_t launch_mma(const DecodeArgs &a, float2 *ws_ml, float *ws_u, int tps,
                               int max_splits, cudaStream_t st) {
-    using Ly = dm::Lay<D, KV8, NRT>;
+    using Ly = dm::Lay<D, KV8, NRT, NG>;
     // cache [num_blocks, Hkv, block_size, D] viewed as {D, Hkv * block_size, num_blocks}
     const uint64_t esz = KV8 ? 1 : 2;
     const uint64_t dims[3] = {static_cast<uint64_t>(D),
@@ -739,12 +757,12 @@ static cudaError_t launch_mma(const DecodeArgs &a, float2 *ws_ml, float *ws_u, i
     if (!make_tmap_3d(&mk, a.Kc, el, dims, strides, box, Ly::PW) ||
         !make_tmap_3d(&mv, a.Vc, el, dims, strides, box, Ly::PW))
         return cudaErrorInvalidValue;
-    auto kern = dm::decode_mma_kernel<D, QBF16, KV8, NRT>;
+    auto kern = dm::decode_mma_kernel<D, QBF16, KV8, NRT, NG>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
     if (e != cudaSuccess)
         return e;
-    const int ngrp = decode_row_tiles(a) / NRT; // CTAs per (split, KV head, sequence)
+    const int ngrp = decode_row_tiles(a) / Ly::NTC; // CTAs per (split, KV head, sequence)
     dim3 grid(max_splits * ngrp, a.Hkv, a.num_seqs);
     kern<<<grid, dm::kThreads, Ly::SMEM, st>>>(
         mk, mv, a.q, a.block_table, a.seq_lens, a.k_scale, a.v_scale, ws_ml, ws_u, a.Hq,
@@ -772,30 +790,35 @@ static int choose_tps(const DecodeArgs &a, int resident_per_sm, int tiles_per_ct
 
 template <int D>
 static cudaError_t decode_d(const DecodeArgs &a, cudaStream_t st) {
-    const int nrt = decode_tiles_per_cta<D>(a);
+    const int ntc = decode_tiles_per_cta<D>(a);
     int resident = dm::min_ctas<D, 1>();
     if constexpr (D == 64)
-        resident = nrt == 2 ? dm::min_ctas<D, 2>() : resident;
-    const int tps = choose_tps(a, resident, nrt);
+        resident = ntc == 2 ? dm::min_ctas<D, 2, 1>() : resident;
+    if constexpr (D >= 128)
+        resident = ntc == 2 ? dm::min_ctas<D, 1, 2>() : resident;
+    const int tps = choose_tps(a, resident, ntc);
     const int max_splits = max(1, (a.max_seq_len + tps - 1) / tps);
     const size_t n = static_cast<size_t>(a.num_seqs) * a.Hq * a.T * max_splits;
     size_t ml_bytes = (n * sizeof(float2) + 255) & ~static_cast<size_t>(255);
     float2 *ws_ml = static_cast<float2 *>(a.workspace);
     float *ws_u = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + ml_bytes);
     cudaError_t e;
-    auto run = [&](auto nrt_c) -> cudaError_t {
-        constexpr int NRT = decltype(nrt_c)::value;
+    auto run = [&](auto nrt_c, auto ng_c) -> cudaError_t {
+        constexpr int NRT = decltype(nrt_c)::value, NG = decltype(ng_c)::value;
         if (a.kv_e4m3)
-            return a.q_bf16 ? launch_mma<D, true, true, NRT>(a, ws_ml, ws_u, tps, max_splits, st)
-                            : launch_mma<D, false, true, NRT>(a, ws_ml, ws_u, tps, max_splits,
-                                                               st);
-        return a.q_bf16 ? launch_mma<D, true, false, NRT>(a, ws_ml, ws_u, tps, max_splits, st)
-                        : launch_mma<D, false, false, NRT>(a, ws_ml, ws_u, tps, max_splits, st);
+            return a.q_bf16
+                       ? launch_mma<D, true, true, NRT, NG>(a, ws_ml, ws_u, tps, max_splits, st)
+                       : launch_mma<D, false, true, NRT, NG>(a, ws_ml, ws_u, tps, max_splits, st);
+        return a.q_bf16
+                   ? launch_mma<D, true, false, NRT, NG>(a, ws_ml, ws_u, tps, max_splits, st)
+                   : launch_mma<D, false, false, NRT, NG>(a, ws_ml, ws_u, tps, max_splits, st);
     };
+    using I1 = std::integral_constant<int, 1>;
+    using I2 = std::integral_constant<int, 2>;
     if constexpr (D == 64)
-        e = nrt == 2 ? run(std::integral_constant<int, 2>{}) : run(std::integral_constant<int, 1>{});
+        e = ntc == 2 ? run(I2{}, I1{}) : run(I1{}, I1{});
     else
-        e = run(std::integral_constant<int, 1>{});
+        e = ntc == 2 ? run(I1{}, I2{}) : run(I1{}, I1{});
     if (e != cudaSuccess)
         return e;
     switch (a.out_dtype) {
