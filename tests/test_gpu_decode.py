@@ -29,6 +29,8 @@ CASES = [
     (3, 32, 1, 64, 16, [1, 777, 3000], "bf16"),              # d = 64, G = 32: one CTA, two tiles
     (2, 40, 1, 64, 32, [100, 2500], "f16"),                  # G = 40: three tiles, last ragged
     (2, 64, 1, 256, 16, [17, 1200], "bf16"),                 # G = 64: four tiles
+    (2, 32, 1, 128, 16, [900, 33], "f16"),                   # f16, two consumer groups
+    (2, 48, 2, 128, 16, [31, 2222], "bf16"),                 # G = 24: two tiles, 8-row tail
 ]
 
 
@@ -51,7 +53,9 @@ def test_decode_small(case):
 
 
 @pytest.mark.parametrize("d,G", [(d, G) for d in (64, 128, 256) for G in (1, 4, 8, 16)] +
-                         [(64, 32)])  # d = 64, G = 32: one CTA serving two row tiles
+                         [(64, 32),    # d = 64, G = 32: one warp serving two row tiles
+                          (128, 32),   # two consumer groups, one row tile each
+                          (256, 32)])
 def test_decode_e4m3(d, G):
     spec = W.DecodeSpec(3, 2 * G, 2, d, 1, 2000, 16, "bf16", "e4m3", "bf16")
     t = W.make_decode(spec, seed=2, lens=[2000, 1500, 37], keep_unquantised=True)
