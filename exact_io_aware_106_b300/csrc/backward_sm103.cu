@@ -84,52 +84,74 @@ struct Shape {
     float c, scale;
 };
 
-// D_i = sum_c dO_ic O_ic (fp32), one warp per row; O in the inputs' 16-bit
-// format or in fp32 (OF32).
+// D_i = sum_c dO_ic O_ic (fp32); O in the inputs' 16-bit format or in fp32
+// (OF32).  Each thread takes 8 elements of a row with 16-byte loads (D / 8
+// lanes per row), and each warp PREP_UNROLL groups of 32 / (D / 8) rows, all
+// loads issued before the arithmetic so that several are in flight.
+constexpr int PREP_UNROLL = 4;
+template <int D>
+constexpr long long prep_rows_per_block() {
+    return 8LL * (32 / (D / 8)) * PREP_UNROLL; // 8 warps per 256-thread block
+}
 template <int D, bool BF16, bool OF32>
 __global__ void __launch_bounds__(256)
     bwd_prep_kernel(const void *__restrict__ O_, const uint16_t *__restrict__ dO,
                     float *__restrict__ Drow, long long rows) {
-    const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (r >= rows)
-        return;
-    constexpr int EPL = D / 32; // 2 or 4 elements per lane
-    const uint16_t *g = dO + r * D + lane * EPL;
-    float gv[EPL], ov[EPL];
-    if constexpr (EPL == 2) {
-        const uint32_t b = *reinterpret_cast<const uint32_t *>(g);
-        gv[0] = lo16<BF16>(b), gv[1] = hi16<BF16>(b);
-    } else {
-        const uint2 b = *reinterpret_cast<const uint2 *>(g);
-        gv[0] = lo16<BF16>(b.x), gv[1] = hi16<BF16>(b.x), gv[2] = lo16<BF16>(b.y),
-        gv[3] = hi16<BF16>(b.y);
-    }
-    if constexpr (OF32) {
-        const float *o = static_cast<const float *>(O_) + r * D + lane * EPL;
+    constexpr int LPR = D / 8;   // lanes per row
+    constexpr int RPW = 32 / LPR; // rows per warp and group
+    const int lane = threadIdx.x & 31, sub = lane / LPR, c = lane % LPR;
+    const long long r0 = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RPW *
+                         PREP_UNROLL;
+    uint4 g[PREP_UNROLL], o[PREP_UNROLL][OF32 ? 2 : 1];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e)
-            ov[e] = o[e];
-    } else {
-        const uint16_t *o = static_cast<const uint16_t *>(O_) + r * D + lane * EPL;
-        if constexpr (EPL == 2) {
-            const uint32_t a = *reinterpret_cast<const uint32_t *>(o);
-            ov[0] = lo16<BF16>(a), ov[1] = hi16<BF16>(a);
-        } else {
-            const uint2 a = *reinterpret_cast<const uint2 *>(o);
-            ov[0] = lo16<BF16>(a.x), ov[1] = hi16<BF16>(a.x), ov[2] = lo16<BF16>(a.y),
-            ov[3] = hi16<BF16>(a.y);
+    for (int u = 0; u < PREP_UNROLL; ++u) {
+        const long long r = r0 + u * RPW + sub;
+        g[u] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int h = 0; h < (OF32 ? 2 : 1); ++h)
+            o[u][h] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows) {
+            g[u] = *reinterpret_cast<const uint4 *>(dO + r * D + c * 8);
+            if constexpr (OF32) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    static_cast<const float *>(O_) + r * D + c * 8);
+                o[u][0] = src[0];
+                o[u][1] = src[1];
+            } else {
+                o[u][0] = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(O_) +
+                                                          r * D + c * 8);
+            }
         }
     }
-    float acc = 0.f;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e)
-        acc = fmaf(gv[e], ov[e], acc);
+    for (int u = 0; u < PREP_UNROLL; ++u) {
+        const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+        float ov[8];
+        if constexpr (OF32) {
+            const uint32_t w[8] = {o[u][0].x, o[u][0].y, o[u][0].z, o[u][0].w,
+                                   o[u][1].x, o[u][1].y, o[u][1].z, o[u][1].w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0)
-        Drow[r] = acc;
+            for (int e = 0; e < 8; ++e)
+                ov[e] = __uint_as_float(w[e]);
+        } else {
+            const uint32_t w[4] = {o[u][0].x, o[u][0].y, o[u][0].z, o[u][0].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                ov[2 * e] = lo16<BF16>(w[e]), ov[2 * e + 1] = hi16<BF16>(w[e]);
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(lo16<BF16>(gw[e]), ov[2 * e], acc);
+            acc = fmaf(hi16<BF16>(gw[e]), ov[2 * e + 1], acc);
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const long long r = r0 + u * RPW + sub;
+        if (c == 0 && r < rows)
+            Drow[r] = acc;
+    }
 }
 
 // Loads one 128-row tile of a [d, n, bh] tensor map (all d/64 panels).
@@ -876,11 +898,13 @@ static cudaError_t backward_t(const BackwardArgs &a, cudaStream_t st) {
     sh.scale = a.scale;
     float *Drow = static_cast<float *>(a.workspace);
     const long long rows = static_cast<long long>(a.B) * a.Hq * a.n_q;
+    const unsigned prep_grid = static_cast<unsigned>((rows + bw::prep_rows_per_block<D>() - 1) /
+                                                     bw::prep_rows_per_block<D>());
     if (a.o_f32)
-        bw::bwd_prep_kernel<D, BF16, true><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+        bw::bwd_prep_kernel<D, BF16, true><<<prep_grid, 256, 0, st>>>(
             a.O, static_cast<const uint16_t *>(a.dO), Drow, rows);
     else
-        bw::bwd_prep_kernel<D, BF16, false><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+        bw::bwd_prep_kernel<D, BF16, false><<<prep_grid, 256, 0, st>>>(
             a.O, static_cast<const uint16_t *>(a.dO), Drow, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
