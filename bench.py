@@ -667,6 +667,15 @@ def run_reference(args):
 
 # ------------------------------------------------------------------- main
 
+def max_over_ranks(values, device):
+    """Elementwise maximum of `values` over the ranks of the default process
+    group (the job's time is its slowest rank's); NCCL on the GPU, gloo on
+    the CPU in the tests."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -714,9 +723,7 @@ def main():
     t_e2e = res["t_e2e"] if res["t_e2e"] is not None else float("nan")
     roof_total = res["roof_step"]
     if world > 1:
-        t = torch.tensor([t_step, t_e2e], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_step, t_e2e = float(t[0]), float(t[1])
+        t_step, t_e2e = max_over_ranks([t_step, t_e2e], "cuda")
         roof_total = res["roof_step"] * world
     pk = res["peaks"]
     if rank == 0:
