@@ -299,7 +299,9 @@ def run_ours(args, rank, world):
     Bp = prefill_bytes(PREFILL)
     Bd = decode_bytes(DECODE, lens)
     Ba = append_bytes(DECODE)
-    P = pk["bf16_tflops_sustained"] * 1e12
+    # the dense bf16 peak as a burst: the timed region is well under a second,
+    # far shorter than the seconds-long loop the sustained figure comes from
+    P = pk["bf16_tflops"] * 1e12
     BW = pk["hbm_gbs"] * 1e9
     roof_pre = max(F / P, Bp / BW) if do_pre else 0.0
     roof_dec = max(decode_flops(DECODE, lens) / P, Bd / BW) if do_dec else 0.0
@@ -622,7 +624,7 @@ def oracle_sample(threads: int, rows: int, seqs: int, seed: int = 0):
 
 
 def oracle_values(smp, pk):
-    P = pk["bf16_tflops_sustained"] * 1e12
+    P = pk["bf16_tflops"] * 1e12
     BW = pk["hbm_gbs"] * 1e9
     roof = smp["F"] / P + smp["Bd"] / BW
     return {"pct": 100.0 * roof / (smp["t_pre"] + smp["t_dec"]),
@@ -760,10 +762,10 @@ def main():
                 "first_call_ms": res["first_call"].get("prefill_ms")}
             line["roofline"] = {
                 "bound": "tensor", "kernel": "prefill_kernel<128,bf16,bf16>",
-                "achieved": round(pre_tflops, 2), "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": round(pre_tflops / pk["bf16_tflops_sustained"], 4),
-                "frac_of_burst": round(pre_tflops / pk["bf16_tflops"], 4),
-                "peak_kind": f"{pk['source']} sustained bf16 (kernel timed inside the step)",
+                "achieved": round(pre_tflops, 2), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(pre_tflops / pk["bf16_tflops"], 4),
+                "frac_of_sustained": round(pre_tflops / pk["bf16_tflops_sustained"], 4),
+                "peak_kind": f"{pk['source']} burst bf16 (sub-second timed region)",
                 "traffic": res["traffic"]}
         if dec_gbs is not None:
             line["decode"] = {

@@ -9,8 +9,9 @@
 // the max, u += P V, and u / l is written once at the end.  The full score
 // matrix never leaves the SM.  Normalisation is deferred to the end of the
 // loop (the FA2 scheduling on the same page), causal tiles entirely in the
-// future are skipped (page 5, causal masking), and query head h reads KV
-// head h / G (code-journey.com "Attention co-design", Group Size).
+// future are skipped (the same page's section on causal masking), and query
+// head h reads KV head h / G (code-journey.com "Attention co-design", Group
+// Size).
 //
 // B300 mapping (one CTA = 2 query tiles of 128 rows = 256 rows of one head):
 //   warp 8      TMA producer: Q tiles once, then K_j / V_j through rings of
@@ -46,6 +47,8 @@
 // <= 2^8.  u / l does not depend on which reference value is subtracted
 // (the max-subtraction invariance of §8); keeping a slightly stale one
 // avoids most O rescales.
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -1344,13 +1347,17 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
     const pf::Scales sc{a.q_scale, a.k_scale, a.v_scale};
     auto kern = pf::prefill_kernel<D, BF16, F8, PAGED, OUT>;
     // the in-kernel register split adds up only if the kernel launches with
-    // exactly kLaunchRegs registers per thread; never launch it otherwise
-    static int regs = -1;
+    // exactly kLaunchRegs registers per thread; never launch it otherwise.
+    // The count is looked up once per instance; concurrent callers may race
+    // to store the same value, which the atomic makes well defined.
+    static std::atomic<int> regs_cache{-1};
+    int regs = regs_cache.load(std::memory_order_relaxed);
     if (regs < 0) {
         cudaFuncAttributes fa;
         if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
             return cudaErrorInvalidDeviceFunction;
         regs = fa.numRegs;
+        regs_cache.store(regs, std::memory_order_relaxed);
     }
     if (regs != pf::kLaunchRegs)
         return cudaErrorInvalidConfiguration;

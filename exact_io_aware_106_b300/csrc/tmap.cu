@@ -1,6 +1,8 @@
 // tmap.cu -- host-side construction of TMA tensor maps (cuTensorMapEncodeTiled
 // reached through the runtime's driver entry-point query, so the library
 // needs no libcuda at link time).
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -52,18 +54,19 @@ bool make_tmap_3d_16bit(CUtensorMap *m, const void *ptr, bool bf16, const uint64
 }
 
 int sm_count() {
-    static int cache[64] = {0};
+    // per-device cache; threads that race store the same value
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return 148;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             n <= 0)
             n = 148;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 } // namespace attn

@@ -5,8 +5,12 @@
 * 16-bit outputs: the same 2e-3 plus half a unit in the last place of the
   output format at |O_ref| -- the rounding of a correct result to the output
   format alone can exceed 2e-3 when |O| > 0.5 (a causal row 0 returns V[0]).
-* lse: |lse_gpu - lse_ref| <= 1e-4 * max(1, |lse_ref|) (relative, with an
-  absolute floor where lse is near 0).
+* lse: |lse_gpu - lse_ref| <= 1e-4 * max(0.1, |lse_ref|): 1e-4 relative,
+  with an absolute floor of 1e-5 where |lse| < 0.1.  A purely relative gate
+  is ill-posed at lse = 0 (a causal row 0 or a one-token sequence has
+  lse = its single scaled score, which can be arbitrarily close to 0), and
+  the fp32 evaluation m + ln l carries an absolute error of a few 1e-7 from
+  m and l alone; the floor is a deliberate departure from "relative".
 * E4M3 KV: 3e-2 max-abs against the oracle fed the unquantised values, and
   the 16-bit rule against the oracle fed the dequantised values.
 """
@@ -16,6 +20,7 @@ import torch
 ATOL = 2e-3
 ATOL_FP8 = 3e-2
 LSE_RTOL = 1e-4
+LSE_FLOOR = 0.1  # |lse| below which the gate is absolute (LSE_RTOL * LSE_FLOOR)
 _MANT = {torch.bfloat16: 7, torch.float16: 10, torch.float32: 23}
 
 
@@ -52,7 +57,7 @@ def assert_lse(lse_gpu, lse_ref, what: str = "lse"):
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(got), fin), f"{what}: finiteness differs"
     d = np.abs(got[fin] - lse_ref[fin])
-    tol = LSE_RTOL * np.maximum(1.0, np.abs(lse_ref[fin]))
+    tol = LSE_RTOL * np.maximum(LSE_FLOOR, np.abs(lse_ref[fin]))
     bad = ~(d <= tol)
     if bad.any():
         raise AssertionError(f"{what}: {int(bad.sum())} rows outside 1e-4 relative "

@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from exact_io_aware_106_b300 import attn, workloads as W
 from tests.parity import assert_lse, assert_out
 
@@ -61,6 +62,37 @@ def test_static_ws_decode_matches_workspace_decode_twice():
         assert attn.last_error() == attn.OK
         assert_out(O, O_ref.double().cpu().numpy(), what="static-ws O")
         assert_lse(lse, lse_ref.double().cpu().numpy(), what="static-ws lse")
+        # and against the fp64 oracle directly
+        O_or, lse_or = oracle.decode_paged(t["q"], t["Kc"], t["Vc"], t["block_table"],
+                                           t["seq_lens"])
+        assert_out(O, O_or, what="static-ws O vs oracle")
+        assert_lse(lse, lse_or, what="static-ws lse vs oracle")
+
+
+@pytest.mark.gpu
+def test_static_ws_decode_allocates_no_device_memory():
+    """The entry point's promise: once its kernels are loaded (a first call),
+    a call leaves the device's free memory exactly where it was."""
+    spec = W.DecodeSpec(5, 16, 4, 128, 1, 4000, 16, "bf16", "bf16", "bf16")
+    t = W.make_decode(spec, seed=13, lens=[4000, 7, 1234, 16, 2500])
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    st, O, lse = _static_ws_decode(g, spec.len_hi, torch.bfloat16)  # loads the kernels
+    assert st == attn.OK
+    torch.cuda.synchronize()
+    S, Hq, d = g["q"].shape
+    num_blocks, Hkv, bs, _ = g["Kc"].shape
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        st = attn.lib().attn_decode_static_ws(
+            _p(g["q"]), _p(g["Kc"]), _p(g["Vc"]), _p(g["block_table"]), _p(g["seq_lens"]),
+            _p(O), _p(lse), S, Hq, Hkv, d, bs, g["block_table"].shape[1], num_blocks,
+            spec.len_hi, 1.0 / np.sqrt(d), 1, 1, 1, None, None, stream)
+        assert st == attn.OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    assert attn.last_error() == attn.OK
 
 
 def test_static_ws_decode_refuses_sizes_beyond_its_scratch():
