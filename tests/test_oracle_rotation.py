@@ -92,3 +92,112 @@ def test_rotation_lowers_fp8_attention_error_on_outlier_data():
     err_naive = np.sqrt(np.mean((On - O) ** 2))
     err_rot = np.sqrt(np.mean((Or - O) ** 2))
     assert err_rot < err_naive / 1.1, (err_naive, err_rot)
+
+
+# ------------------------------------------------- block-wise quantisation
+# marketmaker.cc "Flash Attention and sequence length", FA3 item 3: the
+# rotation comes before a block-wise quantisation.  Blocks of 128 rows of a
+# head (the block size is this build's reading).
+
+def test_quantize_per_block_is_round_to_nearest_of_the_block_scaled_values():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((2, 3, 300, 64)) * rng.uniform(0.5, 4, (2, 3, 300, 1))
+    codes, scales = R.quantize_per_block(x, 128)
+    assert scales.shape == (6, 3)  # ceil(300 / 128) blocks, the last one ragged
+    dq = R.dequantize_per_block(codes, scales, 128)
+    xf, df = x.reshape(6, 300, 64), dq.reshape(6, 300, 64)
+    for blk in range(3):
+        rows = slice(128 * blk, 128 * (blk + 1))
+        sc = scales[:, blk].astype(np.float64)
+        v = np.abs(xf[:, rows] / sc[:, None, None])
+        ex = np.floor(np.log2(np.maximum(v, 2.0 ** -6)))
+        half_step = 0.5 * np.where(v < 2.0 ** -6, 2.0 ** -9, 2.0 ** (ex - 3))
+        assert (np.abs(xf[:, rows] - df[:, rows]) <=
+                half_step * sc[:, None, None] * (1 + 1e-6)).all()
+        # the block's largest entry maps to the largest finite code, +-448
+        for h in range(6):
+            assert np.max(np.abs(df[h, rows])) == pytest.approx(448 * sc[h], rel=1e-6)
+
+
+def test_quantize_per_block_codes_match_torch_cast():
+    """An independent encoder: torch's float8_e4m3fn cast of the fp32
+    quotient x / scale[block] gives the same codes."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((1, 2, 260, 128)) * 3
+    codes, scales = R.quantize_per_block(x, 128)
+    xf = x.reshape(2, 260, 128).astype(np.float32)
+    sc = scales[:, np.arange(260) // 128][:, :, None]
+    q = torch.from_numpy((xf / sc).astype(np.float32)).to(torch.float8_e4m3fn)
+    assert np.array_equal(codes.reshape(2, 260, 128), q.view(torch.uint8).numpy())
+
+
+def test_block_scales_relate_to_the_head_scale():
+    """Each block's scale is at most the head's; the largest equals it; one
+    block covering the whole head is per-head quantisation, bit for bit."""
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((2, 2, 500, 64))
+    cb, sb = R.quantize_per_block(x, 128)
+    ch, sh = R.quantize_per_head(x)
+    assert (sb <= sh[:, None]).all()
+    assert np.array_equal(sb.max(axis=1), sh)
+    c1, s1 = R.quantize_per_block(x, 500)
+    assert np.array_equal(c1, ch) and np.array_equal(s1[:, 0], sh)
+
+
+def test_an_outlier_coarsens_only_its_own_block():
+    """The property block-wise quantisation exists for: an outlier planted in
+    block 1 raises that block's scale and changes that block's codes only;
+    per head, it changes the codes of every block."""
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((1, 1, 384, 64))
+    y = x.copy()
+    y[0, 0, 200, 5] = 80.0
+    cx, sx = R.quantize_per_block(x, 128)
+    cy, sy = R.quantize_per_block(y, 128)
+    assert sy[0, 1] > 10 * sx[0, 1]
+    assert sy[0, 0] == sx[0, 0] and sy[0, 2] == sx[0, 2]
+    assert np.array_equal(cy[..., :128, :], cx[..., :128, :])
+    assert np.array_equal(cy[..., 256:, :], cx[..., 256:, :])
+    hx, _ = R.quantize_per_head(x)
+    hy, _ = R.quantize_per_head(y)
+    assert not np.array_equal(hy[..., :128, :], hx[..., :128, :])
+    # and the error of the untouched blocks stays that of clean data
+    err_b = np.abs(R.dequantize_per_block(cy, sy, 128) - y)[..., :128, :].max()
+    hy_c, hy_s = R.quantize_per_head(y)
+    err_h = np.abs(R.dequantize(hy_c, hy_s) - y)[..., :128, :].max()
+    assert err_b < err_h
+
+
+def test_rotation_lowers_the_block_peak_on_outlier_data():
+    """The mechanism under block-wise scales: after the rotation every
+    128-row block's peak-to-RMS ratio falls by more than half."""
+    rng = np.random.default_rng(15)
+    x = outlier_tensor(rng, (1, 2, 512, 128))
+    xr = R.rotate(x, rng.choice([-1.0, 1.0], 128))
+
+    def par(a):
+        b = a.reshape(2, 4, 128 * 128)
+        return np.abs(b).max(axis=2) / np.sqrt((b ** 2).mean(axis=2))
+    assert (par(xr) < 0.5 * par(x)).all()
+
+
+def test_rotation_lowers_fp8_attention_error_under_block_scales():
+    """Exact attention with Q, K quantised block-wise (128 rows) to E4M3,
+    directly (naive) or after the rotation, V per head in both arms, on the
+    outlier recipe: the rotated error is lower.  The page's 2.6x is its own
+    H100 measurement on its own data and is not pinned."""
+    rng = np.random.default_rng(2)
+    B, H, n, d = 1, 4, 256 * 2, 128
+    Q, K = outlier_tensor(rng, (B, H, n, d)), outlier_tensor(rng, (B, H, n, d))
+    V = rng.standard_normal((B, H, n, d))
+    O, _ = oracle.sdpa(Q, K, V, True)
+    vq, vs = R.quantize_per_head(V)
+    Vd = R.dequantize(vq, vs)
+    deq = lambda a: R.dequantize_per_block(*R.quantize_per_block(a, 128), 128)  # noqa: E731
+    On, _ = oracle.sdpa(deq(Q), deq(K), Vd, True)
+    s = rng.choice([-1.0, 1.0], d)
+    Or, _ = oracle.sdpa(deq(R.rotate(Q, s)), deq(R.rotate(K, s)), Vd, True,
+                        scale=1.0 / (d * np.sqrt(d)))
+    err_naive = np.sqrt(np.mean((On - O) ** 2))
+    err_rot = np.sqrt(np.mean((Or - O) ** 2))
+    assert err_rot < err_naive / 1.1, (err_naive, err_rot)
