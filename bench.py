@@ -46,7 +46,7 @@ PREFILL = W.PREFILL_WORKLOADS["long-32k"]
 DECODE = W.DECODE_WORKLOADS["paged-decode"]
 METRIC = "prefill attn TFLOP/s & decode KV GB/s on 1 B300, as % of roofline"
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-ESZ = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1}
+ESZ = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e4m3b": 1}
 
 
 # --------------------------------------------------------------- roofline
@@ -461,17 +461,30 @@ def workload_lines(name: str, steps: int, warmup: int):
             if kind == "prefill":
                 t = W.make_prefill(spec, seed=0, device=dev)
                 kw = {}
+                call = attn.prefill
                 if spec.dtype == "e4m3":
                     kw = W.quantize_prefill_e4m3(t)
+                elif spec.dtype == "e4m3b":
+                    # block-wise Q / K scales (128 rows), V per head: quantised by
+                    # the library's own kernel, outside the timed region
+                    kw = W.quantize_prefill_e4m3(t)
+                    for n in ("Q", "K"):
+                        x = t[n]
+                        c, s_ = attn.rotate_quantize_e4m3(
+                            x.reshape(-1, x.shape[2], x.shape[3]).contiguous(), None,
+                            rows_per_block=attn.E4M3_SCALE_BLOCK)
+                        kw[n], kw[n.lower() + "_scale"] = c.view(x.shape), s_
+                    call = attn.prefill_e4m3_blocks
                 Q, K, V = kw.pop("Q", t["Q"]), kw.pop("K", t["K"]), kw.pop("V", t["V"])
                 O = torch.empty(t["Q"].shape, dtype=W.DTYPES[spec.out_dtype], device=dev)
                 lse = torch.empty(t["Q"].shape[:3], dtype=torch.float32, device=dev)
 
                 def fn():
-                    attn.prefill(Q, K, V, spec.causal, O=O, lse=lse, stream=stream, **kw)
+                    call(Q, K, V, spec.causal, O=O, lse=lse, stream=stream, **kw)
                 med, best = _time_kernel(fn, stream, warmup, steps, flush)
                 F = prefill_flops(spec)
-                peak = pk["bf16_tflops"] * (2.0 if spec.dtype == "e4m3" else 1.0)
+                f8 = spec.dtype.startswith("e4m3")
+                peak = pk["bf16_tflops"] * (2.0 if f8 else 1.0)
                 Bp = prefill_bytes(spec)
                 roof = max(F / (peak * 1e12), Bp / (pk["hbm_gbs"] * 1e9))
                 line.update(ms=round(med * 1e3, 4), best_ms=round(best * 1e3, 4),
@@ -480,7 +493,7 @@ def workload_lines(name: str, steps: int, warmup: int):
                             pct_roofline=round(100 * roof / med, 2),
                             peak_tflops=peak,
                             peak_kind="measured burst bf16" + (
-                                " x 2 (nominal fp8/bf16 ratio)" if spec.dtype == "e4m3" else ""))
+                                " x 2 (nominal fp8/bf16 ratio)" if f8 else ""))
             elif kind == "backward":
                 line["workload"] = "bwd-" + spec.name
                 t = W.make_backward(spec, seed=0, device=dev)

@@ -23,8 +23,11 @@ EXPORTS = ("attn_prefill", "attn_prefill_from_host", "attn_prefill_from_host_hea
            "attn_prefill_paged", "attn_decode_workspace_bytes", "attn_decode",
            "attn_decode_tokens", "attn_kv_append", "attn_backward",
            "attn_backward_workspace_bytes", "attn_rotate_quantize_e4m3",
-           "attn_last_error", "attn_status_str", "attn_last_launch_count",
-           "attn_decode_static_ws")
+           "attn_prefill_e4m3_blocks", "attn_last_error", "attn_status_str",
+           "attn_last_launch_count", "attn_decode_static_ws")
+
+# Rows per E4M3 scale block in prefill_e4m3_blocks (ATTN_E4M3_SCALE_BLOCK).
+E4M3_SCALE_BLOCK = 128
 
 # Scratch size compiled into the library for attn_decode_static_ws.
 DECODE_STATIC_WS_BYTES = 16 << 20
@@ -76,8 +79,12 @@ def lib():
         L.attn_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                     i32, i32, f32, i32, i32, i32, vp, sz, vp]
         L.attn_backward.restype = i32
-        L.attn_rotate_quantize_e4m3.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+        L.attn_rotate_quantize_e4m3.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                vp]
         L.attn_rotate_quantize_e4m3.restype = i32
+        L.attn_prefill_e4m3_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                               i32, i32, f32, i32, vp, vp, vp, vp]
+        L.attn_prefill_e4m3_blocks.restype = i32
         L.attn_last_error.argtypes = [vp]
         L.attn_last_error.restype = i32
         L.attn_status_str.argtypes = [i32]
@@ -264,21 +271,54 @@ def backward(Q, K, V, O, dO, lse, causal: bool, scale: float | None = None, out_
     return dQ, dK, dV
 
 
-def rotate_quantize_e4m3(X, signs, stream=None):
-    """Rows of X [..., n, d] times diag(signs) H_d, quantised to E4M3 with one
-    scale per head (all leading dims but the last two flattened).  Returns
-    (codes like X in float8_e4m3fn, scales [heads] fp32)."""
+def rotate_quantize_e4m3(X, signs=None, rows_per_block: int = 0, stream=None):
+    """Rows of X [..., n, d] times diag(signs) H_d (no rotation when signs is
+    None), quantised to E4M3 with one scale per block of rows_per_block rows
+    of a head (0: one per head; all leading dims but the last two flattened
+    into heads).  Returns (codes like X in float8_e4m3fn, scales
+    [heads, ceil(n / rows_per_block)] fp32, or [heads] for per-head)."""
     _cuda(X, signs)
     d = X.shape[-1]
     n = X.shape[-2]
     heads = X.numel() // (n * d)
+    rpb = n if rows_per_block <= 0 or rows_per_block > n else rows_per_block
+    nb = -(-n // rpb)
     codes = torch.empty(X.shape, dtype=torch.float8_e4m3fn, device=X.device)
-    scales = torch.empty(heads, dtype=torch.float32, device=X.device)
-    ws = torch.empty(heads, dtype=torch.int32, device=X.device)
+    scales = torch.empty((heads, nb), dtype=torch.float32, device=X.device)
+    ws = torch.empty(heads * nb, dtype=torch.int32, device=X.device)
     st = lib().attn_rotate_quantize_e4m3(_ptr(X), _ptr(signs), _ptr(codes), _ptr(scales),
-                                         _ptr(ws), heads, n, d, _DT[X.dtype], _stream(stream))
+                                         _ptr(ws), heads, n, d, int(rows_per_block),
+                                         _DT[X.dtype], _stream(stream))
     _check("attn_rotate_quantize_e4m3", st)
-    return codes, scales
+    return codes, (scales.view(heads) if rows_per_block <= 0 else scales)
+
+
+def prefill_e4m3_blocks(Q, K, V, causal: bool, q_scale, k_scale, v_scale,
+                        scale: float | None = None, out_dtype=torch.bfloat16, O=None, lse=None,
+                        want_lse: bool = True, stream=None):
+    """prefill() for E4M3 Q [B,Hq,n_q,d], K/V [B,Hkv,n_kv,d] with block-wise
+    scales: q_scale [B*Hq, ceil(n_q/128)], k_scale [B*Hkv, ceil(n_kv/128)]
+    (one per 128 rows of a head), v_scale [B*Hkv].  Returns (O, lse)."""
+    _cuda(Q, K, V, q_scale, k_scale, v_scale)
+    B, Hq, nq, d = Q.shape
+    _, Hkv, nkv, _ = K.shape
+    bq, bk = -(-nq // E4M3_SCALE_BLOCK), -(-nkv // E4M3_SCALE_BLOCK)
+    if q_scale.numel() != B * Hq * bq or k_scale.numel() != B * Hkv * bk or \
+            v_scale.numel() != B * Hkv:
+        raise ValueError("scale arrays do not match the block-wise layout")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if O is None:
+        O = torch.empty((B, Hq, nq, d), dtype=out_dtype, device=Q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, nq), dtype=torch.float32, device=Q.device)
+    _cuda(O, lse)
+    st = lib().attn_prefill_e4m3_blocks(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), B, Hq,
+                                        Hkv, nq, nkv, d, int(bool(causal)), float(scale),
+                                        _DT[O.dtype], _ptr(q_scale), _ptr(k_scale),
+                                        _ptr(v_scale), _stream(stream))
+    _check("attn_prefill_e4m3_blocks", st)
+    return O, lse
 
 
 def decode_workspace_bytes(num_seqs: int, Hq: int, d: int, max_seq_len: int) -> int:

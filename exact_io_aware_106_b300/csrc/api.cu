@@ -120,6 +120,24 @@ attn_status attn_prefill(const void *Q, const void *K, const void *V, void *O, f
     return ATTN_OK;
 }
 
+attn_status attn_prefill_e4m3_blocks(const void *Q, const void *K, const void *V, void *O,
+                                     float *lse, int B, int Hq, int Hkv, int n_q, int n_kv,
+                                     int d, int causal, float scale, attn_dtype out_dtype,
+                                     const float *q_scale, const float *k_scale,
+                                     const float *v_scale, void *stream) {
+    t_last_launches = 0;
+    attn::PrefillArgs a;
+    const attn_status s = prefill_args(Q, K, V, O, lse, B, Hq, Hkv, n_q, n_kv, d, causal, scale,
+                                       ATTN_E4M3, out_dtype, q_scale, k_scale, v_scale, &a);
+    if (s != ATTN_OK)
+        return s;
+    a.e4m3_blocks = true;
+    if (attn::prefill_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = 1;
+    return ATTN_OK;
+}
+
 int attn_prefill_from_host_heads_per_chunk(int B, int Hq, int Hkv, int n_q, int d, int chunks,
                                            int sms) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || n_q <= 0 || d <= 0 || chunks < 0 ||
@@ -380,10 +398,11 @@ attn_status attn_backward(const void *Q, const void *K, const void *V, const voi
 
 attn_status attn_rotate_quantize_e4m3(const void *X, const int8_t *signs, void *codes,
                                       float *scales, void *amax_ws, int heads,
-                                      int rows_per_head, int d, attn_dtype in_dtype,
-                                      void *stream) {
+                                      int rows_per_head, int d, int rows_per_block,
+                                      attn_dtype in_dtype, void *stream) {
     t_last_launches = 0;
-    if (!X || !signs || !codes || !scales || !amax_ws || heads <= 0 || rows_per_head <= 0)
+    if (!X || !codes || !scales || !amax_ws || heads <= 0 || rows_per_head <= 0 ||
+        rows_per_block < 0)
         return ATTN_ERR_INVALID;
     if (!is16(in_dtype) || (d != 64 && d != 128 && d != 256))
         return ATTN_ERR_UNSUPPORTED;
@@ -391,8 +410,10 @@ attn_status attn_rotate_quantize_e4m3(const void *X, const int8_t *signs, void *
         return ATTN_ERR_INVALID;
     if (static_cast<long long>(heads) * rows_per_head > (1LL << 40))
         return ATTN_ERR_UNSUPPORTED;
+    const int rpb = (rows_per_block == 0 || rows_per_block > rows_per_head) ? rows_per_head
+                                                                            : rows_per_block;
     attn::RotQArgs a{X, signs, static_cast<uint8_t *>(codes), scales,
-                     static_cast<unsigned *>(amax_ws), heads, rows_per_head, d,
+                     static_cast<unsigned *>(amax_ws), heads, rows_per_head, d, rpb,
                      in_dtype == ATTN_BF16};
     if (attn::rotate_quantize_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;

@@ -24,6 +24,8 @@ struct PrefillArgs {
     const float *k_scale;
     const float *v_scale;
     unsigned *err;
+    // E4M3 Q / K scales per 128-row block of a head instead of per head
+    bool e4m3_blocks = false;
     // prefill over a block-paged cache (K, V are then the caches)
     bool paged = false;
     const int32_t *block_table = nullptr;
@@ -111,11 +113,11 @@ cudaError_t backward_launch(const BackwardArgs &a, cudaStream_t st);
 
 struct RotQArgs {
     const void *X;       // [heads, rows_per_head, d] 16-bit
-    const int8_t *signs; // [d], +-1
+    const int8_t *signs; // [d], +-1; null: no rotation
     uint8_t *codes;      // [heads, rows_per_head, d] E4M3
-    float *scales;       // [heads]
-    unsigned *amax_ws;   // [heads] scratch
-    int heads, rows_per_head, d;
+    float *scales;       // [heads, nb], nb = ceil(rows_per_head / rows_per_block)
+    unsigned *amax_ws;   // [heads, nb] scratch
+    int heads, rows_per_head, d, rows_per_block;
     bool bf16;
 };
 

@@ -112,11 +112,16 @@ struct Shape {
     float scale; // for reference only
 };
 
-// Per-head scales of E4M3 inputs (null for 16-bit inputs).
+// Scales of E4M3 inputs (null for 16-bit inputs).  Q and K carry one scale
+// per head or one per block of 128 rows of a head: query tile t (rows
+// 128t .. 128t+127) of head bh uses q[bh * qh + t * qb], keys 128j .. 128j+127
+// of KV head bkv use k[bkv * kh + j * kb] (qb = kb = 0 and qh = kh = 1 for
+// per-head scales).  V has one scale per KV head.
 struct Scales {
     const float *q;
     const float *k;
     const float *v;
+    int qh, qb, kh, kb;
 };
 
 // Block-paged K/V (prefill over a cache): per sequence b, seq_lens[b]
@@ -264,23 +269,19 @@ __device__ __forceinline__ int paged_len_or_reject(const Paged &pg, const Shape 
     return -1;
 }
 
-// CTA index -> (query block, batch, head).  Dense: query blocks in
-// descending order (heaviest causal work first), (batch, head) fastest.
-// Paged: (batch, KV head) slowest, then query block, then the G heads.
-__device__ __forceinline__ void work_item(const Shape &sh, bool paged, int idx, int &qb, int &b,
-                                          int &h) {
-    if (!paged) {
-        const int BH = sh.B * sh.Hq;
-        qb = sh.nqb - 1 - idx / BH;
-        b = (idx % BH) / sh.Hq;
-        h = (idx % BH) % sh.Hq;
-    } else {
-        const int per_kv = sh.nqb * sh.G;
-        const int kvi = idx / per_kv, rem = idx % per_kv;
-        qb = sh.nqb - 1 - rem / sh.G;
-        b = kvi / sh.Hkv;
-        h = (kvi % sh.Hkv) * sh.G + rem % sh.G;
-    }
+// CTA index -> (query block, batch, head): (batch, KV head) slowest, then
+// query blocks in descending order (heaviest causal work first), then the G
+// query heads of the group.  The CTAs resident at one time then belong to
+// one or two KV heads, whose K / V (16.8 MB per KV head at n = 32768,
+// d = 128) stay in L2 while all of the group's query heads and query blocks
+// stream them; with (batch, head) fastest the resident CTAs spread over
+// every KV head and their K / V together outgrow L2.
+__device__ __forceinline__ void work_item(const Shape &sh, int idx, int &qb, int &b, int &h) {
+    const int per_kv = sh.nqb * sh.G;
+    const int kvi = idx / per_kv, rem = idx % per_kv;
+    qb = sh.nqb - 1 - rem / sh.G;
+    b = kvi / sh.Hkv;
+    h = (kvi % sh.Hkv) * sh.G + rem % sh.G;
 }
 
 __device__ __forceinline__ int tile_blocks(const Shape &sh, int q0, int t) {
@@ -398,13 +399,12 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- work item.  Dense: heaviest query blocks first (causal work grows
-    // with q).  Paged: the CTAs sharing one (sequence, KV head) -- all its
-    // query blocks and the G heads of the group -- are adjacent, so that its
-    // cached K/V (a long prefix, read by every one of them) streams from
+    // ---- work item: the CTAs sharing one (sequence, KV head) -- all its
+    // query blocks, heaviest first, and the G heads of the group -- are
+    // adjacent, so that its K/V (read by every one of them) streams from
     // DRAM about once and is reused from L2.
     int qb, b, h;
-    work_item(sh, PAGED, static_cast<int>(blockIdx.x), qb, b, h);
+    work_item(sh, static_cast<int>(blockIdx.x), qb, b, h);
     const int bh = b * sh.Hq + h;
     const int bkv = b * sh.Hkv + h / sh.G;
     const int q0 = qb * (NT * BM);
@@ -687,11 +687,24 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         const int off = sh.n_kv - sh.n_q;
         const bool split = tile_split(sh, q0, t);
         const int r0 = q0 + t * BM;
-        const float c = F8 ? sh.c * sc.q[bh] * sc.k[bkv] : sh.c;
+        // score factor c = scale * log2(e) [* q_scale * k_scale of this
+        // (query tile, key block) pair for E4M3 inputs; the next block's k
+        // scale is fetched one block ahead]
+        // (a tile past the last query row has no blocks and reads no scale)
+        const bool live = nb[t] > 0;
+        const float cq =
+            (F8 && live) ? sh.c * sc.q[static_cast<size_t>(bh) * sc.qh + (r0 / BM) * sc.qb]
+                         : sh.c;
+        const float *ksc = F8 ? sc.k + static_cast<size_t>(bkv) * sc.kh : nullptr;
+        float k_next = (F8 && live) ? ksc[0] : 1.0f;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
 
         for (int j = 0; j < nb[t]; ++j) {
+            const float c = F8 ? cq * k_next : cq;
+            if constexpr (F8)
+                if (j + 1 < nb[t])
+                    k_next = ksc[(j + 1) * sc.kb];
             if (!mbar_wait_warp(b_sfull(t), j & 1, abort_flag, err)) {
                 ok = false;
                 break;
@@ -921,7 +934,7 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int qb, b, h;
-    pf::work_item(sh, PAGED, static_cast<int>(blockIdx.x), qb, b, h);
+    pf::work_item(sh, static_cast<int>(blockIdx.x), qb, b, h);
     const int bh = b * sh.Hq + h;
     const int bkv = b * sh.Hkv + h / sh.G;
     const int r0 = qb * BM;
@@ -1146,10 +1159,19 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
         const uint32_t tO = tmem + lane_off + O_COL;
         const int off = sh.n_kv - sh.n_q;
         const bool split = (sh.causal ? (r0 + off + 1) : sh.n_kv) < pf::kSplitKeys;
-        const float c = F8 ? sh.c * sc.q[bh] * sc.k[bkv] : sh.c;
+        // per (query tile, key block) score factor, as in the d <= 128 kernel;
+        // a 128-key scale block spans 128 / BN of this kernel's key blocks
+        const float cq =
+            F8 ? sh.c * sc.q[static_cast<size_t>(bh) * sc.qh + (r0 / BM) * sc.qb] : sh.c;
+        const float *ksc = F8 ? sc.k + static_cast<size_t>(bkv) * sc.kh : nullptr;
+        float k_next = (F8 && nb > 0) ? ksc[0] : 1.0f;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
+            const float c = F8 ? cq * k_next : cq;
+            if constexpr (F8)
+                if (j + 1 < nb)
+                    k_next = ksc[((j + 1) * BN / 128) * sc.kb];
             const int buf = j & 1;
             const uint32_t tS = tmem + lane_off + S_COL0 + buf * BN;
             if (!mbar_wait_warp(b_sfull(buf), (j >> 1) & 1, abort_flag, err)) {
@@ -1302,6 +1324,19 @@ static pf::Shape make_shape(const PrefillArgs &a, int rows_per_cta) {
     return sh;
 }
 
+// E4M3 scale indexing: per head (stride 1, no block step) or per 128-row
+// block (one row of ceil(n / 128) scales per head).
+static pf::Scales make_scales(const PrefillArgs &a) {
+    pf::Scales sc{a.q_scale, a.k_scale, a.v_scale, 1, 0, 1, 0};
+    if (a.e4m3_blocks) {
+        sc.qh = (a.n_q + 127) / 128;
+        sc.qb = 1;
+        sc.kh = (a.n_kv + 127) / 128;
+        sc.kb = 1;
+    }
+    return sc;
+}
+
 // Cache [num_blocks, Hkv, bs, d] (16-bit) viewed as {d, Hkv * bs, num_blocks},
 // box 64 x 16 x 1, 128-byte swizzle.
 static bool make_cache_map(CUtensorMap *m, const void *ptr, const PrefillArgs &a) {
@@ -1344,7 +1379,7 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
         !make_kv_maps(&mk, &mv, a, D, BF16, F8, pf::BN))
         return cudaErrorInvalidValue;
     const pf::Shape sh = make_shape(a, pf::NT * pf::BM);
-    const pf::Scales sc{a.q_scale, a.k_scale, a.v_scale};
+    const pf::Scales sc = make_scales(a);
     auto kern = pf::prefill_kernel<D, BF16, F8, PAGED, OUT>;
     // the in-kernel register split adds up only if the kernel launches with
     // exactly kLaunchRegs registers per thread; never launch it otherwise.
@@ -1381,7 +1416,7 @@ static cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t st) {
         !make_kv_maps(&mk, &mv, a, pfw::D, BF16, F8, pfw::Cfg<F8>::BN))
         return cudaErrorInvalidValue;
     const pf::Shape sh = make_shape(a, pfw::BM);
-    const pf::Scales sc{a.q_scale, a.k_scale, a.v_scale};
+    const pf::Scales sc = make_scales(a);
     auto kern = pfw::prefill_wide_kernel<BF16, F8, PAGED, OUT>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

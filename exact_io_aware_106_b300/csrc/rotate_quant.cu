@@ -1,17 +1,19 @@
 // rotate_quant.cu -- incoherent processing before fp8 attention.
 //
-// marketmaker.cc "Flash Attention and sequence length", FA3: Q and K are
-// multiplied by the same random orthogonal matrix before FP8 quantisation,
-// which spreads a few large entries over all d components so that the
-// per-head scale (amax / 448) no longer has to cover them.  The matrix here
-// is diag(s) H_d, s = +-1 random signs, H_d the Sylvester Hadamard matrix
-// (entries +-1, H H^T = d I), applied unnormalised: (Q R)(K R)^T = d Q K^T,
-// so attention on the rotated codes uses scale / d.
+// marketmaker.cc "Flash Attention and sequence length", FA3 (item 3): Q and
+// K are multiplied by the same random orthogonal matrix before the
+// block-wise FP8 quantisation, which spreads a few large entries over all d
+// components so that the block scales (amax / 448) no longer have to cover
+// them.  The matrix here is diag(s) H_d, s = +-1 random signs, H_d the
+// Sylvester Hadamard matrix (entries +-1, H H^T = d I), applied
+// unnormalised: (Q R)(K R)^T = d Q K^T, so attention on the rotated codes
+// uses scale / d.  Without signs the rows are quantised as they are (the
+// naive arm).  A block is `rpb` consecutive rows of one head.
 //
 // One warp per row: lane l holds elements l*E .. l*E+E-1 (E = d / 32); the
 // fast Walsh-Hadamard transform pairs element e with e + h for h = 1, 2,
 // ..., d/2 -- inside a lane while h < E, across lanes (shfl.xor by h / E)
-// after.  Pass 1 takes each head's amax of the rotated rows (atomic max on
+// after.  Pass 1 takes each block's amax of the (rotated) rows (atomic max on
 // the float bits, non-negative), pass 2 recomputes the transform and writes
 // codes rn_satfinite(y / scale), scale = amax / 448, division in fp32.
 #include "common.cuh"
@@ -21,7 +23,7 @@ namespace attn {
 
 namespace rq {
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool ROT>
 __device__ __forceinline__ void rotate_row(const uint16_t *row, const int8_t *signs, int lane,
                                            float (&y)[D / 32]) {
     constexpr int E = D / 32;
@@ -30,8 +32,10 @@ __device__ __forceinline__ void rotate_row(const uint16_t *row, const int8_t *si
         const uint16_t v = row[lane * E + k];
         const float x = BF16 ? __uint_as_float(static_cast<uint32_t>(v) << 16)
                              : __half2float(__ushort_as_half(v));
-        y[k] = signs[lane * E + k] < 0 ? -x : x;
+        y[k] = (ROT && signs[lane * E + k] < 0) ? -x : x;
     }
+    if constexpr (!ROT)
+        return;
 #pragma unroll
     for (int h = 1; h < D; h <<= 1) {
         if (h < E) {
@@ -54,16 +58,23 @@ __device__ __forceinline__ void rotate_row(const uint16_t *row, const int8_t *si
     }
 }
 
-template <int D, bool BF16>
+// Block index of row r: head r / rows_per_head, block (r % rows_per_head) / rpb
+// of that head's nb blocks.
+__device__ __forceinline__ long long block_of(long long r, int rows_per_head, int rpb, int nb) {
+    return (r / rows_per_head) * nb + (r % rows_per_head) / rpb;
+}
+
+template <int D, bool BF16, bool ROT>
 __global__ void __launch_bounds__(256)
     rotq_amax_kernel(const uint16_t *__restrict__ X, const int8_t *__restrict__ signs,
-                     unsigned *__restrict__ amax_bits, long long rows, int rows_per_head) {
+                     unsigned *__restrict__ amax_bits, long long rows, int rows_per_head, int rpb,
+                     int nb) {
     const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows)
         return;
     float y[D / 32];
-    rotate_row<D, BF16>(X + r * D, signs, lane, y);
+    rotate_row<D, BF16, ROT>(X + r * D, signs, lane, y);
     float a = 0.f;
 #pragma unroll
     for (int k = 0; k < D / 32; ++k)
@@ -72,26 +83,27 @@ __global__ void __launch_bounds__(256)
     for (int off = 16; off > 0; off >>= 1)
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
     if (lane == 0 && a > 0.f)
-        atomicMax(amax_bits + r / rows_per_head, __float_as_uint(a));
+        atomicMax(amax_bits + block_of(r, rows_per_head, rpb, nb), __float_as_uint(a));
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool ROT>
 __global__ void __launch_bounds__(256)
     rotq_quant_kernel(const uint16_t *__restrict__ X, const int8_t *__restrict__ signs,
                       const unsigned *__restrict__ amax_bits, uint8_t *__restrict__ codes,
-                      float *__restrict__ scales, long long rows, int rows_per_head) {
+                      float *__restrict__ scales, long long rows, int rows_per_head, int rpb,
+                      int nb) {
     constexpr int E = D / 32;
     const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows)
         return;
-    const long long head = r / rows_per_head;
-    const float amax = __uint_as_float(amax_bits[head]);
+    const long long blk = block_of(r, rows_per_head, rpb, nb);
+    const float amax = __uint_as_float(amax_bits[blk]);
     const float scale = (amax > 0.f && isfinite(amax)) ? amax / 448.0f : 1.0f;
-    if (lane == 0 && r % rows_per_head == 0)
-        scales[head] = scale;
+    if (lane == 0 && (r % rows_per_head) % rpb == 0)
+        scales[blk] = scale;
     float y[E];
-    rotate_row<D, BF16>(X + r * D, signs, lane, y);
+    rotate_row<D, BF16, ROT>(X + r * D, signs, lane, y);
     uint8_t q[E];
 #pragma unroll
     for (int k = 0; k < E; k += 2) {
@@ -119,29 +131,39 @@ __global__ void __launch_bounds__(256)
 
 } // namespace rq
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool ROT>
 static cudaError_t rotq_t(const RotQArgs &a, cudaStream_t st) {
     const long long rows = static_cast<long long>(a.heads) * a.rows_per_head;
     const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
-    cudaError_t e = cudaMemsetAsync(a.amax_ws, 0, static_cast<size_t>(a.heads) * 4, st);
+    const int rpb = a.rows_per_block;
+    const int nb = (a.rows_per_head + rpb - 1) / rpb;
+    cudaError_t e =
+        cudaMemsetAsync(a.amax_ws, 0, static_cast<size_t>(a.heads) * nb * 4, st);
     if (e != cudaSuccess)
         return e;
-    rq::rotq_amax_kernel<D, BF16><<<grid, 256, 0, st>>>(
-        static_cast<const uint16_t *>(a.X), a.signs, a.amax_ws, rows, a.rows_per_head);
+    rq::rotq_amax_kernel<D, BF16, ROT><<<grid, 256, 0, st>>>(
+        static_cast<const uint16_t *>(a.X), a.signs, a.amax_ws, rows, a.rows_per_head, rpb, nb);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    rq::rotq_quant_kernel<D, BF16><<<grid, 256, 0, st>>>(
+    rq::rotq_quant_kernel<D, BF16, ROT><<<grid, 256, 0, st>>>(
         static_cast<const uint16_t *>(a.X), a.signs, a.amax_ws, a.codes, a.scales, rows,
-        a.rows_per_head);
+        a.rows_per_head, rpb, nb);
     return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t rotq_d(const RotQArgs &a, cudaStream_t st) {
+    if (a.signs != nullptr)
+        return a.bf16 ? rotq_t<D, true, true>(a, st) : rotq_t<D, false, true>(a, st);
+    return a.bf16 ? rotq_t<D, true, false>(a, st) : rotq_t<D, false, false>(a, st);
 }
 
 cudaError_t rotate_quantize_launch(const RotQArgs &a, cudaStream_t st) {
     switch (a.d) {
-    case 64: return a.bf16 ? rotq_t<64, true>(a, st) : rotq_t<64, false>(a, st);
-    case 128: return a.bf16 ? rotq_t<128, true>(a, st) : rotq_t<128, false>(a, st);
-    case 256: return a.bf16 ? rotq_t<256, true>(a, st) : rotq_t<256, false>(a, st);
+    case 64: return rotq_d<64>(a, st);
+    case 128: return rotq_d<128>(a, st);
+    case 256: return rotq_d<256>(a, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -106,8 +106,10 @@ DECODE_WORKLOADS = {
 
 
 def sweep_prefill(G: int, d: int, kv: str = "bf16") -> PrefillSpec:
-    return PrefillSpec(1, 8 * G, 8, 8192, 8192, d, True, kv if kv != "e4m3" else "e4m3",
-                       "bf16", f"sweep-prefill-G{G}-d{d}-{kv}")
+    """kv: "bf16", "e4m3" (one scale per head) or "e4m3b" (E4M3 with Q / K
+    scales per 128-row block, the block-wise form; values drawn as bf16)."""
+    return PrefillSpec(1, 8 * G, 8, 8192, 8192, d, True, kv, "bf16",
+                       f"sweep-prefill-G{G}-d{d}-{kv}")
 
 
 def sweep_decode(G: int, d: int, kv: str = "bf16") -> DecodeSpec:
@@ -129,7 +131,7 @@ def make_prefill(spec: PrefillSpec, seed: int = 0, device="cpu"):
     """Q [B,Hq,n_q,d], K/V [B,Hkv,n_kv,d] in the spec's storage type, drawn in
     the order Q, K, V from one generator."""
     g = _gen(device, seed)
-    dt = DTYPES["bf16" if spec.dtype == "e4m3" else spec.dtype]
+    dt = DTYPES["bf16" if spec.dtype.startswith("e4m3") else spec.dtype]
     Q = _randn((spec.B, spec.Hq, spec.n_q, spec.d), dt, g, device)
     K = _randn((spec.B, spec.Hkv, spec.n_kv, spec.d), dt, g, device)
     V = _randn((spec.B, spec.Hkv, spec.n_kv, spec.d), dt, g, device)

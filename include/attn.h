@@ -91,6 +91,33 @@ ATTN_API attn_status attn_prefill(const void *Q, const void *K, const void *V, v
                          attn_dtype out_dtype, const float *q_scale,
                          const float *k_scale, const float *v_scale, void *stream);
 
+/* Size of the row blocks that carry one E4M3 scale in
+ * attn_prefill_e4m3_blocks and attn_rotate_quantize_e4m3 (the prefill's
+ * query tile and key block). */
+#define ATTN_E4M3_SCALE_BLOCK 128
+
+/* attn_prefill for E4M3 Q, K, V with block-wise scales on Q and K
+ * (marketmaker.cc, "Flash Attention and sequence length", FA3 item 3:
+ * block-wise fp8 quantisation, after the rotation of
+ * attn_rotate_quantize_e4m3 or without it).  Rows 128 b .. 128 b + 127 of
+ * a head of Q (of K) share one scale:
+ *   q_scale [B * Hq,  ceil(n_q  / 128)] fp32: q_scale[bh][b] for query rows of
+ *           block b of head bh (bh = batch * Hq + head);
+ *   k_scale [B * Hkv, ceil(n_kv / 128)] fp32, likewise for keys;
+ *   v_scale [B * Hkv] fp32: one scale per KV head (V is not rotated).
+ * Dequantised value = code * scale.  The score of query i and key j is
+ * formed as scale * q_scale[bh][i/128] * k_scale[bkv][j/128] * (codes q_i .
+ * k_j), so each (query tile, key block) pair of score tiles carries one
+ * scale product.  Q [B, Hq, n_q, d], K, V [B, Hkv, n_kv, d] E4M3; O, lse,
+ * sizes, checks and errors as attn_prefill (the scale arrays' sizes are the
+ * caller's responsibility).  One kernel launch. */
+ATTN_API attn_status attn_prefill_e4m3_blocks(const void *Q, const void *K, const void *V,
+                                              void *O, float *lse, int B, int Hq, int Hkv,
+                                              int n_q, int n_kv, int d, int causal, float scale,
+                                              attn_dtype out_dtype, const float *q_scale,
+                                              const float *k_scale, const float *v_scale,
+                                              void *stream);
+
 /* attn_prefill with Q, K, V starting in host memory and O (and lse) ending
  * there, the host<->device copies overlapped with the attention kernels
  * (auturnal.com, "From attention to IO-aware execution" §10: the slowest
@@ -262,22 +289,28 @@ ATTN_API attn_status attn_backward(const void *Q, const void *K, const void *V, 
                                    size_t workspace_bytes, void *stream);
 
 /* Incoherent processing for fp8 attention (marketmaker.cc, "Flash Attention
- * and sequence length", FA3: a random orthogonal rotation of Q and K before
- * FP8 quantisation spreads outliers over all components).  Each row x of X
- * becomes y = x diag(signs) H_d (H_d the Sylvester Hadamard matrix, entries
- * +-1, unnormalised), quantised per head: scale[h] = amax_h / 448 over the
- * head's rotated rows, codes = e4m3_rn_satfinite(y / scale[h]).  Rotating Q
- * and K with the same signs gives (Q R)(K R)^T = d Q K^T: pass scale / d to
- * attn_prefill with the codes (V is quantised without rotation).
+ * and sequence length", FA3 item 3: a random orthogonal rotation of Q and K
+ * before the block-wise FP8 quantisation spreads outliers over all
+ * components).  Each row x of X becomes y = x diag(signs) H_d (H_d the
+ * Sylvester Hadamard matrix, entries +-1, unnormalised), quantised per block
+ * of rows_per_block consecutive rows of a head: scale = amax / 448 over the
+ * block's rotated values, codes = e4m3_rn_satfinite(y / scale) with the
+ * division in fp32.  Rotating Q and K with the same signs gives
+ * (Q R)(K R)^T = d Q K^T: pass scale / d to the prefill with the codes (V is
+ * quantised without rotation).  signs == NULL quantises the rows as they are
+ * (naive fp8).
  *   X [heads, rows_per_head, d] in_dtype (F16 / BF16); signs [d] int8, +-1
- *     (host-chosen, e.g. seeded random)
- *   codes [heads, rows_per_head, d] E4M3; scales [heads] fp32
- *   amax_ws: device scratch of heads * 4 bytes
+ *     (host-chosen, e.g. seeded random), or NULL
+ *   rows_per_block: 0 (or >= rows_per_head) for one scale per head;
+ *     ATTN_E4M3_SCALE_BLOCK for the scales attn_prefill_e4m3_blocks takes
+ *   codes [heads, rows_per_head, d] E4M3;
+ *   scales [heads, nb] fp32, nb = ceil(rows_per_head / rows_per_block)
+ *   amax_ws: device scratch of heads * nb * 4 bytes
  * d in {64, 128, 256}.  One memset and two kernel launches. */
 ATTN_API attn_status attn_rotate_quantize_e4m3(const void *X, const int8_t *signs, void *codes,
                                                float *scales, void *amax_ws, int heads,
-                                               int rows_per_head, int d, attn_dtype in_dtype,
-                                               void *stream);
+                                               int rows_per_head, int d, int rows_per_block,
+                                               attn_dtype in_dtype, void *stream);
 
 /* Synchronises `stream`, then returns and clears the current device's error
  * word: ATTN_ERR_TIMEOUT if a bounded wait expired, ATTN_ERR_INVALID if a

@@ -71,6 +71,37 @@ def test_prefill_host_validation(L):
     assert L.attn_last_launch_count() == 0
 
 
+def test_prefill_e4m3_blocks_host_validation(L):
+    def call(**kw):
+        a = dict(Q=FAKE, B=1, Hq=4, Hkv=2, nq=128, nkv=128, d=128, causal=1, outd=1, qs=FAKE,
+                 ks=FAKE, vs=FAKE)
+        a.update(kw)
+        return L.attn_prefill_e4m3_blocks(a["Q"], FAKE, FAKE, FAKE, None, a["B"], a["Hq"],
+                                          a["Hkv"], a["nq"], a["nkv"], a["d"], a["causal"], 0.1,
+                                          a["outd"], a["qs"], a["ks"], a["vs"], None)
+    assert call(Q=None) == attn.ERR_INVALID
+    assert call(qs=None) == attn.ERR_INVALID                          # scales required
+    assert call(ks=None) == attn.ERR_INVALID
+    assert call(nq=300, nkv=200) == attn.ERR_INVALID                  # causal, n_q > n_kv
+    assert call(d=80) == attn.ERR_UNSUPPORTED
+    assert call(outd=3) == attn.ERR_UNSUPPORTED                       # E4M3 output
+    assert L.attn_last_launch_count() == 0
+
+
+def test_rotate_quantize_host_validation(L):
+    def call(**kw):
+        a = dict(X=FAKE, heads=2, rows=100, d=128, rpb=128, ind=1)
+        a.update(kw)
+        return L.attn_rotate_quantize_e4m3(a["X"], None, FAKE, FAKE, FAKE, a["heads"], a["rows"],
+                                           a["d"], a["rpb"], a["ind"], None)
+    assert call(X=None) == attn.ERR_INVALID
+    assert call(rpb=-1) == attn.ERR_INVALID
+    assert call(rows=0) == attn.ERR_INVALID
+    assert call(d=32) == attn.ERR_UNSUPPORTED
+    assert call(ind=3) == attn.ERR_UNSUPPORTED                        # E4M3 input
+    assert L.attn_last_launch_count() == 0
+
+
 def _prefill_paged(L, **kw):
     a = dict(B=2, Hq=4, Hkv=2, nq=64, d=128, bs=16, mb=8, nb=32, msl=128, causal=1, scale=0.1,
              ind=1, outd=1, bt=FAKE)

@@ -109,15 +109,19 @@ def test_decode_bad_block_index_is_reported_not_read():
     assert attn.last_error() == attn.OK  # the error word was cleared
 
 
-def test_decode_full_size_sampled_sequences():
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_decode_full_size_sampled_sequences(out):
+    """The 64-sequence paged-decode workload in the launch configuration the
+    benchmark times (bf16 output there), on sampled sequences: the shortest,
+    the longest and six others."""
     spec = W.DECODE_WORKLOADS["paged-decode"]
     t = W.make_decode(spec, seed=0, device="cuda")
     lens = t["seq_lens"].cpu()
     O, lse = attn.decode(t["q"], t["Kc"], t["Vc"], t["block_table"], t["seq_lens"],
-                         max_seq_len=spec.len_hi, out_dtype=torch.float32)
+                         max_seq_len=spec.len_hi, out_dtype=W.DTYPES[out])
     assert attn.last_error() == attn.OK
     order = torch.argsort(lens)
-    pick = sorted({int(order[0]), int(order[-1]), 7, 40})
+    pick = sorted({int(order[0]), int(order[-1]), 7, 40, 3, 21, 55, 63})
     # gather the sampled sequences' blocks into a compact cache for the oracle
     bt = t["block_table"].cpu()
     rows, phys = [], []
@@ -138,9 +142,10 @@ def test_decode_full_size_sampled_sequences():
     assert torch.isfinite(O).all()
 
 
-SWEEP_DECODE = [W.sweep_decode(G, d, kv) for G, d, kv in
-                ((1, 256, "bf16"), (16, 256, "bf16"), (4, 64, "bf16"), (8, 128, "bf16"),
-                 (1, 256, "e4m3"), (16, 128, "e4m3"))]
+# every cell of the G x d x cache-format sweep (code-journey.com "Attention
+# co-design", Group Size (G) x Head Dimension (Hsz)): 32 sequences x 8192
+SWEEP_DECODE = [W.sweep_decode(G, d, kv) for kv in ("bf16", "e4m3") for G in (1, 4, 8, 16)
+                for d in (64, 128, 256)]
 
 
 @pytest.mark.parametrize("spec", SWEEP_DECODE, ids=lambda s: s.name)
@@ -165,6 +170,12 @@ def test_decode_sweep_full_size_sampled_sequences(spec):
     assert_out(O[pick], O_ref)
     assert_lse(lse[pick], lse_ref)
     assert torch.isfinite(O).all()
+    # the bf16 output the benchmark writes: the same call rounded once
+    O16, _ = attn.decode(t["q"], t["Kc"], t["Vc"], t["block_table"], t["seq_lens"],
+                         max_seq_len=spec.len_hi, k_scale=t["k_scale"], v_scale=t["v_scale"],
+                         out_dtype=torch.bfloat16)
+    assert attn.last_error() == attn.OK
+    assert torch.equal(O16, O.to(torch.bfloat16))
 
 
 # ----------------------------------------------------------------- append

@@ -98,8 +98,10 @@ def _sample_rows(n_q, rng, k=6):
     return sorted({r for r in base if 0 <= r < n_q})
 
 
-SWEEP_PREFILL = [W.sweep_prefill(G, d) for G, d in ((1, 64), (16, 64), (4, 128), (16, 128),
-                                                   (1, 256), (8, 256), (16, 256))]
+# every cell of the G x d sweep (code-journey.com "Attention co-design", Group
+# Size (G) x Head Dimension (Hsz)): B = 1, ISL = 8192, Hkv = 8, Hq = 8 G
+SWEEP_GRID = [(G, d) for G in (1, 4, 8, 16) for d in (64, 128, 256)]
+SWEEP_PREFILL = [W.sweep_prefill(G, d) for G, d in SWEEP_GRID]
 
 
 @pytest.mark.parametrize("name", ["gqa-4k", "long-23k", "long-32k"] +
@@ -175,11 +177,14 @@ def test_prefill_e4m3_quantisation_budget(case):
     assert_out(O.float(), O_src, atol=ATOL_FP8)
 
 
-SWEEP_PREFILL_E4M3 = [W.sweep_prefill(G, d, "e4m3") for G, d in ((1, 64), (8, 128), (16, 256))]
+SWEEP_PREFILL_E4M3 = [W.sweep_prefill(G, d, "e4m3") for G, d in SWEEP_GRID]
 
 
 @pytest.mark.parametrize("spec", SWEEP_PREFILL_E4M3, ids=lambda s: s.name)
 def test_prefill_e4m3_full_size_sampled_rows(spec):
+    """Every E4M3 sweep cell at full size: sampled rows against the oracle fed
+    the dequantised inputs (16-bit rule), and rows that see >= 512 keys
+    against the oracle fed the unquantised inputs (3e-2)."""
     t = W.make_prefill(spec, seed=0, device="cuda")
     qz = W.quantize_prefill_e4m3(t)
     O, lse = attn.prefill(qz["Q"], qz["K"], qz["V"], spec.causal,
@@ -197,4 +202,10 @@ def test_prefill_e4m3_full_size_sampled_rows(spec):
         Or, lr = oracle.sdpa_rows(Qh, Kh, Vh, [(0, 0, r) for r in rows], spec.causal, nthreads=0)
         assert_out(O[0, h, rows], Or, what=f"{spec.name} h{h}")
         assert_lse(lse[0, h, rows], lr, what=f"{spec.name} h{h}")
+        # the quantisation budget on rows that average >= 512 keys
+        long_rows = [r for r in rows if r >= 511]
+        Os, _ = oracle.sdpa_rows(t["Q"][:, h:h + 1].cpu(), t["K"][:, hk:hk + 1].cpu(),
+                                 t["V"][:, hk:hk + 1].cpu(), [(0, 0, r) for r in long_rows],
+                                 spec.causal, nthreads=0)
+        assert_out(O[0, h, long_rows], Os, atol=ATOL_FP8, what=f"{spec.name} h{h} vs source")
     assert torch.isfinite(O.float()).all()
