@@ -9,9 +9,11 @@
 #include "launch.h"
 
 
-// The device error word: bit DERR_TIMEOUT / DERR_INDEX, set by kernels with
-// atomicOr, read and cleared by attn_last_error().
-__device__ unsigned int g_attn_err_word;
+// The per-device control words every kernel receives (common.cuh): [0] is
+// the error word (bits DERR_TIMEOUT / DERR_INDEX, set by kernels with
+// atomicOr, read and cleared by attn_last_error()); [1] and [2] are the wait
+// limit and test hooks that only attn_debug_prefill_timeout sets.
+__device__ unsigned int g_attn_err_word[attn::CTL_WORDS];
 
 namespace {
 
@@ -421,16 +423,85 @@ attn_status attn_rotate_quantize_e4m3(const void *X, const int8_t *signs, void *
     return ATTN_OK;
 }
 
+attn_status attn_debug_prefill_timeout(const void *Q, const void *K, const void *V, void *O,
+                                       float *lse, int B, int Hq, int Hkv, int n_q, int n_kv,
+                                       int d, int causal, float scale, attn_dtype in_dtype,
+                                       attn_dtype out_dtype, unsigned wait_limit_us,
+                                       void *stream) {
+    t_last_launches = 0;
+    if (wait_limit_us == 0 || wait_limit_us > 1000000u)
+        return ATTN_ERR_INVALID;
+    if (!is16(in_dtype) || (d != 64 && d != 128))
+        return ATTN_ERR_UNSUPPORTED; // the hook lives in the dense d <= 128 kernel
+    attn::PrefillArgs a;
+    const attn_status s = prefill_args(Q, K, V, O, lse, B, Hq, Hkv, n_q, n_kv, d, causal, scale,
+                                       in_dtype, out_dtype, nullptr, nullptr, nullptr, &a);
+    if (s != ATTN_OK)
+        return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // set the limit and the hook, run the prefill, clear both: all in stream
+    // order; the stream is synchronised before the host words go out of scope
+    const unsigned set_words[2] = {wait_limit_us, attn::HOOK_WITHHOLD_Q};
+    static const unsigned clear_words[2] = {0u, 0u};
+    if (cudaMemcpyToSymbolAsync(g_attn_err_word, set_words, sizeof set_words,
+                                attn::CTL_WAIT_US * sizeof(unsigned), cudaMemcpyHostToDevice,
+                                st) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    const cudaError_t e = attn::prefill_launch(a, st);
+    if (cudaMemcpyToSymbolAsync(g_attn_err_word, clear_words, sizeof clear_words,
+                                attn::CTL_WAIT_US * sizeof(unsigned), cudaMemcpyHostToDevice,
+                                st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess || e != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = 1;
+    return ATTN_OK;
+}
+
+} // extern "C"
+
+namespace {
+
+// Both exponentials the prefill's softmax uses, elementwise, for the test
+// of the polynomial against the SFU and the exact values.
+__global__ void debug_exp2_kernel(const float *__restrict__ x, float *__restrict__ y_poly,
+                                  float *__restrict__ y_sfu, long long n) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n)
+        return;
+    const float v = x[i];
+    y_poly[i] = attn::ex2_poly2(make_float2(v, v)).x;
+    y_sfu[i] = attn::ex2(v);
+}
+
+} // namespace
+
+extern "C" {
+
+attn_status attn_debug_exp2(const float *x, float *y_poly, float *y_sfu, long long n,
+                            void *stream) {
+    t_last_launches = 0;
+    if (!x || !y_poly || !y_sfu || n <= 0 || n > (1LL << 34))
+        return ATTN_ERR_INVALID;
+    const unsigned grid = static_cast<unsigned>((n + 255) / 256);
+    debug_exp2_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y_poly, y_sfu, n);
+    if (cudaGetLastError() != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    t_last_launches = 1;
+    return ATTN_OK;
+}
+
 attn_status attn_last_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return ATTN_ERR_CUDA;
     unsigned w = 0;
-    if (cudaMemcpyFromSymbol(&w, g_attn_err_word, sizeof w) != cudaSuccess)
+    if (cudaMemcpyFromSymbol(&w, g_attn_err_word, sizeof w, attn::CTL_ERR * sizeof w) !=
+        cudaSuccess)
         return ATTN_ERR_CUDA;
     if (w != 0) {
         const unsigned zero = 0;
-        if (cudaMemcpyToSymbol(g_attn_err_word, &zero, sizeof zero) != cudaSuccess)
+        if (cudaMemcpyToSymbol(g_attn_err_word, &zero, sizeof zero, attn::CTL_ERR * sizeof w) !=
+            cudaSuccess)
             return ATTN_ERR_CUDA;
     }
     if (w & attn::DERR_TIMEOUT)

@@ -14,10 +14,25 @@ namespace attn {
 // Bits of the per-device error word.
 enum : unsigned { DERR_TIMEOUT = 1u, DERR_INDEX = 2u };
 
+// The error word is the first of CTL_WORDS per-device control words that
+// every kernel receives as `err`:
+//   [CTL_ERR]     error bits, set by kernels, read and cleared by the host;
+//   [CTL_WAIT_US] limit of the bounded waits in microseconds (0: the default
+//                 kWaitTimeoutNs); set only by the test entry point;
+//   [CTL_HOOKS]   test hooks (HOOK_WITHHOLD_Q: the dense prefill's producer
+//                 does not issue the Q copy, so the first wait on it expires).
+enum : int { CTL_ERR = 0, CTL_WAIT_US = 1, CTL_HOOKS = 2, CTL_WORDS = 4 };
+enum : unsigned { HOOK_WITHHOLD_Q = 1u };
+
 // A bounded wait gives up after this long (a healthy wait in these kernels
 // lasts microseconds).  On expiry the waiter sets DERR_TIMEOUT and the CTA's
 // abort flag, and every role unwinds to the common exit.
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long wait_limit_ns(const unsigned *ctl) {
+    const unsigned us = *reinterpret_cast<const volatile unsigned *>(ctl + CTL_WAIT_US);
+    return us != 0u ? 1000ull * us : kWaitTimeoutNs;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -69,13 +84,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = globaltimer();
+    unsigned long long limit = 0; // read once the wait has spun a while
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity))
             return true;
         if ((n & 31u) == 0) {
             if (*abort_flag)
                 return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs) {
+            if (limit == 0)
+                limit = wait_limit_ns(err);
+            if (globaltimer() - t0 > limit) {
                 atomicOr(err, DERR_TIMEOUT);
                 *abort_flag = 1;
                 return false;
@@ -94,7 +112,9 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
 }
 
 // Wait used only while unwinding after an abort: ignores the abort flag so
-// that copies already in flight land before the CTA exits; still bounded.
+// that copies already in flight land before the CTA exits; bounded by the
+// default limit (never the test's shorter one, so that copies in flight
+// always land).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait(bar, parity))
@@ -449,6 +469,33 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 2^x for two values on the FMA pipe instead of the SFU, for x <= 2^22
+// (the softmax passes x <= 8).  Range reduction 2^x = 2^j * 2^f with
+// j = rint(x), |f| <= 1/2 (exact: adding 1.5 * 2^23 rounds x to an integer
+// and leaves j in the low mantissa bits of the sum), then the degree-4
+// minimax polynomial p(f) = 1 + a1 f + ... + a4 f^4 of 2^f (relative error
+// 2.8e-6; exp2_poly.py derives the coefficients), and 2^j added to p's
+// exponent field as the integer j << 23 taken from the same sum.  x is
+// clamped to -127 first: f is then 0 and p exactly 1, so the result is
+// exactly +0 for x <= -127 (and for -inf); results below 2^-126 are tiny
+// positive values instead of exact.
+__device__ __forceinline__ float2 ex2_poly2(float2 x) {
+    constexpr float kA1 = 0x1.62e12ap-1f, kA2 = 0x1.ec0382p-3f, kA3 = 0x1.c9fd1ep-5f,
+                    kA4 = 0x1.3a007ap-7f;
+    constexpr float kRound = 12582912.0f; // 1.5 * 2^23
+    x.x = fmaxf(x.x, -127.0f);
+    x.y = fmaxf(x.y, -127.0f);
+    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
+    const float2 j = __fadd2_rn(t, make_float2(-kRound, -kRound));      // rint(x), exact
+    const float2 f = __ffma2_rn(j, make_float2(-1.0f, -1.0f), x);        // x - j, exact
+    float2 p = __ffma2_rn(make_float2(kA4, kA4), f, make_float2(kA3, kA3));
+    p = __ffma2_rn(p, f, make_float2(kA2, kA2));
+    p = __ffma2_rn(p, f, make_float2(kA1, kA1));
+    p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
+    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
 }
 
 // max(a, b, c) in one instruction (three-input max, sm_100 and later).

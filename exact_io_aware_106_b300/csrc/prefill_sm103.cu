@@ -63,6 +63,16 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kConvWarp = 10;
 constexpr int kSplitKeys = 512; // rows seeing fewer keys carry the P residual
+// Pairs of every 16 whose exponentials run on the FMA pipe (exp_pack_store),
+// per head size of the two-tile kernel.
+#ifndef ATTN_POLY_PAIRS_D64
+#define ATTN_POLY_PAIRS_D64 6
+#endif
+#ifndef ATTN_POLY_PAIRS_D128
+#define ATTN_POLY_PAIRS_D128 4
+#endif
+template <int D>
+constexpr int kPolyPairs = D == 64 ? ATTN_POLY_PAIRS_D64 : ATTN_POLY_PAIRS_D128;
 constexpr float kRescaleThreshold = 8.0f;
 // Registers per thread: 384 threads launch with 168 each (the most that three
 // warps per SM sub-partition allow); the producer / MMA / converter
@@ -308,7 +318,10 @@ __device__ __forceinline__ bool tile_split(const Shape &sh, int q0, int t) {
 // Returns the row sum of p (fp32, eight independent partial sums).  The
 // score scaling and the sums run as packed pairs (fma/add .f32x2: one
 // instruction per two elements, each lane rounded as the scalar form).
-template <int NB, bool BF16, bool SPLIT>
+// NPOLY of every 16 pairs take 2^x from the polynomial on the FMA pipe
+// (ex2_poly2) instead of the SFU, spread evenly over the 16, so that the
+// two pipes share the exponentials.
+template <int NB, bool BF16, bool SPLIT, int NPOLY>
 __device__ __forceinline__ float exp_pack_store(const float (&s)[NB], float c, float neg,
                                                 uint32_t tS) {
     float2 acc[4];
@@ -323,7 +336,8 @@ __device__ __forceinline__ float exp_pack_store(const float (&s)[NB], float c, f
         for (int i = 0; i < 16; ++i) {
             const float2 x =
                 __ffma2_rn(make_float2(s[ch * 32 + 2 * i], s[ch * 32 + 2 * i + 1]), c2, n2);
-            const float2 p = make_float2(ex2(x.x), ex2(x.y));
+            const float2 p = ((i * NPOLY) % 16 < NPOLY) ? ex2_poly2(x)
+                                                         : make_float2(ex2(x.x), ex2(x.y));
             acc[i & 3] = __fadd2_rn(acc[i & 3], p);
             hi[i] = pack2<BF16>(p.x, p.y);
             if constexpr (SPLIT)
@@ -484,15 +498,22 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             // ================================================= TMA producer
             if (lane == 0) {
                 constexpr int XP = C::PW / C::EB; // elements per Q/K panel row
+                // test hook: without the Q copy the MMA issuer's first wait
+                // expires, which exercises the unwinding below
+                const bool withhold_q =
+                    (*reinterpret_cast<const volatile unsigned *>(err + CTL_HOOKS) &
+                     HOOK_WITHHOLD_Q) != 0u;
                 int ntiles = 0;
                 for (int t = 0; t < NT; ++t)
                     ntiles += nb[t] > 0;
-                mbar_arrive_expect_tx(b_qfull, ntiles * C::Q_TILE_BYTES);
-                for (int t = 0; t < NT; ++t)
-                    if (nb[t] > 0)
-                        for (int p = 0; p < C::QK_PANELS; ++p)
-                            tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q, b_qfull,
-                                        p * XP, q0 + t * BM, bh);
+                if (!withhold_q) {
+                    mbar_arrive_expect_tx(b_qfull, ntiles * C::Q_TILE_BYTES);
+                    for (int t = 0; t < NT; ++t)
+                        if (nb[t] > 0)
+                            for (int p = 0; p < C::QK_PANELS; ++p)
+                                tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q,
+                                            b_qfull, p * XP, q0 + t * BM, bh);
+                }
                 int k_issued = 0, v_issued = 0;
                 for (int j = 0; j < nb_max; ++j) {
                     const int ks = j % C::NK;
@@ -527,7 +548,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                     v_issued = j + 1;
                 }
                 if (*abort_flag) { // let in-flight copies land before the CTA exits
-                    mbar_wait_drain(b_qfull, 0);
+                    if (!withhold_q)
+                        mbar_wait_drain(b_qfull, 0);
                     for (int u = max(0, k_issued - C::NK); u < k_issued; ++u)
                         mbar_wait_drain(b_kfull(u % C::NK), (u / C::NK) & 1);
                     if constexpr (F8) {
@@ -747,8 +769,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             const float alpha =
                 (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
             const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
-            const float sum = split ? exp_pack_store<BN, PB, true>(s, c, neg, tS)
-                                    : exp_pack_store<BN, PB, false>(s, c, neg, tS);
+            const float sum = split ? exp_pack_store<BN, PB, true, kPolyPairs<D>>(s, c, neg, tS)
+                                    : exp_pack_store<BN, PB, false, kPolyPairs<D>>(s, c, neg, tS);
             // O_t holds the sum over earlier blocks (their MMAs completed
             // before S_t of this block was produced); rescale it in place.
             if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
@@ -1232,8 +1254,8 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
                     tmem_st32(tO + ch * 32, u);
                 }
             }
-            const float sum = split ? pf::exp_pack_store<BN, PB, true>(s, c, neg, tS)
-                                    : pf::exp_pack_store<BN, PB, false>(s, c, neg, tS);
+            const float sum = split ? pf::exp_pack_store<BN, PB, true, 0>(s, c, neg, tS)
+                                    : pf::exp_pack_store<BN, PB, false, 0>(s, c, neg, tS);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();

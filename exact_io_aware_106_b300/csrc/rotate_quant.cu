@@ -34,25 +34,25 @@ __device__ __forceinline__ void rotate_row(const uint16_t *row, const int8_t *si
                              : __half2float(__ushort_as_half(v));
         y[k] = (ROT && signs[lane * E + k] < 0) ? -x : x;
     }
-    if constexpr (!ROT)
-        return;
+    if constexpr (ROT) {
 #pragma unroll
-    for (int h = 1; h < D; h <<= 1) {
-        if (h < E) {
+        for (int h = 1; h < D; h <<= 1) {
+            if (h < E) {
 #pragma unroll
-            for (int k = 0; k < E; ++k)
-                if ((k & h) == 0) {
-                    const float a = y[k], b = y[k + h];
-                    y[k] = a + b;
-                    y[k + h] = a - b;
+                for (int k = 0; k < E; ++k)
+                    if ((k & h) == 0) {
+                        const float a = y[k], b = y[k + h];
+                        y[k] = a + b;
+                        y[k + h] = a - b;
+                    }
+            } else {
+                const int m = h / E;
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int k = 0; k < E; ++k) {
+                    const float p = __shfl_xor_sync(0xffffffffu, y[k], m);
+                    y[k] = upper ? p - y[k] : y[k] + p;
                 }
-        } else {
-            const int m = h / E;
-            const bool upper = (lane & m) != 0;
-#pragma unroll
-            for (int k = 0; k < E; ++k) {
-                const float p = __shfl_xor_sync(0xffffffffu, y[k], m);
-                y[k] = upper ? p - y[k] : y[k] + p;
             }
         }
     }

@@ -318,6 +318,35 @@ ATTN_API attn_status attn_rotate_quantize_e4m3(const void *X, const int8_t *sign
  * CUDA error, else ATTN_OK. */
 ATTN_API attn_status attn_last_error(void *stream);
 
+/* Test entry point for the bounded waits (a failure-path check; the method
+ * has no counterpart of it).  Every wait inside the kernels of these
+ * libraries gives up after a limit (2 s by default), records
+ * ATTN_ERR_TIMEOUT, and the CTA unwinds: copies in flight land, tensor
+ * memory is freed, the CTA's output rows are written as O = 0 and
+ * lse = NaN.  This call runs attn_prefill (16-bit inputs, d in {64, 128})
+ * with the limit set to wait_limit_us and with the producer of the dense
+ * prefill kernel withholding its Q copy, so that the first wait on Q
+ * expires in every CTA.  The limit and the hook are set and cleared in
+ * stream order around the one kernel launch, and the call synchronises
+ * `stream` before it returns; it must not overlap any other call on the
+ * device (their waits would see the short limit).  Returns ATTN_OK when
+ * the launch went through; attn_last_error() then reports
+ * ATTN_ERR_TIMEOUT.  wait_limit_us in [1, 1000000]. */
+ATTN_API attn_status attn_debug_prefill_timeout(const void *Q, const void *K, const void *V,
+                                                void *O, float *lse, int B, int Hq, int Hkv,
+                                                int n_q, int n_kv, int d, int causal,
+                                                float scale, attn_dtype in_dtype,
+                                                attn_dtype out_dtype, unsigned wait_limit_us,
+                                                void *stream);
+
+/* Test entry point for the exponential of the prefill's softmax (the method
+ * has no counterpart of it): y_poly[i] = 2^x[i] from the FMA-pipe
+ * polynomial that evaluates part of each row's exponentials, y_sfu[i] =
+ * 2^x[i] from the SFU instruction that evaluates the rest.  x, y_poly,
+ * y_sfu: n fp32 device values.  One kernel launch. */
+ATTN_API attn_status attn_debug_exp2(const float *x, float *y_poly, float *y_sfu, long long n,
+                                     void *stream);
+
 /* Static string naming a status code (never NULL). */
 ATTN_API const char *attn_status_str(attn_status s);
 

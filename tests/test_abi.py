@@ -88,6 +88,17 @@ def test_prefill_e4m3_blocks_host_validation(L):
     assert L.attn_last_launch_count() == 0
 
 
+def test_debug_prefill_timeout_host_validation(L):
+    def call(limit=300, d=128, ind=1):
+        return L.attn_debug_prefill_timeout(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 1, 128, 128, d,
+                                            1, 0.1, ind, 2, limit, None)
+    assert call(limit=0) == attn.ERR_INVALID
+    assert call(limit=2000000) == attn.ERR_INVALID
+    assert call(d=256) == attn.ERR_UNSUPPORTED                         # hook is in the d<=128 kernel
+    assert call(ind=3) == attn.ERR_UNSUPPORTED                         # 16-bit inputs only
+    assert L.attn_last_launch_count() == 0
+
+
 def test_rotate_quantize_host_validation(L):
     def call(**kw):
         a = dict(X=FAKE, heads=2, rows=100, d=128, rpb=128, ind=1)
