@@ -24,8 +24,7 @@ EXPORTS = ("attn_prefill", "attn_prefill_from_host", "attn_prefill_from_host_hea
            "attn_decode_tokens", "attn_kv_append", "attn_backward",
            "attn_backward_workspace_bytes", "attn_rotate_quantize_e4m3",
            "attn_prefill_e4m3_blocks", "attn_last_error", "attn_status_str",
-           "attn_last_launch_count", "attn_decode_static_ws", "attn_debug_prefill_timeout",
-           "attn_debug_exp2")
+           "attn_last_launch_count", "attn_decode_static_ws", "attn_debug_prefill_timeout")
 
 # Rows per E4M3 scale block in prefill_e4m3_blocks (ATTN_E4M3_SCALE_BLOCK).
 E4M3_SCALE_BLOCK = 128
@@ -89,8 +88,6 @@ def lib():
         L.attn_debug_prefill_timeout.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                  i32, i32, f32, i32, i32, ctypes.c_uint, vp]
         L.attn_debug_prefill_timeout.restype = i32
-        L.attn_debug_exp2.argtypes = [vp, vp, vp, ctypes.c_longlong, vp]
-        L.attn_debug_exp2.restype = i32
         L.attn_last_error.argtypes = [vp]
         L.attn_last_error.restype = i32
         L.attn_status_str.argtypes = [i32]

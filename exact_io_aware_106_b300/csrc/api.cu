@@ -457,39 +457,6 @@ attn_status attn_debug_prefill_timeout(const void *Q, const void *K, const void 
     return ATTN_OK;
 }
 
-} // extern "C"
-
-namespace {
-
-// Both exponentials the prefill's softmax uses, elementwise, for the test
-// of the polynomial against the SFU and the exact values.
-__global__ void debug_exp2_kernel(const float *__restrict__ x, float *__restrict__ y_poly,
-                                  float *__restrict__ y_sfu, long long n) {
-    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= n)
-        return;
-    const float v = x[i];
-    y_poly[i] = attn::ex2_poly2(make_float2(v, v)).x;
-    y_sfu[i] = attn::ex2(v);
-}
-
-} // namespace
-
-extern "C" {
-
-attn_status attn_debug_exp2(const float *x, float *y_poly, float *y_sfu, long long n,
-                            void *stream) {
-    t_last_launches = 0;
-    if (!x || !y_poly || !y_sfu || n <= 0 || n > (1LL << 34))
-        return ATTN_ERR_INVALID;
-    const unsigned grid = static_cast<unsigned>((n + 255) / 256);
-    debug_exp2_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y_poly, y_sfu, n);
-    if (cudaGetLastError() != cudaSuccess)
-        return ATTN_ERR_CUDA;
-    t_last_launches = 1;
-    return ATTN_OK;
-}
-
 attn_status attn_last_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)

@@ -471,33 +471,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// 2^x for two values on the FMA pipe instead of the SFU, for x <= 2^22
-// (the softmax passes x <= 8).  Range reduction 2^x = 2^j * 2^f with
-// j = rint(x), |f| <= 1/2 (exact: adding 1.5 * 2^23 rounds x to an integer
-// and leaves j in the low mantissa bits of the sum), then the degree-4
-// minimax polynomial p(f) = 1 + a1 f + ... + a4 f^4 of 2^f (relative error
-// 2.8e-6; exp2_poly.py derives the coefficients), and 2^j added to p's
-// exponent field as the integer j << 23 taken from the same sum.  x is
-// clamped to -127 first: f is then 0 and p exactly 1, so the result is
-// exactly +0 for x <= -127 (and for -inf); results below 2^-126 are tiny
-// positive values instead of exact.
-__device__ __forceinline__ float2 ex2_poly2(float2 x) {
-    constexpr float kA1 = 0x1.62e12ap-1f, kA2 = 0x1.ec0382p-3f, kA3 = 0x1.c9fd1ep-5f,
-                    kA4 = 0x1.3a007ap-7f;
-    constexpr float kRound = 12582912.0f; // 1.5 * 2^23
-    x.x = fmaxf(x.x, -127.0f);
-    x.y = fmaxf(x.y, -127.0f);
-    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
-    const float2 j = __fadd2_rn(t, make_float2(-kRound, -kRound));      // rint(x), exact
-    const float2 f = __ffma2_rn(j, make_float2(-1.0f, -1.0f), x);        // x - j, exact
-    float2 p = __ffma2_rn(make_float2(kA4, kA4), f, make_float2(kA3, kA3));
-    p = __ffma2_rn(p, f, make_float2(kA2, kA2));
-    p = __ffma2_rn(p, f, make_float2(kA1, kA1));
-    p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
-    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
-
 // max(a, b, c) in one instruction (three-input max, sm_100 and later).
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float y;

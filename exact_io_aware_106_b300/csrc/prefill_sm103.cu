@@ -63,16 +63,7 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kConvWarp = 10;
 constexpr int kSplitKeys = 512; // rows seeing fewer keys carry the P residual
-// Pairs of every 16 whose exponentials run on the FMA pipe (exp_pack_store),
-// per head size of the two-tile kernel.
-#ifndef ATTN_POLY_PAIRS_D64
-#define ATTN_POLY_PAIRS_D64 6
-#endif
-#ifndef ATTN_POLY_PAIRS_D128
-#define ATTN_POLY_PAIRS_D128 4
-#endif
-template <int D>
-constexpr int kPolyPairs = D == 64 ? ATTN_POLY_PAIRS_D64 : ATTN_POLY_PAIRS_D128;
+
 constexpr float kRescaleThreshold = 8.0f;
 // Registers per thread: 384 threads launch with 168 each (the most that three
 // warps per SM sub-partition allow); the producer / MMA / converter
@@ -118,6 +109,7 @@ struct Cfg {
 
 struct Shape {
     int B, Hq, Hkv, G, n_q, n_kv, causal, nqb;
+    int kvg;     // (batch, KV head) pairs per group of the CTA order (work_item)
     float c;     // scale * log2(e)
     float scale; // for reference only
 };
@@ -279,19 +271,27 @@ __device__ __forceinline__ int paged_len_or_reject(const Paged &pg, const Shape 
     return -1;
 }
 
-// CTA index -> (query block, batch, head): (batch, KV head) slowest, then
-// query blocks in descending order (heaviest causal work first), then the G
-// query heads of the group.  The CTAs resident at one time then belong to
-// one or two KV heads, whose K / V (16.8 MB per KV head at n = 32768,
-// d = 128) stay in L2 while all of the group's query heads and query blocks
-// stream them; with (batch, head) fastest the resident CTAs spread over
-// every KV head and their K / V together outgrow L2.
+// CTA index -> (query block, batch, head).  The (batch, KV head) pairs are
+// taken in groups of kvg; within a group the query blocks run in descending
+// order (heaviest causal work first), then the group's pairs and the G query
+// heads of each.  The host sizes a group so that its K / V fit in L2 with
+// room to spare: the CTAs resident at one time then stream K / V that stay in
+// L2 while all the group's query heads and query blocks read them (at
+// n = 32768, d = 128, one KV head's K / V are 16.8 MB, and with every head
+// resident at once they outgrow L2 and are re-read from DRAM about 23
+// times), while the readers of any one line stay spread over the group's
+// pairs and query blocks.  When all K / V fit, the whole grid is one group:
+// heaviest query blocks of every head first.
 __device__ __forceinline__ void work_item(const Shape &sh, int idx, int &qb, int &b, int &h) {
-    const int per_kv = sh.nqb * sh.G;
-    const int kvi = idx / per_kv, rem = idx % per_kv;
-    qb = sh.nqb - 1 - rem / sh.G;
-    b = kvi / sh.Hkv;
-    h = (kvi % sh.Hkv) * sh.G + rem % sh.G;
+    const int per_group = sh.nqb * sh.kvg * sh.G;
+    const int grp = idx / per_group, rem = idx % per_group;
+    const int kvg = min(sh.kvg, sh.B * sh.Hkv - grp * sh.kvg); // the last group may be smaller
+    const int width = kvg * sh.G;
+    qb = sh.nqb - 1 - rem / width;
+    const int inner = rem % width;
+    const int pair = grp * sh.kvg + inner / sh.G;
+    b = pair / sh.Hkv;
+    h = (pair % sh.Hkv) * sh.G + inner % sh.G;
 }
 
 __device__ __forceinline__ int tile_blocks(const Shape &sh, int q0, int t) {
@@ -318,10 +318,7 @@ __device__ __forceinline__ bool tile_split(const Shape &sh, int q0, int t) {
 // Returns the row sum of p (fp32, eight independent partial sums).  The
 // score scaling and the sums run as packed pairs (fma/add .f32x2: one
 // instruction per two elements, each lane rounded as the scalar form).
-// NPOLY of every 16 pairs take 2^x from the polynomial on the FMA pipe
-// (ex2_poly2) instead of the SFU, spread evenly over the 16, so that the
-// two pipes share the exponentials.
-template <int NB, bool BF16, bool SPLIT, int NPOLY>
+template <int NB, bool BF16, bool SPLIT>
 __device__ __forceinline__ float exp_pack_store(const float (&s)[NB], float c, float neg,
                                                 uint32_t tS) {
     float2 acc[4];
@@ -336,8 +333,7 @@ __device__ __forceinline__ float exp_pack_store(const float (&s)[NB], float c, f
         for (int i = 0; i < 16; ++i) {
             const float2 x =
                 __ffma2_rn(make_float2(s[ch * 32 + 2 * i], s[ch * 32 + 2 * i + 1]), c2, n2);
-            const float2 p = ((i * NPOLY) % 16 < NPOLY) ? ex2_poly2(x)
-                                                         : make_float2(ex2(x.x), ex2(x.y));
+            const float2 p = make_float2(ex2(x.x), ex2(x.y));
             acc[i & 3] = __fadd2_rn(acc[i & 3], p);
             hi[i] = pack2<BF16>(p.x, p.y);
             if constexpr (SPLIT)
@@ -413,10 +409,9 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- work item: the CTAs sharing one (sequence, KV head) -- all its
-    // query blocks, heaviest first, and the G heads of the group -- are
-    // adjacent, so that its K/V (read by every one of them) streams from
-    // DRAM about once and is reused from L2.
+    // ---- work item: query blocks heaviest first within groups of (sequence,
+    // KV head) pairs sized for L2 (paged: one pair per group), so that the
+    // K/V read by the group's CTAs stream from DRAM about once.
     int qb, b, h;
     work_item(sh, static_cast<int>(blockIdx.x), qb, b, h);
     const int bh = b * sh.Hq + h;
@@ -769,8 +764,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             const float alpha =
                 (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
             const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
-            const float sum = split ? exp_pack_store<BN, PB, true, kPolyPairs<D>>(s, c, neg, tS)
-                                    : exp_pack_store<BN, PB, false, kPolyPairs<D>>(s, c, neg, tS);
+            const float sum = split ? exp_pack_store<BN, PB, true>(s, c, neg, tS)
+                                    : exp_pack_store<BN, PB, false>(s, c, neg, tS);
             // O_t holds the sum over earlier blocks (their MMAs completed
             // before S_t of this block was produced); rescale it in place.
             if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
@@ -1254,8 +1249,8 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
                     tmem_st32(tO + ch * 32, u);
                 }
             }
-            const float sum = split ? pf::exp_pack_store<BN, PB, true, 0>(s, c, neg, tS)
-                                    : pf::exp_pack_store<BN, PB, false, 0>(s, c, neg, tS);
+            const float sum = split ? pf::exp_pack_store<BN, PB, true>(s, c, neg, tS)
+                                    : pf::exp_pack_store<BN, PB, false>(s, c, neg, tS);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -1331,8 +1326,28 @@ static bool make_map(CUtensorMap *m, const void *ptr, int d, int n, int bh, bool
     return make_tmap_3d(m, ptr, el, dims, strides, box, pw);
 }
 
+// K / V bytes the CTAs of one group of the grid order may share through L2
+// (a third of its 126 MB).
+#ifndef ATTN_KV_GROUP_BYTES
+#define ATTN_KV_GROUP_BYTES (40ll << 20)
+#endif
+
+// (batch, KV head) pairs per group of the CTA order (pf::work_item): as many
+// as keep the group's K / V within ATTN_KV_GROUP_BYTES, at least one.  Paged
+// prefill takes one pair (one sequence's cache) per group.
+static int kv_group(const PrefillArgs &a) {
+    const long long pairs = static_cast<long long>(a.B) * a.Hkv;
+    if (a.paged)
+        return 1;
+    const long long esz = a.e4m3 ? 1 : 2;
+    const long long per_pair = 2ll * a.n_kv * a.d * esz;
+    const long long g = ATTN_KV_GROUP_BYTES / (per_pair > 0 ? per_pair : 1);
+    return static_cast<int>(g < 1 ? 1 : (g > pairs ? pairs : g));
+}
+
 static pf::Shape make_shape(const PrefillArgs &a, int rows_per_cta) {
     pf::Shape sh;
+    sh.kvg = kv_group(a);
     sh.B = a.B;
     sh.Hq = a.Hq;
     sh.Hkv = a.Hkv;

@@ -339,14 +339,6 @@ ATTN_API attn_status attn_debug_prefill_timeout(const void *Q, const void *K, co
                                                 attn_dtype out_dtype, unsigned wait_limit_us,
                                                 void *stream);
 
-/* Test entry point for the exponential of the prefill's softmax (the method
- * has no counterpart of it): y_poly[i] = 2^x[i] from the FMA-pipe
- * polynomial that evaluates part of each row's exponentials, y_sfu[i] =
- * 2^x[i] from the SFU instruction that evaluates the rest.  x, y_poly,
- * y_sfu: n fp32 device values.  One kernel launch. */
-ATTN_API attn_status attn_debug_exp2(const float *x, float *y_poly, float *y_sfu, long long n,
-                                     void *stream);
-
 /* Static string naming a status code (never NULL). */
 ATTN_API const char *attn_status_str(attn_status s);
 
