@@ -140,6 +140,11 @@ struct Lay {
     static constexpr int NST = KV8 ? (D == 64 ? 24 : (D == 128 ? 16 : 8))
                                    : (D == 64 ? 12 : (D == 128 ? 8 : 4));
     static_assert(NST % GW == 0, "each stage must belong to one consumer warp per group");
+    // producer lanes issuing copies side by side: four for units up to 8 KB,
+    // one for 16 KB units (16-bit caches at d = 256), which one lane keeps
+    // up with and which four lanes slowed down
+    static constexpr int ISSUE_LANES = STAGE >= 16384 ? 1 : 4;
+    static_assert(NST % ISSUE_LANES == 0, "each stage must belong to one producer lane");
     static constexpr int MIN_CTAS = min_ctas<D, NRT, NG>();
     static constexpr int QROW = 2 * D + 16;                // padded q row (16-bit caches)
     static constexpr int QBYTES1 = KV8 ? (D / 16) * 32 * 16 : 16 * QROW; // one row tile
@@ -352,11 +357,20 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT, NG>::MIN_CTAS)
 
     if (warp == kNC) {
         // ------------------------------------------------ producer warp
-        if (lane == 0) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            int issued = 0;
-            for (int u = 0; u < nunits; ++u) {
+        // IL lanes issue at once, lane i the units i, i + IL, ...: each unit
+        // costs its lane a stage wait and an expect-tx arrival of a few hundred
+        // cycles besides the copies, so with one issuing lane the cells with
+        // small units (16 tokens x 64 bytes of K and of V) could not keep HBM
+        // busy.  The lanes divide the stages among them (NST is a multiple of
+        // IL), so each stage is refilled, waited on and drained by one lane.
+        constexpr int IL = Ly::ISSUE_LANES;
+        if (lane < IL) {
+            if (lane == 0) {
+                prefetch_tmap(&tm_k);
+                prefetch_tmap(&tm_v);
+            }
+            int last = -1; // last unit this lane issued
+            for (int u = lane; u < nunits; u += IL) {
                 const int st = u % Ly::NST;
                 if (u >= Ly::NST &&
                     !mbar_wait(b_empty(st), ((u / Ly::NST) - 1) & 1, abort_flag, err))
@@ -371,11 +385,11 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT, NG>::MIN_CTAS)
                     tma_load_3d(dst + Ly::HALF + p * Ly::PANEL_BYTES, &tm_v, b_full(st), x, y,
                                 blk_ids[u]);
                 }
-                issued = u + 1;
+                last = u;
             }
             if (*abort_flag) {
-                // let copies already in flight land before the CTA exits
-                for (int u = max(0, issued - Ly::NST); u < issued; ++u)
+                // let this lane's copies in flight land before the CTA exits
+                for (int u = last; u >= 0 && u > last - Ly::NST; u -= IL)
                     mbar_wait_drain(b_full(u % Ly::NST), (u / Ly::NST) & 1);
             }
         }
