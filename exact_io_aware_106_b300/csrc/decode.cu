@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(D)
                           const int32_t *__restrict__ seq_lens, OutT *__restrict__ O,
                           float *__restrict__ lse, int Hq, int T, int block_size,
                           int max_blocks, int max_seq_len, int tps, int max_splits) {
+    // the split kernel's partials are complete and visible past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int sh = blockIdx.x; // (sequence, query head, new token)
     const int s = sh / (Hq * T);
     const int e = threadIdx.x;
@@ -215,6 +217,9 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT, NG>::MIN_CTAS)
     using Ly = Lay<D, KV8, NRT, NG>;
     constexpr int NTC = Ly::NTC, GW = Ly::GW;
     constexpr bool MB = KV8 ? false : QBF16; // operand format of the MMAs (bf16 or f16)
+    // the combine kernel may start launching once every CTA of this grid has
+    // started; it waits for this grid's completion before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u; // swizzle atoms repeat every 1 KB
@@ -732,11 +737,28 @@ size_t decode_workspace_bytes(int num_seqs, int Hq, int d, int max_seq_len) {
 }
 
 template <int D, typename OutT>
+// The combine kernel is launched as a programmatic dependent of the split
+// kernel: its launch and CTA set-up overlap the split kernel's last CTAs,
+// and each of its CTAs waits (griddepcontrol.wait) until the split kernel
+// has finished and its partials are visible.
 static cudaError_t launch_combine(const DecodeArgs &a, const float2 *ws_ml, const float *ws_u,
                                   int tps, int max_splits, cudaStream_t st) {
-    dec::decode_combine_kernel<D, OutT><<<a.num_seqs * a.Hq * a.T, D, 0, st>>>(
-        ws_ml, ws_u, a.seq_lens, static_cast<OutT *>(a.O), a.lse, a.Hq, a.T, a.block_size,
-        a.max_blocks, a.max_seq_len, tps, max_splits);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.num_seqs * a.Hq * a.T), 1, 1);
+    cfg.blockDim = dim3(D, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, dec::decode_combine_kernel<D, OutT>, ws_ml, ws_u, a.seq_lens,
+        static_cast<OutT *>(a.O), a.lse, a.Hq, a.T, a.block_size, a.max_blocks, a.max_seq_len, tps,
+        max_splits);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
