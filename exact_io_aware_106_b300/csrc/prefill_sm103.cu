@@ -372,7 +372,8 @@ template <int D, bool BF16, bool F8, bool PAGED, int OUT>
 __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, void *__restrict__ O,
+                   const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_o, void *__restrict__ O,
                    float *__restrict__ lse, const Shape sh_in, const Scales sc, const Paged pg,
                    unsigned *err) {
     using C = Cfg<D, F8>;
@@ -796,7 +797,47 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         if (ok && nb[t] > 0)
             ok = mbar_wait_warp(b_ofull, 0, abort_flag, err);
         tc_fence_after();
-        if (nb[t] > 0) {
+        // 16-bit O of 16-bit inputs leaves through TMA: each warp stages its
+        // 32 rows in the tile's Q buffer (free once the O-full barrier has
+        // passed: every product has completed) in the Q tile's own swizzled
+        // layout and stores them with one tensor copy per 64-column panel, so
+        // O reaches L2 as whole lines instead of 16-byte pieces of 32 rows.
+        // After an abort the plain stores below write the zero rows (a Q copy
+        // might still be landing in that buffer).
+        constexpr bool TMA_O = !F8 && OUT != 2;
+        if (TMA_O && nb[t] > 0 && ok) {
+            const float inv = l > 0.f ? 1.0f / l : 0.f;
+            const uint32_t sO = sQ + t * C::Q_TILE_BYTES + quarter * 32 * 128;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t u[32];
+                tmem_ld32(tO + ch * 32, u);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack2<OUT == 1>(__uint_as_float(u[2 * i]) * inv,
+                                           __uint_as_float(u[2 * i + 1]) * inv);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int c = ch * 4 + k; // 16-byte chunk of the row
+                    sts_v4(sO + (c / 8) * (BM * 128) + swz_offset<128>(lane, c % 8), w[4 * k],
+                           w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                }
+            }
+            fence_proxy_async_smem(); // generic writes -> TMA reads
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int p = 0; p < D / 64; ++p)
+                    tma_store_3d(&tm_o, sO + p * (BM * 128), p * 64, r0 + quarter * 32, bh);
+                bulk_commit_group();
+                bulk_wait_group_read0(); // the buffer outlives the copy's reads
+            }
+            __syncwarp();
+            if (lse != nullptr && row_g < sh.n_q)
+                lse[static_cast<size_t>(bh) * sh.n_q + row_g] =
+                    (m + __log2f(l)) * 0.69314718055994530942f;
+        } else if (nb[t] > 0) {
             // ---- epilogue: O = u / l, lse = ln(sum exp(scale * s))
             const bool row_ok = row_g < sh.n_q;
             const float vsc = F8 ? sc.v[bkv] : 1.0f;
@@ -1333,14 +1374,12 @@ static bool make_map(CUtensorMap *m, const void *ptr, int d, int n, int bh, bool
 #endif
 
 // (batch, KV head) pairs per group of the CTA order (pf::work_item): as many
-// as keep the group's K / V within ATTN_KV_GROUP_BYTES, at least one.  Paged
-// prefill takes one pair (one sequence's cache) per group.
+// as keep the group's K / V within ATTN_KV_GROUP_BYTES, at least one (for a
+// paged cache, sized by the longest sequence the call allows).
 static int kv_group(const PrefillArgs &a) {
     const long long pairs = static_cast<long long>(a.B) * a.Hkv;
-    if (a.paged)
-        return 1;
     const long long esz = a.e4m3 ? 1 : 2;
-    const long long per_pair = 2ll * a.n_kv * a.d * esz;
+    const long long per_pair = 2ll * (a.paged ? a.max_seq_len : a.n_kv) * a.d * esz;
     const long long g = ATTN_KV_GROUP_BYTES / (per_pair > 0 ? per_pair : 1);
     return static_cast<int>(g < 1 ? 1 : (g > pairs ? pairs : g));
 }
@@ -1411,10 +1450,19 @@ static pf::Paged make_paged(const PrefillArgs &a) {
 template <int D, bool BF16, bool F8, bool PAGED, int OUT>
 static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
     using C = pf::Cfg<D, F8>;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, a.Q, D, a.n_q, a.B * a.Hq, BF16, F8, pf::BM) ||
         !make_kv_maps(&mk, &mv, a, D, BF16, F8, pf::BN))
         return cudaErrorInvalidValue;
+    // O [B * Hq, n_q, D] in its 16-bit format, 32-row boxes (one warp's rows)
+    // for the TMA-stored epilogue; fp32 and E4M3-input calls store directly
+    // and never read this map
+    if (!F8 && OUT != 2) {
+        if (!make_map(&mo, a.O, D, a.n_q, a.B * a.Hq, OUT == 1, false, 32))
+            return cudaErrorInvalidValue;
+    } else {
+        mo = mq;
+    }
     const pf::Shape sh = make_shape(a, pf::NT * pf::BM);
     const pf::Scales sc = make_scales(a);
     auto kern = pf::prefill_kernel<D, BF16, F8, PAGED, OUT>;
@@ -1440,8 +1488,8 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
     const long long grid = static_cast<long long>(sh.nqb) * a.B * a.Hq;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidValue;
-    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(mq, mk, mv, a.O, a.lse, sh, sc,
-                                                                  make_paged(a), a.err);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(mq, mk, mv, mo, a.O, a.lse, sh,
+                                                                  sc, make_paged(a), a.err);
     return cudaGetLastError();
 }
 
