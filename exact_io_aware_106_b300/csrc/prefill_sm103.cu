@@ -958,7 +958,8 @@ template <bool BF16, bool F8, bool PAGED, int OUT>
 __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
     prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, void *__restrict__ O,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_o, void *__restrict__ O,
                         float *__restrict__ lse, const pf::Shape sh_in, const pf::Scales sc,
                         const pf::Paged pg, unsigned *err) {
     using C = Cfg<F8>;
@@ -1303,40 +1304,78 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
         if (ok && nb > 0)
             ok = mbar_wait_warp(b_ofull, 0, abort_flag, err);
         tc_fence_after();
-        const bool row_ok = row_g < sh.n_q;
-        const float vsc = F8 ? sc.v[bkv] : 1.0f;
-        const float inv = (ok && l > 0.f) ? vsc / l : 0.f;
-        const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row_g) * D;
+        // 16-bit O of 16-bit inputs: each warp stages its 32 rows in the Q
+        // buffer (free once O-full has passed) and stores them by TMA, as in
+        // pf::prefill_kernel; after an abort the plain stores write zeros
+        constexpr bool TMA_O = !F8 && OUT != 2;
+        if (TMA_O && ok && nb > 0) {
+            const float inv = l > 0.f ? 1.0f / l : 0.f;
+            const uint32_t sO = sQ + warp * 32 * 128;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t u[32];
-            tmem_ld32(tO + ch * 32, u);
-            if (row_ok) {
-                float o[32];
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t u[32];
+                tmem_ld32(tO + ch * 32, u);
+                uint32_t w[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    o[i] = ok ? __uint_as_float(u[i]) * inv : 0.f;
-                if constexpr (OUT == 2) {
-                    float4 *dst =
-                        reinterpret_cast<float4 *>(static_cast<float *>(O) + orow + ch * 32);
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack2<OUT == 1>(__uint_as_float(u[2 * i]) * inv,
+                                           __uint_as_float(u[2 * i + 1]) * inv);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                } else {
-                    uint4 *dst =
-                        reinterpret_cast<uint4 *>(static_cast<uint16_t *>(O) + orow + ch * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pack2<OUT == 1>(o[8 * i], o[8 * i + 1]),
-                                            pack2<OUT == 1>(o[8 * i + 2], o[8 * i + 3]),
-                                            pack2<OUT == 1>(o[8 * i + 4], o[8 * i + 5]),
-                                            pack2<OUT == 1>(o[8 * i + 6], o[8 * i + 7]));
+                for (int k = 0; k < 4; ++k) {
+                    const int c = ch * 4 + k; // 16-byte chunk of the row
+                    sts_v4(sO + (c / 8) * (BM * 128) + swz_offset<128>(lane, c % 8), w[4 * k],
+                           w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
                 }
             }
+            fence_proxy_async_smem(); // generic writes -> TMA reads
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int p = 0; p < D / 64; ++p)
+                    tma_store_3d(&tm_o, sO + p * (BM * 128), p * 64, r0 + warp * 32, bh);
+                bulk_commit_group();
+                bulk_wait_group_read0(); // the buffer outlives the copy's reads
+            }
+            __syncwarp();
+            if (lse != nullptr && row_g < sh.n_q)
+                lse[static_cast<size_t>(bh) * sh.n_q + row_g] =
+                    (m + __log2f(l)) * 0.69314718055994530942f;
+        } else {
+            const bool row_ok = row_g < sh.n_q;
+            const float vsc = F8 ? sc.v[bkv] : 1.0f;
+            const float inv = (ok && l > 0.f) ? vsc / l : 0.f;
+            const size_t orow = (static_cast<size_t>(bh) * sh.n_q + row_g) * D;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t u[32];
+                tmem_ld32(tO + ch * 32, u);
+                if (row_ok) {
+                    float o[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = ok ? __uint_as_float(u[i]) * inv : 0.f;
+                    if constexpr (OUT == 2) {
+                        float4 *dst =
+                            reinterpret_cast<float4 *>(static_cast<float *>(O) + orow + ch * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    } else {
+                        uint4 *dst =
+                            reinterpret_cast<uint4 *>(static_cast<uint16_t *>(O) + orow + ch * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack2<OUT == 1>(o[8 * i], o[8 * i + 1]),
+                                                pack2<OUT == 1>(o[8 * i + 2], o[8 * i + 3]),
+                                                pack2<OUT == 1>(o[8 * i + 4], o[8 * i + 5]),
+                                                pack2<OUT == 1>(o[8 * i + 6], o[8 * i + 7]));
+                    }
+                }
+            }
+            if (lse != nullptr && row_ok)
+                lse[static_cast<size_t>(bh) * sh.n_q + row_g] =
+                    ok ? (m + __log2f(l)) * 0.69314718055994530942f : __int_as_float(0x7fc00000);
         }
-        if (lse != nullptr && row_ok)
-            lse[static_cast<size_t>(bh) * sh.n_q + row_g] =
-                ok ? (m + __log2f(l)) * 0.69314718055994530942f : __int_as_float(0x7fc00000);
     }
 
     tc_fence_before();
@@ -1496,10 +1535,16 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t st) {
 template <bool BF16, bool F8, bool PAGED, int OUT>
 static cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t st) {
     using C = pfw::Cfg<F8>;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, a.Q, pfw::D, a.n_q, a.B * a.Hq, BF16, F8, pfw::BM) ||
         !make_kv_maps(&mk, &mv, a, pfw::D, BF16, F8, pfw::Cfg<F8>::BN))
         return cudaErrorInvalidValue;
+    if (!F8 && OUT != 2) { // 32-row boxes of O for the TMA-stored epilogue
+        if (!make_map(&mo, a.O, pfw::D, a.n_q, a.B * a.Hq, OUT == 1, false, 32))
+            return cudaErrorInvalidValue;
+    } else {
+        mo = mq;
+    }
     const pf::Shape sh = make_shape(a, pfw::BM);
     const pf::Scales sc = make_scales(a);
     auto kern = pfw::prefill_wide_kernel<BF16, F8, PAGED, OUT>;
@@ -1510,8 +1555,8 @@ static cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t st) {
     const long long grid = static_cast<long long>(sh.nqb) * a.B * a.Hq;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidValue;
-    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(mq, mk, mv, a.O, a.lse, sh, sc,
-                                                                  make_paged(a), a.err);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(mq, mk, mv, mo, a.O, a.lse, sh,
+                                                                  sc, make_paged(a), a.err);
     return cudaGetLastError();
 }
 
