@@ -102,6 +102,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Three waits at once: the three try_waits are issued back to back, so that
+// when all phases have already completed (the common case in a pipeline
+// whose producers run ahead) their latencies overlap instead of adding up;
+// otherwise each one not yet seen complete is waited for (bounded) in turn.
+// A barrier with `need` false is not tested.
+__device__ __forceinline__ bool mbar_wait3(uint32_t b0, uint32_t p0, bool need0, uint32_t b1,
+                                           uint32_t p1, bool need1, uint32_t b2, uint32_t p2,
+                                           bool need2, volatile int *abort_flag,
+                                           unsigned *err) {
+    const bool d0 = !need0 || mbar_try_wait(b0, p0);
+    const bool d1 = !need1 || mbar_try_wait(b1, p1);
+    const bool d2 = !need2 || mbar_try_wait(b2, p2);
+    if (d0 && d1 && d2)
+        return true;
+    return (d0 || mbar_wait(b0, p0, abort_flag, err)) && (d1 || mbar_wait(b1, p1, abort_flag, err)) &&
+           (d2 || mbar_wait(b2, p2, abort_flag, err));
+}
+
 // mbar_wait by a whole warp whose next instructions are warp-wide
 // (.sync.aligned tensor-memory loads, ldmatrix, mma.sync): the result is the
 // same in every lane, so a wait that gives up in one lane never leaves the

@@ -638,21 +638,34 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                     const int vs = j % C::NV;
                     const int kn = j + 1, ks = kn % C::NK;
                     const bool need_k = kn < nb_max;
-                    if (!mbar_wait(b_vfull(vs), (j / C::NV) & 1, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
-                    if (need_k && !mbar_wait(b_kfull(ks), (kn / C::NK) & 1, abort_flag, err)) {
+                    // At d = 128, V(j), K(j+1) and tile 0's P(j) are usually
+                    // all there by now: one fused wait instead of three in a
+                    // row (each satisfied wait costs the issuing thread ~100
+                    // cycles while the tensor core drains its short queue; a
+                    // clock64 trace: 305 -> 120-170 cycles, block period
+                    // 3070 -> 2930).  At d = 64 the softmax is the bound and
+                    // the fused form measured slower, so it waits in turn.
+                    constexpr bool kFused = D == 128;
+                    const bool waited =
+                        kFused ? mbar_wait3(b_vfull(vs), (j / C::NV) & 1, true, b_kfull(ks),
+                                            (kn / C::NK) & 1, need_k, b_pfull(0), j & 1,
+                                            j < nb[0], abort_flag, err)
+                               : (mbar_wait(b_vfull(vs), (j / C::NV) & 1, abort_flag, err) &&
+                                  (!need_k || mbar_wait(b_kfull(ks), (kn / C::NK) & 1,
+                                                        abort_flag, err)));
+                    if (!waited) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (j < nb[0]) {
-                        if (!mbar_wait(b_pfull(0), j & 1, abort_flag, err)) {
-                            ok = false;
-                            break;
+                        if (!kFused) {
+                            if (!mbar_wait(b_pfull(0), j & 1, abort_flag, err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
                         }
-                        tc_fence_after();
                         issue_pv(0, vs, j == 0);
                         if (kn < nb[0]) {
                             issue_qk(0, ks);
