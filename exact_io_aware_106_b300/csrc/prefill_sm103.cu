@@ -294,6 +294,40 @@ __device__ __forceinline__ void work_item(const Shape &sh, int idx, int &qb, int
     h = (pair % sh.Hkv) * sh.G + inner % sh.G;
 }
 
+// Paged calls: the sequence at position pos of the CTA order when the
+// sequences are taken longest first (ties by index), so that the long ones
+// do not make the last wave's tail.  Each warp ranks the seq_lens entries
+// itself with shuffles (rank of c = the entries ordered before it; a total
+// order, so any lengths give a permutation).  Calls with more than
+// kLongestFirstMaxB sequences keep the given order.
+constexpr int kLongestFirstMaxB = 64;
+
+__device__ __forceinline__ int longest_first(const int32_t *lens, int B, int pos) {
+    if (B > kLongestFirstMaxB)
+        return pos;
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    int found = pos;
+    for (int c0 = 0; c0 < B; c0 += 32) {
+        const int c = c0 + lane;
+        const int mine = c < B ? lens[c] : 0;
+        int rank = 0;
+        for (int k0 = 0; k0 < B; k0 += 32) {
+            const int other = k0 + lane < B ? lens[k0 + lane] : 0;
+#pragma unroll 8
+            for (int i = 0; i < 32; ++i) {
+                const int o = __shfl_sync(full, other, i);
+                const int k = k0 + i;
+                rank += (k < B && (o > mine || (o == mine && k < c))) ? 1 : 0;
+            }
+        }
+        const unsigned hit = __ballot_sync(full, c < B && rank == pos);
+        if (hit)
+            found = c0 + __ffs(hit) - 1;
+    }
+    return found;
+}
+
 __device__ __forceinline__ int tile_blocks(const Shape &sh, int q0, int t) {
     const int r0 = q0 + t * BM;
     if (r0 >= sh.n_q)
@@ -411,10 +445,12 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // ---- work item: query blocks heaviest first within groups of (sequence,
-    // KV head) pairs sized for L2 (paged: one pair per group), so that the
-    // K/V read by the group's CTAs stream from DRAM about once.
+    // KV head) pairs sized for L2, so that the K/V read by the group's CTAs
+    // stream from DRAM about once; paged sequences longest first.
     int qb, b, h;
     work_item(sh, static_cast<int>(blockIdx.x), qb, b, h);
+    if constexpr (PAGED)
+        b = longest_first(pg.lens, sh.B, b);
     const int bh = b * sh.Hq + h;
     const int bkv = b * sh.Hkv + h / sh.G;
     const int q0 = qb * (NT * BM);
@@ -1007,6 +1043,8 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int qb, b, h;
     pf::work_item(sh, static_cast<int>(blockIdx.x), qb, b, h);
+    if constexpr (PAGED)
+        b = pf::longest_first(pg.lens, sh.B, b);
     const int bh = b * sh.Hq + h;
     const int bkv = b * sh.Hkv + h / sh.G;
     const int r0 = qb * BM;

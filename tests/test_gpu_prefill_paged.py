@@ -22,6 +22,12 @@ CASES = [
     (2, 4, 2, 64, 128, [100, 2000], 16, False, "bf16", "f32"),   # non-causal
     (1, 16, 1, 256, 64, [4100], 16, True, "f16", "f32"),         # G = 16
     (2, 4, 2, 200, 256, [205, 1333], 16, True, "f16", "bf16"),
+    # the CTAs take the sequences longest first: equal lengths, and more
+    # sequences than one warp ranks in one pass
+    (37, 2, 1, 16, 64, [16 + 9 * ((3 * i) % 20) for i in range(37)], 16, True, "bf16", "f32"),
+    (33, 2, 2, 40, 256, [40 + 11 * ((7 * i) % 12) for i in range(33)], 32, True, "bf16", "f32"),
+    # more sequences than are ranked: the given order
+    (70, 2, 2, 8, 128, [8 + 7 * ((5 * i) % 33) for i in range(70)], 16, True, "f16", "f32"),
 ]
 
 
