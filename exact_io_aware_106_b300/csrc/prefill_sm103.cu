@@ -145,8 +145,10 @@ struct Paged {
 // the end zeroed: their p is 0, and 0 * (stale non-finite cache contents)
 // must not reach u.  K rows past the end need no care -- their scores are
 // replaced by -inf.  Block ids are fetched one key block ahead, one lane per
-// unit; lane u issues unit u's boxes.
-template <int D, int BN, int NK, int NV>
+// unit; lane u issues unit u's boxes.  DO_K / DO_V select the stream(s) this
+// warp feeds: a warp's TMA instructions are taken one at a time, so with a
+// warp to spare the K and V boxes are issued by two warps.
+template <int D, int BN, int NK, int NV, bool DO_K, bool DO_V>
 __device__ __forceinline__ void paged_kv_producer(
     const Paged &pg, int b, int hkv, int Hkv, int n_kv, int nb_max, const CUtensorMap *tm_k,
     const CUtensorMap *tm_v, uint32_t sK, uint32_t sV, uint32_t kfull0, uint32_t kempty0,
@@ -172,30 +174,32 @@ __device__ __forceinline__ void paged_kv_producer(
         if (j + 1 < nb_max)
             nxt = unit_blk(j + 1);
         bad |= cur == -2;
-        // ---- K
-        const int ks = j % NK;
-        int ok = 1;
-        if (j >= NK) {
-            if (lane == 0)
-                ok = mbar_wait(kempty0 + 8u * ks, ((j / NK) - 1) & 1, abort_flag, err);
-            ok = __shfl_sync(full, ok, 0);
-        }
-        if (!ok)
-            break;
-        if (lane == 0)
-            mbar_arrive_expect_tx(kfull0 + 8u * ks, STAGE);
-        __syncwarp();
-        // lane u issues unit u's boxes: one instruction starts every unit's copy
         const int z = cur >= 0 ? cur : pg.num_blocks;
         const int y = hkv * pg.bs + (j * BN + 16 * lane) % pg.bs;
-        if (lane < UPB) {
+        int ok = 1;
+        if constexpr (DO_K) {
+            const int ks = j % NK;
+            if (j >= NK) {
+                if (lane == 0)
+                    ok = mbar_wait(kempty0 + 8u * ks, ((j / NK) - 1) & 1, abort_flag, err);
+                ok = __shfl_sync(full, ok, 0);
+            }
+            if (!ok)
+                break;
+            if (lane == 0)
+                mbar_arrive_expect_tx(kfull0 + 8u * ks, STAGE);
+            __syncwarp();
+            // lane u issues unit u's boxes: one instruction starts every unit's copy
+            if (lane < UPB) {
 #pragma unroll
-            for (int p = 0; p < PANELS; ++p)
-                tma_load_3d(sK + ks * STAGE + p * BN * 128 + lane * 16 * 128, tm_k,
-                            kfull0 + 8u * ks, p * 64, y, z);
+                for (int p = 0; p < PANELS; ++p)
+                    tma_load_3d(sK + ks * STAGE + p * BN * 128 + lane * 16 * 128, tm_k,
+                                kfull0 + 8u * ks, p * 64, y, z);
+            }
+            k_issued = j + 1;
         }
-        k_issued = j + 1;
-        // ---- V
+        if constexpr (!DO_V)
+            continue;
         const int vs = j % NV;
         if (j >= NV) {
             if (lane == 0)
@@ -236,10 +240,12 @@ __device__ __forceinline__ void paged_kv_producer(
     if (__any_sync(full, bad) && lane == 0)
         atomicOr(err, DERR_INDEX);
     if (lane == 0 && *abort_flag) { // let in-flight copies land before the CTA exits
-        for (int u = max(0, k_issued - NK); u < k_issued; ++u)
-            mbar_wait_drain(kfull0 + 8u * (u % NK), (u / NK) & 1);
-        for (int u = max(0, v_issued - NV); u < v_issued; ++u)
-            mbar_wait_drain(vfull0 + 8u * (u % NV), (u / NV) & 1);
+        if constexpr (DO_K)
+            for (int u = max(0, k_issued - NK); u < k_issued; ++u)
+                mbar_wait_drain(kfull0 + 8u * (u % NK), (u / NK) & 1);
+        if constexpr (DO_V)
+            for (int u = max(0, v_issued - NV); u < v_issued; ++u)
+                mbar_wait_drain(vfull0 + 8u * (u % NV), (u / NV) & 1);
     }
 }
 
@@ -521,11 +527,18 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                             tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q, b_qfull,
                                         p * 64, q0 + t * BM, bh);
             }
-            paged_kv_producer<D, BN, C::NK, C::NV>(pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb_max, &tm_k,
-                                                   &tm_v, sK, sV, b_kfull(0), b_kempty(0),
-                                                   b_vfull(0), b_vempty(0), abort_flag, err, lane);
+            paged_kv_producer<D, BN, C::NK, C::NV, true, false>(
+                pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb_max, &tm_k, &tm_v, sK, sV, b_kfull(0),
+                b_kempty(0), b_vfull(0), b_vempty(0), abort_flag, err, lane);
             if (lane == 0 && *abort_flag)
                 mbar_wait_drain(b_qfull, 0);
+        } else if (warp == kConvWarp && PAGED) {
+            // ================================================= paged V producer
+            // (paged inputs are 16-bit: the widening warps are free)
+            static_assert(!PAGED || !F8, "paged inputs are 16-bit");
+            paged_kv_producer<D, BN, C::NK, C::NV, false, true>(
+                pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb_max, &tm_k, &tm_v, sK, sV, b_kfull(0),
+                b_kempty(0), b_vfull(0), b_vempty(0), abort_flag, err, lane);
         } else if (warp == kProducerWarp) {
             // ================================================= TMA producer
             if (lane == 0) {
@@ -1101,9 +1114,9 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
             for (int p = 0; p < C::QK_PANELS; ++p)
                 tma_load_3d(sQ + p * BM * C::PW, &tm_q, b_qfull, p * 64, r0, bh);
         }
-        pf::paged_kv_producer<D, BN, NK, NV>(pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb, &tm_k, &tm_v,
-                                             sK, sV, b_kfull(0), b_kempty(0), b_vfull(0),
-                                             b_vempty(0), abort_flag, err, lane);
+        pf::paged_kv_producer<D, BN, NK, NV, true, true>(
+            pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb, &tm_k, &tm_v, sK, sV, b_kfull(0), b_kempty(0),
+            b_vfull(0), b_vempty(0), abort_flag, err, lane);
         if (lane == 0 && *abort_flag)
             mbar_wait_drain(b_qfull, 0);
     } else if (warp == kProducerWarp) {
