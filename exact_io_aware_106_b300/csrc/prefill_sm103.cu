@@ -88,7 +88,11 @@ struct Cfg {
     static constexpr int V_BYTES = BN * D * 2;              // 16-bit V operand stage
     static constexpr int VS_BYTES = BN * D;                 // E4M3 V staging
     static constexpr int NK = (F8 || D == 64) ? 3 : 2;      // K stages
-    static constexpr int NV = D == 64 ? 3 : 2;              // V stages
+    static constexpr int NV = (D == 64 || !F8) ? 3 : 2;     // V stages
+    // 16-bit d = 128: V stages are released by the softmax warps (below)
+    // instead of a commit of the MMA-issuing thread, one block later; the
+    // third V stage covers the delay
+    static constexpr bool SOFTMAX_FREES_V = !F8 && D == 128;
     static constexpr int NVS = F8 ? 2 : 0;                  // E4M3 V staging buffers
     static constexpr int NCONV = F8 ? 2 : 0;                // V widening warps
     static constexpr int THREADS = kThreadsAll; // warps 10-11 idle for 16-bit inputs
@@ -680,7 +684,6 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                                 issue_qk(t, 0);
                                 tc_commit(b_sfull(t));
                             }
-                        tc_commit(b_kempty(0));
                     }
                 }
                 for (int j = 0; ok && j < nb_max; ++j) {
@@ -729,13 +732,14 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                         tc_fence_after();
                         issue_pv(1, vs, j == 0);
                     }
-                    tc_commit(b_vempty(vs));
+                    if constexpr (!C::SOFTMAX_FREES_V)
+                        tc_commit(b_vempty(vs));
                     if (j < nb[1] && kn < nb[1]) {
                         issue_qk(1, ks);
                         tc_commit(b_sfull(1));
                     }
-                    if (need_k)
-                        tc_commit(b_kempty(ks));
+                    // K(j+1) is released by the softmax warps that wait for
+                    // the last S product reading it (below)
                 }
                 if (ok)
                     tc_commit(b_ofull);
@@ -780,6 +784,16 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
 
+        // The tile whose S product is the last to read each K stage (tile
+        // 1, which has at least tile 0's blocks, unless it lies past n_q)
+        // releases the stage once its S-full phase has passed: the commit
+        // behind it tracks every earlier product of the issuing thread, so
+        // no product still reads K(j) -- nor V(j-1), whose P.V products were
+        // issued before S(j).  An arrive from this side replaces a commit in
+        // the MMA-issuing thread, whose barrier work is what keeps the
+        // tensor core idle between products.  (The last V stage of the
+        // sequence is never released: nothing waits for it.)
+        const bool frees_k = (t == 1 || nb[1] == 0) && quarter == 0 && lane == 0;
         for (int j = 0; j < nb[t]; ++j) {
             const float c = F8 ? cq * k_next : cq;
             if constexpr (F8)
@@ -788,6 +802,11 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             if (!mbar_wait_warp(b_sfull(t), j & 1, abort_flag, err)) {
                 ok = false;
                 break;
+            }
+            if (frees_k) {
+                mbar_arrive(b_kempty(j % C::NK));
+                if (C::SOFTMAX_FREES_V && j > 0)
+                    mbar_arrive(b_vempty((j - 1) % C::NV));
             }
             tc_fence_after();
             float s[BN];
