@@ -141,30 +141,40 @@ struct Paged {
 };
 
 // Whole-warp producer of the K and V blocks (BN keys, 16-bit, D) of one
-// (sequence, KV head) from a block-paged cache: one TMA box (16 tokens x 64
-// elements) per 16-token unit and 128-byte panel, into the same swizzled
-// stage layout dense tiles have.  Units past the sequence end read a block
+// (sequence, KV head) from a block-paged cache: one TMA box (block_size
+// tokens x 64 elements) per cache block ("unit") and 128-byte panel, into
+// the same swizzled stage layout dense tiles have.  Units past the sequence end read a block
 // coordinate past the tensor, which TMA fills with zeros.  The one V unit
 // that holds the sequence end is copied with plain loads and its rows past
 // the end zeroed: their p is 0, and 0 * (stale non-finite cache contents)
 // must not reach u.  K rows past the end need no care -- their scores are
 // replaced by -inf.  Block ids are fetched one key block ahead, one lane per
-// unit; lane u issues unit u's boxes.  DO_K / DO_V select the stream(s) this
-// warp feeds: a warp's TMA instructions are taken one at a time, so with a
-// warp to spare the K and V boxes are issued by two warps.
-template <int D, int BN, int NK, int NV, bool DO_K, bool DO_V>
+// unit; lane u issues unit u's boxes.  [KP0, KP1) and [VP0, VP1) are the
+// 128-byte panels of each K and V row this warp copies (an empty range: not
+// that tensor): a warp's TMA instructions are taken one at a time, so with
+// warps to spare the boxes are spread over several warps.  Each warp
+// arrives once per stage on the full barriers it feeds, announcing its own
+// bytes (the barriers count the warps that feed them).
+template <int D, int BN, int NK, int NV, int KP0, int KP1, int VP0, int VP1>
 __device__ __forceinline__ void paged_kv_producer(
     const Paged &pg, int b, int hkv, int Hkv, int n_kv, int nb_max, const CUtensorMap *tm_k,
     const CUtensorMap *tm_v, uint32_t sK, uint32_t sV, uint32_t kfull0, uint32_t kempty0,
     uint32_t vfull0, uint32_t vempty0, volatile int *abort_flag, unsigned *err, int lane) {
-    constexpr int UPB = BN / 16;                // 16-token units per key block
-    constexpr int PANELS = D / 64;
-    constexpr int STAGE = BN * D * 2;
-    constexpr int UNIT = 16 * 128 * PANELS;     // bytes of one unit
+    const int U = pg.bs;                        // tokens per unit: one cache block
+    const int UPB = BN / U;                     // units per key block (BN % U == 0)
+    constexpr bool DO_K = KP1 > KP0, DO_V = VP1 > VP0;
+    static_assert(0 <= KP0 && KP0 <= KP1 && KP1 <= D / 64, "K panel range");
+    static_assert(0 <= VP0 && VP0 <= VP1 && VP1 <= D / 64, "V panel range");
+    static_assert(DO_K || DO_V, "a producer feeds at least one tensor");
+    constexpr int VNP = VP1 - VP0;
+    constexpr int VCH = VNP > 0 ? VNP * 8 : 1;      // 16-byte chunks of a V row it copies
+    constexpr int K_STAGE = BN * (KP1 - KP0) * 128; // this warp's bytes of a K stage
+    const int v_unit = U * 128 * VNP;               // this warp's bytes of one V unit
+    constexpr int STAGE = BN * D * 2;               // bytes of a whole stage
     const unsigned full = 0xffffffffu;
     const int32_t *trow = pg.table + static_cast<size_t>(b) * pg.max_blocks;
     auto unit_blk = [&](int j) -> int {
-        const int tok = j * BN + 16 * lane;
+        const int tok = j * BN + U * lane;
         if (lane >= UPB || tok >= n_kv)
             return -1;
         const int phys = trow[tok / pg.bs];
@@ -179,7 +189,7 @@ __device__ __forceinline__ void paged_kv_producer(
             nxt = unit_blk(j + 1);
         bad |= cur == -2;
         const int z = cur >= 0 ? cur : pg.num_blocks;
-        const int y = hkv * pg.bs + (j * BN + 16 * lane) % pg.bs;
+        const int y = hkv * pg.bs; // a unit is a whole cache block
         int ok = 1;
         if constexpr (DO_K) {
             const int ks = j % NK;
@@ -191,13 +201,13 @@ __device__ __forceinline__ void paged_kv_producer(
             if (!ok)
                 break;
             if (lane == 0)
-                mbar_arrive_expect_tx(kfull0 + 8u * ks, STAGE);
+                mbar_arrive_expect_tx(kfull0 + 8u * ks, K_STAGE);
             __syncwarp();
             // lane u issues unit u's boxes: one instruction starts every unit's copy
             if (lane < UPB) {
 #pragma unroll
-                for (int p = 0; p < PANELS; ++p)
-                    tma_load_3d(sK + ks * STAGE + p * BN * 128 + lane * 16 * 128, tm_k,
+                for (int p = KP0; p < KP1; ++p)
+                    tma_load_3d(sK + ks * STAGE + p * BN * 128 + lane * U * 128, tm_k,
                                 kfull0 + 8u * ks, p * 64, y, z);
             }
             k_issued = j + 1;
@@ -213,30 +223,29 @@ __device__ __forceinline__ void paged_kv_producer(
         if (!ok)
             break;
         const int rem = n_kv - j * BN; // keys of this block inside the sequence
-        const int up = (rem > 0 && rem < BN && (rem & 15) != 0) ? (rem >> 4) : -1;
+        const int up = (rem > 0 && rem < BN && rem % U != 0) ? rem / U : -1;
         if (up >= 0) {
             const int blk = __shfl_sync(full, cur, up);
-            const int nval = rem & 15;
-            const size_t row0 = (static_cast<size_t>(blk >= 0 ? blk : 0) * Hkv + hkv) * pg.bs +
-                                (j * BN + 16 * up) % pg.bs;
-            for (int i = lane; i < 16 * (D / 8); i += 32) {
-                const int r = i / (D / 8), c = i % (D / 8);
+            const int nval = rem % U;
+            const size_t row0 = (static_cast<size_t>(blk >= 0 ? blk : 0) * Hkv + hkv) * pg.bs;
+            for (int i = lane; i < U * VNP * 8; i += 32) { // U rows x this warp's chunks
+                const int r = i / VCH, c = VP0 * 8 + i % VCH;
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
                 if (r < nval && blk >= 0)
                     v = *reinterpret_cast<const uint4 *>(pg.vcache + (row0 + r) * (D * 2) + c * 16);
-                sts_v4(sV + vs * STAGE + (c / 8) * (BN * 128) + swz_offset<128>(up * 16 + r, c % 8),
+                sts_v4(sV + vs * STAGE + (c / 8) * (BN * 128) + swz_offset<128>(up * U + r, c % 8),
                        v.x, v.y, v.z, v.w);
             }
             fence_proxy_async_smem(); // generic writes -> tensor-core reads
             __syncwarp();
         }
         if (lane == 0)
-            mbar_arrive_expect_tx(vfull0 + 8u * vs, (UPB - (up >= 0 ? 1 : 0)) * UNIT);
+            mbar_arrive_expect_tx(vfull0 + 8u * vs, (UPB - (up >= 0 ? 1 : 0)) * v_unit);
         __syncwarp();
         if (lane < UPB && lane != up) {
 #pragma unroll
-            for (int p = 0; p < PANELS; ++p)
-                tma_load_3d(sV + vs * STAGE + p * BN * 128 + lane * 16 * 128, tm_v,
+            for (int p = VP0; p < VP1; ++p)
+                tma_load_3d(sV + vs * STAGE + p * BN * 128 + lane * U * 128, tm_v,
                             vfull0 + 8u * vs, p * 64, y, z);
         }
         v_issued = j + 1;
@@ -531,7 +540,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                             tma_load_3d(sQ + t * C::Q_TILE_BYTES + p * BM * C::PW, &tm_q, b_qfull,
                                         p * 64, q0 + t * BM, bh);
             }
-            paged_kv_producer<D, BN, C::NK, C::NV, true, false>(
+            paged_kv_producer<D, BN, C::NK, C::NV, 0, D / 64, 0, 0>(
                 pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb_max, &tm_k, &tm_v, sK, sV, b_kfull(0),
                 b_kempty(0), b_vfull(0), b_vempty(0), abort_flag, err, lane);
             if (lane == 0 && *abort_flag)
@@ -540,7 +549,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
             // ================================================= paged V producer
             // (paged inputs are 16-bit: the widening warps are free)
             static_assert(!PAGED || !F8, "paged inputs are 16-bit");
-            paged_kv_producer<D, BN, C::NK, C::NV, false, true>(
+            paged_kv_producer<D, BN, C::NK, C::NV, 0, 0, 0, D / 64>(
                 pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb_max, &tm_k, &tm_v, sK, sV, b_kfull(0),
                 b_kempty(0), b_vfull(0), b_vempty(0), abort_flag, err, lane);
         } else if (warp == kProducerWarp) {
@@ -994,6 +1003,13 @@ constexpr int BM = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kConvWarp = 6;
+// Paged calls: the K and V boxes of a 128-key block (8 units x 4 panels
+// each, 2 KB per box) come from three warps -- the producer warp and warps
+// 6-7, present only then -- since one warp takes its TMA instructions one
+// at a time, and 64 boxes per block from one warp left the tensor core idle
+// about two thirds of the time.  (A ninth warp would cap every thread at
+// 168 registers, three warps per SM sub-partition, and spill the softmax.)
+constexpr int kPagedExtraWarps = 2;
 
 template <bool F8>
 struct Cfg {
@@ -1035,8 +1051,11 @@ __device__ __forceinline__ int tile_blocks(const pf::Shape &sh, int r0) {
     return min(nkb, (r_last + (sh.n_kv - sh.n_q)) / BN + 1);
 }
 
+template <bool F8, bool PAGED>
+constexpr int threads() { return Cfg<F8>::THREADS + (PAGED ? 32 * kPagedExtraWarps : 0); }
+
 template <bool BF16, bool F8, bool PAGED, int OUT>
-__global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
+__global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
     prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
@@ -1092,7 +1111,7 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
         *abort_flag = 0;
         mbar_init(b_qfull, 1);
         for (int i = 0; i < NK; ++i) {
-            mbar_init(b_kfull(i), 1);
+            mbar_init(b_kfull(i), PAGED ? 2 : 1); // paged: two warps copy K
             mbar_init(b_kempty(i), 1);
         }
         for (int i = 0; i < NV; ++i) {
@@ -1126,18 +1145,33 @@ __global__ void __launch_bounds__(Cfg<F8>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kProducerWarp && PAGED) {
-        // ================================================= paged producer
-        if (lane == 0) {
-            mbar_arrive_expect_tx(b_qfull, C::Q_BYTES);
-            for (int p = 0; p < C::QK_PANELS; ++p)
-                tma_load_3d(sQ + p * BM * C::PW, &tm_q, b_qfull, p * 64, r0, bh);
+    if (PAGED && (warp == kProducerWarp || warp >= kConvWarp)) {
+        // ================================================= paged producers
+        // (panels of each 512-byte row) warp 4: Q, K 0-1; warp 6: K 2-3;
+        // warp 7: V 0-3.  No warp copies both tensors: with one K and one V
+        // stage, a K copy queued behind a V-empty wait would hold the next
+        // block's scores back until the previous block's P V had finished.
+        static_assert(!PAGED || C::NCONV == 0, "paged inputs are 16-bit");
+        if (warp == kProducerWarp) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(b_qfull, C::Q_BYTES);
+                for (int p = 0; p < C::QK_PANELS; ++p)
+                    tma_load_3d(sQ + p * BM * C::PW, &tm_q, b_qfull, p * 64, r0, bh);
+            }
+            pf::paged_kv_producer<D, BN, NK, NV, 0, 2, 0, 0>(
+                pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb, &tm_k, &tm_v, sK, sV, b_kfull(0),
+                b_kempty(0), b_vfull(0), b_vempty(0), abort_flag, err, lane);
+            if (lane == 0 && *abort_flag)
+                mbar_wait_drain(b_qfull, 0);
+        } else if (warp == kConvWarp) {
+            pf::paged_kv_producer<D, BN, NK, NV, 2, 4, 0, 0>(
+                pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb, &tm_k, &tm_v, sK, sV, b_kfull(0),
+                b_kempty(0), b_vfull(0), b_vempty(0), abort_flag, err, lane);
+        } else {
+            pf::paged_kv_producer<D, BN, NK, NV, 0, 0, 0, 4>(
+                pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb, &tm_k, &tm_v, sK, sV, b_kfull(0),
+                b_kempty(0), b_vfull(0), b_vempty(0), abort_flag, err, lane);
         }
-        pf::paged_kv_producer<D, BN, NK, NV, true, true>(
-            pg, b, h / sh.G, sh.Hkv, sh.n_kv, nb, &tm_k, &tm_v, sK, sV, b_kfull(0), b_kempty(0),
-            b_vfull(0), b_vempty(0), abort_flag, err, lane);
-        if (lane == 0 && *abort_flag)
-            mbar_wait_drain(b_qfull, 0);
     } else if (warp == kProducerWarp) {
         // ================================================= TMA producer
         // lane 0 streams Q and K, lane 1 streams V: each waits only for its
@@ -1536,14 +1570,14 @@ static pf::Scales make_scales(const PrefillArgs &a) {
 }
 
 // Cache [num_blocks, Hkv, bs, d] (16-bit) viewed as {d, Hkv * bs, num_blocks},
-// box 64 x 16 x 1, 128-byte swizzle.
+// box 64 x bs x 1 (one panel of one head's cache block), 128-byte swizzle.
 static bool make_cache_map(CUtensorMap *m, const void *ptr, const PrefillArgs &a) {
     const uint64_t dims[3] = {static_cast<uint64_t>(a.d),
                               static_cast<uint64_t>(a.Hkv) * a.block_size,
                               static_cast<uint64_t>(a.num_blocks)};
     const uint64_t strides[2] = {static_cast<uint64_t>(a.d) * 2,
                                  static_cast<uint64_t>(a.Hkv) * a.block_size * a.d * 2};
-    const uint32_t box[3] = {64, 16, 1};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(a.block_size), 1};
     return make_tmap_3d(m, ptr, a.bf16 ? TmapElem::BF16 : TmapElem::F16, dims, strides, box, 128);
 }
 
@@ -1638,8 +1672,8 @@ static cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t st) {
     const long long grid = static_cast<long long>(sh.nqb) * a.B * a.Hq;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidValue;
-    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(mq, mk, mv, mo, a.O, a.lse, sh,
-                                                                  sc, make_paged(a), a.err);
+    kern<<<static_cast<unsigned>(grid), pfw::threads<F8, PAGED>(), C::SMEM, st>>>(
+        mq, mk, mv, mo, a.O, a.lse, sh, sc, make_paged(a), a.err);
     return cudaGetLastError();
 }
 

@@ -28,6 +28,10 @@ CASES = [
     (33, 2, 2, 40, 256, [40 + 11 * ((7 * i) % 12) for i in range(33)], 32, True, "bf16", "f32"),
     # more sequences than are ranked: the given order
     (70, 2, 2, 8, 128, [8 + 7 * ((5 * i) % 33) for i in range(70)], 16, True, "f16", "f32"),
+    # one TMA box per cache block: 32- and 64-token boxes, sequence ends inside them
+    (3, 4, 2, 100, 128, [100, 777, 1301], 64, True, "bf16", "f32"),
+    (2, 8, 2, 64, 128, [64, 999], 32, True, "f16", "bf16"),
+    (2, 4, 4, 130, 64, [130, 2049], 64, True, "bf16", "f32"),
 ]
 
 
@@ -64,8 +68,10 @@ def test_prefill_paged_small(case):
     assert_lse(lse, lse_ref)
 
 
-def test_prefill_paged_stale_slots_do_not_leak():
-    case = (3, 4, 2, 77, 128, [77, 301, 999], 16, True, "bf16", "f32")
+@pytest.mark.parametrize("d,bs", [(64, 16), (128, 16), (256, 16), (128, 64), (256, 32)])
+def test_prefill_paged_stale_slots_do_not_leak(d, bs):
+    # at d = 256 the sequence-end V unit is copied by two warps, panel by panel
+    case = (3, 4, 2, 77, d, [77, 301, 999], bs, True, "bf16", "f32")
     t, O, lse = _run(case, seed=1, poison=True)
     assert attn.last_error() == attn.OK
     assert torch.isfinite(O).all()
