@@ -74,6 +74,13 @@ enum class TmapElem { BF16, F16, U8 };
 bool make_tmap_3d(CUtensorMap *m, const void *ptr, TmapElem elem, const uint64_t dims[3],
                   const uint64_t strides_bytes[2], const uint32_t box[3], int swizzle_bytes);
 
+// 4-D form.  The strides need not grow with the dimension: a dimension may
+// step through a row in smaller strides than the one before it (the paged
+// V cache's panels, 128 bytes apart, taken as the box's outer dimension so
+// that each panel lands as its own swizzled block of rows).
+bool make_tmap_4d(CUtensorMap *m, const void *ptr, TmapElem elem, const uint64_t dims[4],
+                  const uint64_t strides_bytes[3], const uint32_t box[4], int swizzle_bytes);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

@@ -140,10 +140,34 @@ struct Paged {
     int bs, max_blocks, num_blocks, max_len;
 };
 
+// Paged V stages are unit-major at d = 256 only (see paged_kv_producer).
+template <int D>
+constexpr bool kPagedV4 = D == 256;
+
+// Shared-memory descriptor of the V operand (B, MN-major, 128-byte swizzle)
+// for the P.V product over keys [16 k, 16 k + 16) of a V stage at vb: dense
+// stages are [panel][key] (panel stride BN rows), unit-major paged ones
+// [unit][panel][token] (panel stride U rows, U = tokens per cache block).
+template <bool PAGED, int D, int BN>
+__device__ __forceinline__ uint64_t pv_desc(uint32_t vb, int k, int U) {
+    if constexpr (!(PAGED && kPagedV4<D>)) {
+        return sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+    } else {
+        const int key = 16 * k, u = key / U;
+        return sdesc_sw128(vb + u * ((D / 64) * U * 128) + (key - u * U) * 128, U * 128, 1024);
+    }
+}
+
 // Whole-warp producer of the K and V blocks (BN keys, 16-bit, D) of one
-// (sequence, KV head) from a block-paged cache: one TMA box (block_size
-// tokens x 64 elements) per cache block ("unit") and 128-byte panel, into
-// the same swizzled stage layout dense tiles have.  Units past the sequence end read a block
+// (sequence, KV head) from a block-paged cache, one cache block ("unit") of
+// block_size tokens per lane.  K: one TMA box (block_size tokens x 64
+// elements) per unit and 128-byte panel, into the swizzled stage layout
+// dense tiles have ([panel][key]).  V at d = 256 (kPagedV4): one 4-D box
+// per unit holding its four panels, so the V stage is unit-major
+// ([unit][panel][token], each panel a swizzled block of block_size rows;
+// pv_desc steps the P.V operand through it).  Such a box costs the TMA unit
+// more than a plain one (d = 128: 1447 -> 917 TFLOP/s with it, d = 64, one
+// panel, 787 -> 695), so below d = 256 V keeps one box per panel.  Units past the sequence end read a block
 // coordinate past the tensor, which TMA fills with zeros.  The one V unit
 // that holds the sequence end is copied with plain loads and its rows past
 // the end zeroed: their p is 0, and 0 * (stale non-finite cache contents)
@@ -166,6 +190,9 @@ __device__ __forceinline__ void paged_kv_producer(
     static_assert(0 <= KP0 && KP0 <= KP1 && KP1 <= D / 64, "K panel range");
     static_assert(0 <= VP0 && VP0 <= VP1 && VP1 <= D / 64, "V panel range");
     static_assert(DO_K || DO_V, "a producer feeds at least one tensor");
+    constexpr bool V4 = kPagedV4<D>;
+    static_assert(!V4 || !DO_V || (VP0 == 0 && VP1 == D / 64),
+                  "one V box holds every panel of a unit");
     constexpr int VNP = VP1 - VP0;
     constexpr int VCH = VNP > 0 ? VNP * 8 : 1;      // 16-byte chunks of a V row it copies
     constexpr int K_STAGE = BN * (KP1 - KP0) * 128; // this warp's bytes of a K stage
@@ -233,8 +260,11 @@ __device__ __forceinline__ void paged_kv_producer(
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
                 if (r < nval && blk >= 0)
                     v = *reinterpret_cast<const uint4 *>(pg.vcache + (row0 + r) * (D * 2) + c * 16);
-                sts_v4(sV + vs * STAGE + (c / 8) * (BN * 128) + swz_offset<128>(up * U + r, c % 8),
-                       v.x, v.y, v.z, v.w);
+                const uint32_t dst =
+                    V4 ? sV + vs * STAGE + up * ((D / 64) * U * 128) + (c / 8) * (U * 128) +
+                             swz_offset<128>(r, c % 8)
+                       : sV + vs * STAGE + (c / 8) * (BN * 128) + swz_offset<128>(up * U + r, c % 8);
+                sts_v4(dst, v.x, v.y, v.z, v.w);
             }
             fence_proxy_async_smem(); // generic writes -> tensor-core reads
             __syncwarp();
@@ -243,10 +273,15 @@ __device__ __forceinline__ void paged_kv_producer(
             mbar_arrive_expect_tx(vfull0 + 8u * vs, (UPB - (up >= 0 ? 1 : 0)) * v_unit);
         __syncwarp();
         if (lane < UPB && lane != up) {
+            if constexpr (V4) {
+                tma_load_4d(sV + vs * STAGE + lane * ((D / 64) * U * 128), tm_v, vfull0 + 8u * vs,
+                            0, y, 0, z);
+            } else {
 #pragma unroll
-            for (int p = VP0; p < VP1; ++p)
-                tma_load_3d(sV + vs * STAGE + p * BN * 128 + lane * U * 128, tm_v,
-                            vfull0 + 8u * vs, p * 64, y, z);
+                for (int p = VP0; p < VP1; ++p)
+                    tma_load_3d(sV + vs * STAGE + p * BN * 128 + lane * U * 128, tm_v,
+                                vfull0 + 8u * vs, p * 64, y, z);
+            }
         }
         v_issued = j + 1;
     }
@@ -669,14 +704,14 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                     const uint32_t vb = sV + vs * C::V_BYTES;
     #pragma unroll
                     for (int k = 0; k < BN / 16; ++k) {
-                        const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+                        const uint64_t bd = pv_desc<PAGED, D, BN>(vb, k, pg.bs);
                         mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, bd, idesc_pv,
                                (first && k == 0) ? 0u : 1u);
                     }
                     if (split[t]) {
     #pragma unroll
                         for (int k = 0; k < BN / 16; ++k) {
-                            const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+                            const uint64_t bd = pv_desc<PAGED, D, BN>(vb, k, pg.bs);
                             mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + 64 + k * 8, bd, idesc_pv,
                                    1u);
                         }
@@ -1275,14 +1310,14 @@ __global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
                 const uint32_t vb = sV + vs * C::V_BYTES;
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
-                    const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+                    const uint64_t bd = pf::pv_desc<PAGED, D, BN>(vb, k, pg.bs);
                     mma_ts(tmem + O_COL, tmem + S_COL0 + buf * BN + k * 8, bd, idesc_pv,
                            (first && k == 0) ? 0u : 1u);
                 }
                 if (split) {
 #pragma unroll
                     for (int k = 0; k < BN / 16; ++k) {
-                        const uint64_t bd = sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
+                        const uint64_t bd = pf::pv_desc<PAGED, D, BN>(vb, k, pg.bs);
                         mma_ts(tmem + O_COL, tmem + S_COL0 + buf * BN + BN / 2 + k * 8, bd,
                                idesc_pv, 1u);
                     }
@@ -1581,10 +1616,24 @@ static bool make_cache_map(CUtensorMap *m, const void *ptr, const PrefillArgs &a
     return make_tmap_3d(m, ptr, a.bf16 ? TmapElem::BF16 : TmapElem::F16, dims, strides, box, 128);
 }
 
+// The V cache viewed as {64, Hkv * bs, d / 64, num_blocks}: the third
+// dimension steps through a row's 128-byte panels, so that one box
+// {64, bs, d / 64, 1} lands a cache block as [panel][token] swizzled blocks.
+static bool make_cache_map_v(CUtensorMap *m, const void *ptr, const PrefillArgs &a) {
+    const uint64_t dims[4] = {64, static_cast<uint64_t>(a.Hkv) * a.block_size,
+                              static_cast<uint64_t>(a.d / 64), static_cast<uint64_t>(a.num_blocks)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(a.d) * 2, 128,
+                                 static_cast<uint64_t>(a.Hkv) * a.block_size * a.d * 2};
+    const uint32_t box[4] = {64, static_cast<uint32_t>(a.block_size),
+                             static_cast<uint32_t>(a.d / 64), 1};
+    return make_tmap_4d(m, ptr, a.bf16 ? TmapElem::BF16 : TmapElem::F16, dims, strides, box, 128);
+}
+
 static bool make_kv_maps(CUtensorMap *mk, CUtensorMap *mv, const PrefillArgs &a, int D, bool bf16,
                          bool f8, int rows) {
-    if (a.paged)
-        return make_cache_map(mk, a.K, a) && make_cache_map(mv, a.V, a);
+    if (a.paged) // V: one box per cache block at d = 256 (pf::kPagedV4)
+        return make_cache_map(mk, a.K, a) &&
+               (a.d == 256 ? make_cache_map_v(mv, a.V, a) : make_cache_map(mv, a.V, a));
     return make_map(mk, a.K, D, a.n_kv, a.B * a.Hkv, bf16, f8, rows) &&
            make_map(mv, a.V, D, a.n_kv, a.B * a.Hkv, bf16, f8, rows);
 }

@@ -26,25 +26,41 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-bool make_tmap_3d(CUtensorMap *m, const void *ptr, TmapElem elem, const uint64_t dims[3],
-                  const uint64_t strides_bytes[2], const uint32_t box[3], int swizzle_bytes) {
+static bool make_tmap(CUtensorMap *m, const void *ptr, TmapElem elem, int rank,
+                      const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                      int swizzle_bytes) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc)
         return false;
-    cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
-    cuuint64_t s[2] = {strides_bytes[0], strides_bytes[1]};
-    cuuint32_t b[3] = {box[0], box[1], box[2]};
-    cuuint32_t estr[3] = {1, 1, 1};
+    cuuint64_t d[4], s[3];
+    cuuint32_t b[4], estr[4];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank)
+            s[i] = strides_bytes[i];
+    }
     const CUtensorMapDataType dt = elem == TmapElem::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                    : elem == TmapElem::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                         : CU_TENSOR_MAP_SWIZZLE_NONE;
-    CUresult r = enc(m, dt, 3, const_cast<void *>(ptr), d, s, b, estr,
+    CUresult r = enc(m, dt, static_cast<cuuint32_t>(rank), const_cast<void *>(ptr), d, s, b, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_3d(CUtensorMap *m, const void *ptr, TmapElem elem, const uint64_t dims[3],
+                  const uint64_t strides_bytes[2], const uint32_t box[3], int swizzle_bytes) {
+    return make_tmap(m, ptr, elem, 3, dims, strides_bytes, box, swizzle_bytes);
+}
+
+bool make_tmap_4d(CUtensorMap *m, const void *ptr, TmapElem elem, const uint64_t dims[4],
+                  const uint64_t strides_bytes[3], const uint32_t box[4], int swizzle_bytes) {
+    return make_tmap(m, ptr, elem, 4, dims, strides_bytes, box, swizzle_bytes);
 }
 
 bool make_tmap_3d_16bit(CUtensorMap *m, const void *ptr, bool bf16, const uint64_t dims[3],
