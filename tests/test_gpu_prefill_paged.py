@@ -32,6 +32,10 @@ CASES = [
     (3, 4, 2, 100, 128, [100, 777, 1301], 64, True, "bf16", "f32"),
     (2, 8, 2, 64, 128, [64, 999], 32, True, "f16", "bf16"),
     (2, 4, 4, 130, 64, [130, 2049], 64, True, "bf16", "f32"),
+    # d = 256: V by one box per cache block into a unit-major stage, K by two
+    # warps; 20 key blocks, sequence ends inside a block
+    (2, 4, 2, 300, 256, [1203, 2501], 16, True, "bf16", "bf16"),
+    (2, 4, 2, 300, 256, [1203, 2501], 64, False, "f16", "f32"),
 ]
 
 
