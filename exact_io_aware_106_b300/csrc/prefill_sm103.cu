@@ -138,36 +138,41 @@ struct Paged {
     const int32_t *lens;
     const uint8_t *vcache;
     int bs, max_blocks, num_blocks, max_len;
+    int v4; // V by one 4-D box per cache block into unit-major stages (d = 256, bs = 16)
 };
 
-// Paged V stages are unit-major at d = 256 only (see paged_kv_producer).
+// Paged V stages can be unit-major at d = 256 only (see paged_kv_producer);
+// the call takes that form when its cache blocks are 16 tokens (Paged::v4).
 template <int D>
 constexpr bool kPagedV4 = D == 256;
 
 // Shared-memory descriptor of the V operand (B, MN-major, 128-byte swizzle)
 // for the P.V product over keys [16 k, 16 k + 16) of a V stage at vb: dense
 // stages are [panel][key] (panel stride BN rows), unit-major paged ones
-// [unit][panel][token] (panel stride U rows, U = tokens per cache block).
+// [unit][panel][token] (16-token units: panel stride 16 rows).
+// (The unit-major form is taken with 16-token blocks only, so the 16 keys
+// of step k are exactly unit k: a constant stride, nothing computed per MMA
+// in the issuing thread.)
 template <bool PAGED, int D, int BN>
-__device__ __forceinline__ uint64_t pv_desc(uint32_t vb, int k, int U) {
-    if constexpr (!(PAGED && kPagedV4<D>)) {
-        return sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
-    } else {
-        const int key = 16 * k, u = key / U;
-        return sdesc_sw128(vb + u * ((D / 64) * U * 128) + (key - u * U) * 128, U * 128, 1024);
-    }
+__device__ __forceinline__ uint64_t pv_desc(uint32_t vb, int k, int v4) {
+    if constexpr (PAGED && kPagedV4<D>)
+        if (v4)
+            return sdesc_sw128(vb + k * ((D / 64) * 16 * 128), 16 * 128, 1024);
+    return sdesc_sw128(vb + k * 16 * 128, BN * 128, 1024);
 }
 
 // Whole-warp producer of the K and V blocks (BN keys, 16-bit, D) of one
 // (sequence, KV head) from a block-paged cache, one cache block ("unit") of
 // block_size tokens per lane.  K: one TMA box (block_size tokens x 64
 // elements) per unit and 128-byte panel, into the swizzled stage layout
-// dense tiles have ([panel][key]).  V at d = 256 (kPagedV4): one 4-D box
-// per unit holding its four panels, so the V stage is unit-major
-// ([unit][panel][token], each panel a swizzled block of block_size rows;
-// pv_desc steps the P.V operand through it).  Such a box costs the TMA unit
-// more than a plain one (d = 128: 1447 -> 917 TFLOP/s with it, d = 64, one
-// panel, 787 -> 695), so below d = 256 V keeps one box per panel.  Units past the sequence end read a block
+// dense tiles have ([panel][key]).  V at d = 256 with 16-token blocks
+// (Paged::v4): one 4-D box per unit holding its four panels, so the V stage
+// is unit-major ([unit][panel][token], each panel a swizzled block of
+// block_size rows; pv_desc steps the P.V operand through it).  Such a box
+// costs the TMA unit more than a plain one and pays only where it replaces
+// four 2 KB boxes: d = 256 with 32- or 64-token blocks measured 3-14%
+// slower with it, d = 128 1447 -> 917 TFLOP/s, d = 64 787 -> 695; there V
+// keeps one box per panel.  Units past the sequence end read a block
 // coordinate past the tensor, which TMA fills with zeros.  The one V unit
 // that holds the sequence end is copied with plain loads and its rows past
 // the end zeroed: their p is 0, and 0 * (stale non-finite cache contents)
@@ -190,9 +195,10 @@ __device__ __forceinline__ void paged_kv_producer(
     static_assert(0 <= KP0 && KP0 <= KP1 && KP1 <= D / 64, "K panel range");
     static_assert(0 <= VP0 && VP0 <= VP1 && VP1 <= D / 64, "V panel range");
     static_assert(DO_K || DO_V, "a producer feeds at least one tensor");
-    constexpr bool V4 = kPagedV4<D>;
-    static_assert(!V4 || !DO_V || (VP0 == 0 && VP1 == D / 64),
+    constexpr bool V4_OK = kPagedV4<D>;
+    static_assert(!V4_OK || !DO_V || (VP0 == 0 && VP1 == D / 64),
                   "one V box holds every panel of a unit");
+    const bool v4 = V4_OK && pg.v4 != 0;
     constexpr int VNP = VP1 - VP0;
     constexpr int VCH = VNP > 0 ? VNP * 8 : 1;      // 16-byte chunks of a V row it copies
     constexpr int K_STAGE = BN * (KP1 - KP0) * 128; // this warp's bytes of a K stage
@@ -261,7 +267,7 @@ __device__ __forceinline__ void paged_kv_producer(
                 if (r < nval && blk >= 0)
                     v = *reinterpret_cast<const uint4 *>(pg.vcache + (row0 + r) * (D * 2) + c * 16);
                 const uint32_t dst =
-                    V4 ? sV + vs * STAGE + up * ((D / 64) * U * 128) + (c / 8) * (U * 128) +
+                    v4 ? sV + vs * STAGE + up * ((D / 64) * U * 128) + (c / 8) * (U * 128) +
                              swz_offset<128>(r, c % 8)
                        : sV + vs * STAGE + (c / 8) * (BN * 128) + swz_offset<128>(up * U + r, c % 8);
                 sts_v4(dst, v.x, v.y, v.z, v.w);
@@ -273,7 +279,7 @@ __device__ __forceinline__ void paged_kv_producer(
             mbar_arrive_expect_tx(vfull0 + 8u * vs, (UPB - (up >= 0 ? 1 : 0)) * v_unit);
         __syncwarp();
         if (lane < UPB && lane != up) {
-            if constexpr (V4) {
+            if (v4) {
                 tma_load_4d(sV + vs * STAGE + lane * ((D / 64) * U * 128), tm_v, vfull0 + 8u * vs,
                             0, y, 0, z);
             } else {
@@ -704,14 +710,14 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                     const uint32_t vb = sV + vs * C::V_BYTES;
     #pragma unroll
                     for (int k = 0; k < BN / 16; ++k) {
-                        const uint64_t bd = pv_desc<PAGED, D, BN>(vb, k, pg.bs);
+                        const uint64_t bd = pv_desc<PAGED, D, BN>(vb, k, pg.v4);
                         mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, bd, idesc_pv,
                                (first && k == 0) ? 0u : 1u);
                     }
                     if (split[t]) {
     #pragma unroll
                         for (int k = 0; k < BN / 16; ++k) {
-                            const uint64_t bd = pv_desc<PAGED, D, BN>(vb, k, pg.bs);
+                            const uint64_t bd = pv_desc<PAGED, D, BN>(vb, k, pg.v4);
                             mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + 64 + k * 8, bd, idesc_pv,
                                    1u);
                         }
@@ -1310,14 +1316,14 @@ __global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
                 const uint32_t vb = sV + vs * C::V_BYTES;
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
-                    const uint64_t bd = pf::pv_desc<PAGED, D, BN>(vb, k, pg.bs);
+                    const uint64_t bd = pf::pv_desc<PAGED, D, BN>(vb, k, pg.v4);
                     mma_ts(tmem + O_COL, tmem + S_COL0 + buf * BN + k * 8, bd, idesc_pv,
                            (first && k == 0) ? 0u : 1u);
                 }
                 if (split) {
 #pragma unroll
                     for (int k = 0; k < BN / 16; ++k) {
-                        const uint64_t bd = pf::pv_desc<PAGED, D, BN>(vb, k, pg.bs);
+                        const uint64_t bd = pf::pv_desc<PAGED, D, BN>(vb, k, pg.v4);
                         mma_ts(tmem + O_COL, tmem + S_COL0 + buf * BN + BN / 2 + k * 8, bd,
                                idesc_pv, 1u);
                     }
@@ -1616,6 +1622,11 @@ static bool make_cache_map(CUtensorMap *m, const void *ptr, const PrefillArgs &a
     return make_tmap_3d(m, ptr, a.bf16 ? TmapElem::BF16 : TmapElem::F16, dims, strides, box, 128);
 }
 
+// Paged V by one 4-D box per cache block: d = 256 with 16-token blocks.
+static bool paged_v4(const PrefillArgs &a) {
+    return a.paged && a.d == 256 && a.block_size == 16;
+}
+
 // The V cache viewed as {64, Hkv * bs, d / 64, num_blocks}: the third
 // dimension steps through a row's 128-byte panels, so that one box
 // {64, bs, d / 64, 1} lands a cache block as [panel][token] swizzled blocks.
@@ -1631,9 +1642,9 @@ static bool make_cache_map_v(CUtensorMap *m, const void *ptr, const PrefillArgs 
 
 static bool make_kv_maps(CUtensorMap *mk, CUtensorMap *mv, const PrefillArgs &a, int D, bool bf16,
                          bool f8, int rows) {
-    if (a.paged) // V: one box per cache block at d = 256 (pf::kPagedV4)
+    if (a.paged) // V: one box per cache block at d = 256 with 16-token blocks (Paged::v4)
         return make_cache_map(mk, a.K, a) &&
-               (a.d == 256 ? make_cache_map_v(mv, a.V, a) : make_cache_map(mv, a.V, a));
+               (paged_v4(a) ? make_cache_map_v(mv, a.V, a) : make_cache_map(mv, a.V, a));
     return make_map(mk, a.K, D, a.n_kv, a.B * a.Hkv, bf16, f8, rows) &&
            make_map(mv, a.V, D, a.n_kv, a.B * a.Hkv, bf16, f8, rows);
 }
@@ -1648,6 +1659,7 @@ static pf::Paged make_paged(const PrefillArgs &a) {
         pg.max_blocks = a.max_blocks;
         pg.num_blocks = a.num_blocks;
         pg.max_len = a.max_seq_len;
+        pg.v4 = paged_v4(a) ? 1 : 0;
     }
     return pg;
 }
