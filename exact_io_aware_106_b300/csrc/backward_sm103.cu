@@ -365,8 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int xn = (t + 1) % C::NX, yn = (t + 1) % C::NY;
                 const bool next = t + 1 < nsteps;
                 if (next) {
-                    if (!mbar_wait(b_xfull(xn), ((t + 1) / C::NX) & 1, abort_flag, err) ||
-                        !mbar_wait(b_sfree, t & 1, abort_flag, err)) {
+                    // both usually complete by now: one fused wait (the two
+                    // try_waits back to back) instead of two in a row
+                    if (!mbar_wait3(b_xfull(xn), ((t + 1) / C::NX) & 1, true, b_sfree, t & 1,
+                                    true, 0u, 0u, false, abort_flag, err)) {
                         ok = false;
                         break;
                     }
@@ -385,7 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    t == 0);
                 mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL + 16, sQ(xt), 0, idesc_acc,
                                    t == 0);
-                if (!mbar_wait(b_pready(1), t & 1, abort_flag, err)) {
+                // step t+1's first operand tile has usually landed long
+                // before: tested together with P ready (the later wait for
+                // it below is then satisfied at once)
+                if (!mbar_wait3(b_pready(1), t & 1, true, b_yfull(yn), ((t + 1) / C::NY) & 1, next,
+                                0u, 0u, false, abort_flag, err)) {
                     ok = false;
                     break;
                 }
@@ -398,10 +404,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(b_xempty(xt)); // step t's Q and dO consumed
                 tc_commit(b_yempty(yt));
                 if (next) {
-                    if (!mbar_wait(b_yfull(yn), ((t + 1) / C::NY) & 1, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
                     tc_fence_after();
                     // after half 1's products, which read these columns (the
                     // tensor core runs in issue order)
@@ -697,8 +699,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int xn = (t + 1) % C::NX, yn = (t + 1) % C::NY;
                 const bool next = t + 1 < nsteps;
                 if (next) {
-                    if (!mbar_wait(b_xfull(xn), ((t + 1) / C::NX) & 1, abort_flag, err) ||
-                        !mbar_wait(b_sfree, t & 1, abort_flag, err)) {
+                    // both usually complete by now: one fused wait (the two
+                    // try_waits back to back) instead of two in a row
+                    if (!mbar_wait3(b_xfull(xn), ((t + 1) / C::NX) & 1, true, b_sfree, t & 1,
+                                    true, 0u, 0u, false, abort_flag, err)) {
                         ok = false;
                         break;
                     }
@@ -715,7 +719,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // dQ += dS K over keys 0-63 of the block
                 mma_tmem_a_half<D>(tmem + C::ACC0, tmem + C::DP_COL, sK(xt), 0, idesc_acc,
                                    t == 0);
-                if (!mbar_wait(b_pready(1), t & 1, abort_flag, err)) {
+                // step t+1's first operand tile has usually landed long
+                // before: tested together with P ready (the later wait for
+                // it below is then satisfied at once)
+                if (!mbar_wait3(b_pready(1), t & 1, true, b_yfull(yn), ((t + 1) / C::NY) & 1, next,
+                                0u, 0u, false, abort_flag, err)) {
                     ok = false;
                     break;
                 }
@@ -725,10 +733,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    false);
                 tc_commit(b_xempty(xt)); // step t's K consumed
                 if (next) {
-                    if (!mbar_wait(b_yfull(yn), ((t + 1) / C::NY) & 1, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
                     tc_fence_after();
                     // after half 1's products, which read these columns (the
                     // tensor core runs in issue order)
