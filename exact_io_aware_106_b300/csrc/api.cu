@@ -431,8 +431,8 @@ attn_status attn_debug_prefill_timeout(const void *Q, const void *K, const void 
     t_last_launches = 0;
     if (wait_limit_us == 0 || wait_limit_us > 1000000u)
         return ATTN_ERR_INVALID;
-    if (!is16(in_dtype) || (d != 64 && d != 128))
-        return ATTN_ERR_UNSUPPORTED; // the hook lives in the dense d <= 128 kernel
+    if (!is16(in_dtype) || (d != 64 && d != 128 && d != 256))
+        return ATTN_ERR_UNSUPPORTED; // the hook lives in the dense kernels' producers
     attn::PrefillArgs a;
     const attn_status s = prefill_args(Q, K, V, O, lse, B, Hq, Hkv, n_q, n_kv, d, causal, scale,
                                        in_dtype, out_dtype, nullptr, nullptr, nullptr, &a);

@@ -1239,9 +1239,16 @@ __global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
         // own stage, so a single-stage K never queues behind a V wait
         constexpr int XP = C::PW / C::EB;
         if (lane == 0) {
-            mbar_arrive_expect_tx(b_qfull, C::Q_BYTES);
-            for (int p = 0; p < C::QK_PANELS; ++p)
-                tma_load_3d(sQ + p * BM * C::PW, &tm_q, b_qfull, p * XP, r0, bh);
+            // test hook, as in the d <= 128 kernel: without the Q copy the MMA
+            // issuer's first wait expires and every role unwinds
+            const bool withhold_q =
+                (*reinterpret_cast<const volatile unsigned *>(err + CTL_HOOKS) &
+                 HOOK_WITHHOLD_Q) != 0u;
+            if (!withhold_q) {
+                mbar_arrive_expect_tx(b_qfull, C::Q_BYTES);
+                for (int p = 0; p < C::QK_PANELS; ++p)
+                    tma_load_3d(sQ + p * BM * C::PW, &tm_q, b_qfull, p * XP, r0, bh);
+            }
             int k_issued = 0;
             for (int j = 0; j < nb; ++j) {
                 const int ks = j % NK;
@@ -1254,7 +1261,8 @@ __global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
                 k_issued = j + 1;
             }
             if (*abort_flag) { // let in-flight copies land before the CTA exits
-                mbar_wait_drain(b_qfull, 0);
+                if (!withhold_q)
+                    mbar_wait_drain(b_qfull, 0);
                 for (int u = max(0, k_issued - NK); u < k_issued; ++u)
                     mbar_wait_drain(b_kfull(u % NK), (u / NK) & 1);
             }

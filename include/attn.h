@@ -323,7 +323,7 @@ ATTN_API attn_status attn_last_error(void *stream);
  * libraries gives up after a limit (2 s by default), records
  * ATTN_ERR_TIMEOUT, and the CTA unwinds: copies in flight land, tensor
  * memory is freed, the CTA's output rows are written as O = 0 and
- * lse = NaN.  This call runs attn_prefill (16-bit inputs, d in {64, 128})
+ * lse = NaN.  This call runs attn_prefill (16-bit inputs, d in {64, 128, 256})
  * with the limit set to wait_limit_us and with the producer of the dense
  * prefill kernel withholding its Q copy, so that the first wait on Q
  * expires in every CTA.  The limit and the hook are set and cleared in

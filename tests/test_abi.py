@@ -94,7 +94,7 @@ def test_debug_prefill_timeout_host_validation(L):
                                             1, 0.1, ind, 2, limit, None)
     assert call(limit=0) == attn.ERR_INVALID
     assert call(limit=2000000) == attn.ERR_INVALID
-    assert call(d=256) == attn.ERR_UNSUPPORTED                         # hook is in the d<=128 kernel
+    assert call(d=96) == attn.ERR_UNSUPPORTED                          # head sizes 64/128/256
     assert call(ind=3) == attn.ERR_UNSUPPORTED                         # 16-bit inputs only
     assert L.attn_last_launch_count() == 0
 

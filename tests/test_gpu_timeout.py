@@ -23,7 +23,7 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_expired_wait_is_reported_and_the_device_stays_usable(d):
     spec = W.PrefillSpec(1, 1, 1, 128, 128, d, True, "bf16", "f32")
     t = W.make_prefill(spec, seed=31 + d)
