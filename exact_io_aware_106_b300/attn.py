@@ -24,7 +24,8 @@ EXPORTS = ("attn_prefill", "attn_prefill_from_host", "attn_prefill_from_host_hea
            "attn_decode_tokens", "attn_kv_append", "attn_backward",
            "attn_backward_workspace_bytes", "attn_rotate_quantize_e4m3",
            "attn_prefill_e4m3_blocks", "attn_last_error", "attn_status_str",
-           "attn_last_launch_count", "attn_decode_static_ws", "attn_debug_prefill_timeout")
+           "attn_last_launch_count", "attn_decode_static_ws", "attn_debug_prefill_timeout",
+           "attn_debug_set_hooks")
 
 # Rows per E4M3 scale block in prefill_e4m3_blocks (ATTN_E4M3_SCALE_BLOCK).
 E4M3_SCALE_BLOCK = 128
@@ -88,6 +89,8 @@ def lib():
         L.attn_debug_prefill_timeout.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                  i32, i32, f32, i32, i32, ctypes.c_uint, vp]
         L.attn_debug_prefill_timeout.restype = i32
+        L.attn_debug_set_hooks.argtypes = [ctypes.c_uint, ctypes.c_uint, vp]
+        L.attn_debug_set_hooks.restype = i32
         L.attn_last_error.argtypes = [vp]
         L.attn_last_error.restype = i32
         L.attn_status_str.argtypes = [i32]
@@ -136,6 +139,17 @@ def last_launch_count() -> int:
 def last_error(stream=None) -> int:
     """Synchronise the stream; return (and clear) the device error status."""
     return lib().attn_last_error(_stream(stream))
+
+
+# Test hooks of attn_debug_set_hooks (ATTN_HOOK_*).
+HOOK_WITHHOLD_Q = 1
+HOOK_WITHHOLD_KV = 2
+
+
+def debug_set_hooks(wait_limit_us: int, hooks: int, stream=None) -> int:
+    """Failure-path tests only: set the kernels' wait limit (microseconds,
+    0 = default) and test hooks for every later call; (0, 0) clears them."""
+    return lib().attn_debug_set_hooks(wait_limit_us, hooks, _stream(stream))
 
 
 def prefill(Q, K, V, causal: bool, scale: float | None = None, out_dtype=None, O=None,

@@ -457,6 +457,27 @@ attn_status attn_debug_prefill_timeout(const void *Q, const void *K, const void 
     return ATTN_OK;
 }
 
+static_assert(ATTN_HOOK_WITHHOLD_Q == attn::HOOK_WITHHOLD_Q &&
+                  ATTN_HOOK_WITHHOLD_KV == attn::HOOK_WITHHOLD_KV,
+              "hook bits of the header and the kernels agree");
+
+attn_status attn_debug_set_hooks(unsigned wait_limit_us, unsigned hooks, void *stream) {
+    t_last_launches = 0;
+    if (wait_limit_us > 1000000u || (hooks & ~attn::HOOK_ALL) != 0u)
+        return ATTN_ERR_INVALID;
+    if (!err_word())
+        return ATTN_ERR_CUDA;
+    // after the work already queued on `stream`, before anything queued later
+    const unsigned words[2] = {wait_limit_us, hooks};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_attn_err_word, words, sizeof words,
+                           attn::CTL_WAIT_US * sizeof(unsigned), cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
 attn_status attn_last_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)

@@ -20,9 +20,11 @@ enum : unsigned { DERR_TIMEOUT = 1u, DERR_INDEX = 2u };
 //   [CTL_WAIT_US] limit of the bounded waits in microseconds (0: the default
 //                 kWaitTimeoutNs); set only by the test entry point;
 //   [CTL_HOOKS]   test hooks (HOOK_WITHHOLD_Q: the dense prefill's producer
-//                 does not issue the Q copy, so the first wait on it expires).
+//                 does not issue the Q copy, so the first wait on it expires;
+//                 HOOK_WITHHOLD_KV: the decode split kernel's producer issues
+//                 no K/V copy, so its consumers' first wait expires).
 enum : int { CTL_ERR = 0, CTL_WAIT_US = 1, CTL_HOOKS = 2, CTL_WORDS = 4 };
-enum : unsigned { HOOK_WITHHOLD_Q = 1u };
+enum : unsigned { HOOK_WITHHOLD_Q = 1u, HOOK_WITHHOLD_KV = 2u, HOOK_ALL = 3u };
 
 // A bounded wait gives up after this long (a healthy wait in these kernels
 // lasts microseconds).  On expiry the waiter sets DERR_TIMEOUT and the CTA's

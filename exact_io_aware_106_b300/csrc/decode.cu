@@ -368,6 +368,11 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT, NG>::MIN_CTAS)
         // small units (16 tokens x 64 bytes of K and of V) could not keep HBM
         // busy.  The lanes divide the stages among them (NST is a multiple of
         // IL), so each stage is refilled, waited on and drained by one lane.
+        // test hook: no copies at all, so the consumers' first wait expires
+        // (and they unwind: this warp has nothing in flight to drain)
+        if ((*reinterpret_cast<const volatile unsigned *>(err + CTL_HOOKS) & HOOK_WITHHOLD_KV) !=
+            0u)
+            return;
         constexpr int IL = Ly::ISSUE_LANES;
         if (lane < IL) {
             if (lane == 0) {

@@ -339,7 +339,23 @@ ATTN_API attn_status attn_debug_prefill_timeout(const void *Q, const void *K, co
                                                 attn_dtype out_dtype, unsigned wait_limit_us,
                                                 void *stream);
 
-/* Static string naming a status code (never NULL). */
+/* Test entry point for the bounded waits of every kernel (a failure-path
+ * check; the method has no counterpart of it): synchronises `stream`, then
+ * sets the wait limit to wait_limit_us (0: the 2 s default) and the test
+ * hooks to `hooks`, bits of:
+ *   ATTN_HOOK_WITHHOLD_Q   the dense prefill's producer withholds its Q copy
+ *   ATTN_HOOK_WITHHOLD_KV  the decode split kernel's producer issues no K/V
+ *                          copy
+ * so that a wait expires, the kernel records ATTN_ERR_TIMEOUT, and the
+ * affected output rows are written as O = 0 and lse = NaN.  They stay set
+ * for every later call on the device until cleared with (0, 0); nothing
+ * else may run on the device meanwhile.  wait_limit_us <= 1000000 and no
+ * other hook bits, else ATTN_ERR_INVALID. */
+#define ATTN_HOOK_WITHHOLD_Q 1u
+#define ATTN_HOOK_WITHHOLD_KV 2u
+ATTN_API attn_status attn_debug_set_hooks(unsigned wait_limit_us, unsigned hooks, void *stream);
+
+/* Static string naming a status code (never NULL). *//* Static string naming a status code (never NULL). */
 ATTN_API const char *attn_status_str(attn_status s);
 
 /* Number of kernel launches the most recent successful call of each entry

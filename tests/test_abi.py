@@ -99,6 +99,12 @@ def test_debug_prefill_timeout_host_validation(L):
     assert L.attn_last_launch_count() == 0
 
 
+def test_debug_set_hooks_host_validation(L):
+    assert L.attn_debug_set_hooks(2000000, 0, None) == attn.ERR_INVALID   # limit above 1 s
+    assert L.attn_debug_set_hooks(300, 4, None) == attn.ERR_INVALID       # unknown hook bit
+    assert L.attn_last_launch_count() == 0
+
+
 def test_rotate_quantize_host_validation(L):
     def call(**kw):
         a = dict(X=FAKE, heads=2, rows=100, d=128, rpb=128, ind=1)
