@@ -171,14 +171,17 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *map, 
 template <int D>
 __device__ __forceinline__ void mma_tmem_a_half(uint32_t acc, uint32_t a_half, uint32_t b_tile,
                                                 int e, uint32_t idesc, bool first) {
-    // one descriptor, stepped by offset >> 4 (the start-address field is the
-    // low 14 bits of address >> 4 and shared addresses stay below 2^18, so
-    // the add never carries out of it): no descriptor is rebuilt between the
-    // issuing thread's MMAs
-    const uint64_t b0 = sdesc_sw128(b_tile, BT * 128, 1024);
+    // one descriptor low word, stepped by offset >> 4 (the start-address
+    // field is the low 14 bits of address >> 4 and shared addresses stay
+    // below 2^18, so the add never carries out of it) under the layout's
+    // constant high word: no descriptor is rebuilt between the issuing
+    // thread's MMAs
+    const uint32_t b0 = sdesc_lo(b_tile, BT * 128);
 #pragma unroll
     for (int k = 0; k < HS / 16; ++k) {
-        const uint64_t bd = b0 + static_cast<uint64_t>(((e * (HS / 16) + k) * 16 * 128) >> 4);
+        const uint64_t bd =
+            sdesc(b0 + static_cast<uint32_t>(((e * (HS / 16) + k) * 16 * 128) >> 4),
+                  sdesc_sw128_hi(1024));
         mma_ts(acc, a_half + (k >> 1) * 32 + (k & 1) * 8, bd, idesc, (first && k == 0) ? 0u : 1u);
     }
 }
@@ -188,11 +191,13 @@ __device__ __forceinline__ void mma_tmem_a_half(uint32_t acc, uint32_t a_half, u
 template <int D>
 __device__ __forceinline__ void mma_ss_block(uint32_t acc, uint32_t a_tile, uint32_t b_tile,
                                              uint32_t idesc) {
-    const uint64_t a0 = sdesc_sw128(a_tile, 16, 1024), b0 = sdesc_sw128(b_tile, 16, 1024);
+    const uint32_t a0 = sdesc_lo(a_tile, 16), b0 = sdesc_lo(b_tile, 16);
+    constexpr uint32_t hi = sdesc_sw128_hi(1024);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k / 4) * (BT * 128) + (k % 4) * 32;
-        mma_ss(acc, a0 + (off >> 4), b0 + (off >> 4), idesc, k > 0 ? 1u : 0u);
+        mma_ss(acc, sdesc(a0 + (off >> 4), hi), sdesc(b0 + (off >> 4), hi), idesc,
+               k > 0 ? 1u : 0u);
     }
 }
 

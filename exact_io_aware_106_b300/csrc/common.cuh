@@ -274,27 +274,36 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a
 // K-major: rows of 128 bytes, 8-row atoms SBO apart (LBO unused).
 // MN-major: 64-element (128-byte) MN chunks LBO apart, 8-row K groups SBO
 // apart.  Tiles start on 1024-byte boundaries.
+// The descriptor splits into a low word that depends on the address
+// (start address, leading byte offset) and a high word fixed by the layout
+// (stride byte offset, version, swizzle): kernels that step through an
+// operand keep the low word (32 bits) and attach the constant high word per
+// MMA.
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo, uint32_t layout) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (layout << 29);
+}
+__device__ __forceinline__ uint64_t sdesc(uint32_t lo, uint32_t hi) {
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+// high words of the two layouts below
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo) { return sdesc_hi(sbo, 2u); }
+__host__ __device__ constexpr uint32_t sdesc_kmajor_hi(int row_bytes) {
+    return sdesc_hi(8u * row_bytes, row_bytes == 128 ? 2u : 4u);
+}
+
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
+    return sdesc(sdesc_lo(saddr, lbo), sdesc_sw128_hi(sbo));
 }
 
 // Shared-memory matrix descriptor for a K-major operand whose rows are
 // `row_bytes` (128 or 64) long and swizzled over that span by TMA: 8-row
-// atoms SBO = 8 * row_bytes apart; layout 2 = 128-byte, 4 = 64-byte swizzle.
+// atoms SBO = 8 * row_bytes apart; layout 2 = 128-byte, 4 = 64-byte swizzle;
+// the leading byte offset (unused when swizzled) is 16.
 __device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr, int row_bytes) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>(1) << 16; // leading byte offset (unused when swizzled)
-    d |= static_cast<uint64_t>(((8u * row_bytes) >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(row_bytes == 128 ? 2 : 4) << 61;
-    return d;
+    return sdesc(sdesc_lo(saddr, 16u), sdesc_kmajor_hi(row_bytes));
 }
 
 #define ATTN_R32_OUT(r)                                                                          \

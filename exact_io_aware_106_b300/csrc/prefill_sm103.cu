@@ -155,27 +155,28 @@ constexpr bool kPagedV4 = D == 256;
 // in the issuing thread.)
 //
 // Descriptors are built once per operand region and stepped by adding the
-// byte offset >> 4: the start-address field is the low 14 bits of the
-// address >> 4, and no shared-memory address reaches 2^18, so the add never
-// carries out of the field.  (Rebuilding them per MMA put integer work
-// between the issuing thread's MMAs.)  dv / dv4: the stage's base
-// descriptor for the [panel][key] / unit-major layout.
+// byte offset >> 4 to their low word: the start-address field is the low 14
+// bits of the address >> 4, and no shared-memory address reaches 2^18, so
+// the add never carries out of the field; the high word is a constant of
+// the layout.  (Rebuilding them per MMA put integer work between the
+// issuing thread's MMAs, and 64-bit bases cost that thread's small register
+// budget spills.)  lv / lv4: the stage's low word for the [panel][key] /
+// unit-major layout.
 template <bool PAGED, int D, int BN>
-__device__ __forceinline__ uint64_t pv_desc(uint64_t dv, uint64_t dv4, int k, int v4) {
+__device__ __forceinline__ uint64_t pv_desc(uint32_t lv, uint32_t lv4, int k, int v4) {
+    constexpr uint32_t hi = sdesc_sw128_hi(1024);
     if constexpr (PAGED && kPagedV4<D>)
         if (v4)
-            return dv4 + static_cast<uint64_t>((k * ((D / 64) * 16 * 128)) >> 4);
-    return dv + static_cast<uint64_t>((k * 16 * 128) >> 4);
+            return sdesc(lv4 + static_cast<uint32_t>((k * ((D / 64) * 16 * 128)) >> 4), hi);
+    return sdesc(lv + static_cast<uint32_t>((k * 16 * 128) >> 4), hi);
 }
 
-// Base descriptors of a V stage (see pv_desc).
+// Low descriptor words of a V stage (see pv_desc).
 template <int BN>
-__device__ __forceinline__ uint64_t pv_base(uint32_t vb) {
-    return sdesc_sw128(vb, BN * 128, 1024);
+__device__ __forceinline__ uint32_t pv_base(uint32_t vb) {
+    return sdesc_lo(vb, BN * 128);
 }
-__device__ __forceinline__ uint64_t pv_base4(uint32_t vb) {
-    return sdesc_sw128(vb, 16 * 128, 1024);
-}
+__device__ __forceinline__ uint32_t pv_base4(uint32_t vb) { return sdesc_lo(vb, 16 * 128); }
 
 // Whole-warp producer of the K and V blocks (BN keys, 16-bit, D) of one
 // (sequence, KV head) from a block-paged cache, one cache block ("unit") of
@@ -706,19 +707,20 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                 for (int t = 0; t < NT; ++t)
                     split[t] = tile_split(sh, q0, t);
 
-                // base descriptors (operands are stepped from them, see pv_desc)
-                const uint64_t dq0 = sdesc_kmajor(sQ, C::PW), dk0 = sdesc_kmajor(sK, C::PW);
-                const uint64_t dv0 = pv_base<BN>(sV), dv40 = pv_base4(sV);
+                // low descriptor words of the operand regions (stepped, see pv_desc)
+                constexpr uint32_t hqk = sdesc_kmajor_hi(C::PW);
+                const uint32_t lq0 = sdesc_lo(sQ, 16u), lk0 = sdesc_lo(sK, 16u);
+                const uint32_t lv0 = pv_base<BN>(sV), lv40 = pv_base4(sV);
                 auto issue_qk = [&](int t, int ks) {
-                    const uint64_t qa = dq0 + static_cast<uint64_t>((t * C::Q_TILE_BYTES) >> 4);
-                    const uint64_t kb = dk0 + static_cast<uint64_t>((ks * C::K_BYTES) >> 4);
+                    const uint32_t qa = lq0 + static_cast<uint32_t>((t * C::Q_TILE_BYTES) >> 4);
+                    const uint32_t kb = lk0 + static_cast<uint32_t>((ks * C::K_BYTES) >> 4);
     #pragma unroll
                     for (int k = 0; k < D * C::EB / 32; ++k) { // 32-byte K steps
                         const uint32_t byte = k * 32;
                         const uint32_t offa = (byte / C::PW) * (BM * C::PW) + byte % C::PW;
                         const uint32_t offb = (byte / C::PW) * (BN * C::PW) + byte % C::PW;
-                        const uint64_t ad = qa + (offa >> 4);
-                        const uint64_t bd = kb + (offb >> 4);
+                        const uint64_t ad = sdesc(qa + (offa >> 4), hqk);
+                        const uint64_t bd = sdesc(kb + (offb >> 4), hqk);
                         if constexpr (F8)
                             mma_ss_f8(tmem + C::S_COL(t), ad, bd, idesc_qk, k > 0 ? 1u : 0u);
                         else
@@ -726,8 +728,8 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                     }
                 };
                 auto issue_pv = [&](int t, int vs, bool first) {
-                    const uint64_t voff = static_cast<uint64_t>((vs * C::V_BYTES) >> 4);
-                    const uint64_t dv = dv0 + voff, dv4 = dv40 + voff;
+                    const uint32_t voff = static_cast<uint32_t>((vs * C::V_BYTES) >> 4);
+                    const uint32_t dv = lv0 + voff, dv4 = lv40 + voff;
     #pragma unroll
                     for (int k = 0; k < BN / 16; ++k) {
                         const uint64_t bd = pv_desc<PAGED, D, BN>(dv, dv4, k, pg.v4);
@@ -1325,18 +1327,19 @@ __global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
             constexpr uint32_t idesc_pv = idesc_f16(BM, D, PB, false, true);
             const bool split = (sh.causal ? (r0 + (sh.n_kv - sh.n_q) + 1) : sh.n_kv) <
                                pf::kSplitKeys;
-            // base descriptors (operands are stepped from them, see pf::pv_desc)
-            const uint64_t dq0 = sdesc_kmajor(sQ, C::PW), dk0 = sdesc_kmajor(sK, C::PW);
-            const uint64_t dv0 = pf::pv_base<BN>(sV), dv40 = pf::pv_base4(sV);
+            // low descriptor words of the operand regions (stepped, see pf::pv_desc)
+            constexpr uint32_t hqk = sdesc_kmajor_hi(C::PW);
+            const uint32_t lq0 = sdesc_lo(sQ, 16u), lk0 = sdesc_lo(sK, 16u);
+            const uint32_t lv0 = pf::pv_base<BN>(sV), lv40 = pf::pv_base4(sV);
             auto issue_qk = [&](int buf, int ks) {
-                const uint64_t kb = dk0 + static_cast<uint64_t>((ks * C::K_BYTES) >> 4);
+                const uint32_t kb = lk0 + static_cast<uint32_t>((ks * C::K_BYTES) >> 4);
 #pragma unroll
                 for (int k = 0; k < D * C::EB / 32; ++k) {
                     const uint32_t byte = k * 32;
                     const uint32_t offa = (byte / C::PW) * (BM * C::PW) + byte % C::PW;
                     const uint32_t offb = (byte / C::PW) * (BN * C::PW) + byte % C::PW;
-                    const uint64_t ad = dq0 + (offa >> 4);
-                    const uint64_t bd = kb + (offb >> 4);
+                    const uint64_t ad = sdesc(lq0 + (offa >> 4), hqk);
+                    const uint64_t bd = sdesc(kb + (offb >> 4), hqk);
                     if constexpr (F8)
                         mma_ss_f8(tmem + S_COL0 + buf * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
                     else
@@ -1344,8 +1347,8 @@ __global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
                 }
             };
             auto issue_pv = [&](int buf, int vs, bool first) {
-                const uint64_t voff = static_cast<uint64_t>((vs * C::V_BYTES) >> 4);
-                const uint64_t dv = dv0 + voff, dv4 = dv40 + voff;
+                const uint32_t voff = static_cast<uint32_t>((vs * C::V_BYTES) >> 4);
+                const uint32_t dv = lv0 + voff, dv4 = lv40 + voff;
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     const uint64_t bd = pf::pv_desc<PAGED, D, BN>(dv, dv4, k, pg.v4);
