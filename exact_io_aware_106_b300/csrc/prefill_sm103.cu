@@ -89,10 +89,11 @@ struct Cfg {
     static constexpr int VS_BYTES = BN * D;                 // E4M3 V staging
     static constexpr int NK = (F8 || D == 64) ? 3 : 2;      // K stages
     static constexpr int NV = (D == 64 || !F8) ? 3 : 2;     // V stages
-    // 16-bit d = 128: V stages are released by the softmax warps (below)
+    // 16-bit inputs: V stages are released by the softmax warps (below)
     // instead of a commit of the MMA-issuing thread, one block later; the
-    // third V stage covers the delay
-    static constexpr bool SOFTMAX_FREES_V = !F8 && D == 128;
+    // third V stage covers the delay (E4M3 V is released by the widening
+    // warps)
+    static constexpr bool SOFTMAX_FREES_V = !F8;
     static constexpr int NVS = F8 ? 2 : 0;                  // E4M3 V staging buffers
     static constexpr int NCONV = F8 ? 2 : 0;                // V widening warps
     static constexpr int THREADS = kThreadsAll; // warps 10-11 idle for 16-bit inputs
