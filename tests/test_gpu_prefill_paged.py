@@ -36,6 +36,11 @@ CASES = [
     # warps; 20 key blocks, sequence ends inside a block
     (2, 4, 2, 300, 256, [1203, 2501], 16, True, "bf16", "bf16"),
     (2, 4, 2, 300, 256, [1203, 2501], 64, False, "f16", "f32"),
+    # d = 256 with 16-token blocks (4-D V boxes): non-causal; no cached prefix
+    # (n_q = length) with the end inside the first key block; equal lengths
+    (3, 2, 1, 97, 256, [97, 300, 2048], 16, False, "bf16", "f32"),
+    (2, 2, 2, 77, 256, [77, 77], 16, True, "f16", "f32"),
+    (4, 4, 4, 64, 256, [640, 640, 641, 639], 16, True, "bf16", "bf16"),
 ]
 
 
