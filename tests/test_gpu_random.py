@@ -1,0 +1,134 @@
+"""Seeded random configurations against the fp64 oracle: dense prefill,
+paged prefill, decode and multi-token decode over head sizes, group sizes,
+lengths, block sizes, masking and dtypes drawn together, so that
+combinations the hand-picked cases do not list are exercised too.  The
+draws are fixed (one generator, one seed); sizes are capped so that the
+oracle finishes each case in a second or two."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_io_aware_106_b300 import attn, workloads as W
+from tests.parity import assert_lse, assert_out
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+_rng = np.random.RandomState(20261203)
+_MAX_WORK = 1.5e9  # multiply-adds of the oracle per case (B Hq n_q n_kv d)
+
+
+def _pick(xs):
+    return xs[_rng.randint(len(xs))]
+
+
+def _dense_cases(n):
+    out = []
+    while len(out) < n:
+        d = _pick([64, 128, 256])
+        G = _pick([1, 2, 3, 4, 8])
+        Hkv = _pick([1, 2])
+        B = _pick([1, 2])
+        causal = bool(_rng.randint(2))
+        n_q = int(_rng.randint(1, 600))
+        n_kv = n_q + int(_rng.randint(0, 900)) if causal else int(_rng.randint(1, 1200))
+        ind = _pick(["bf16", "f16"])
+        outd = _pick(["f32", ind])
+        if B * Hkv * G * n_q * n_kv * d > _MAX_WORK:
+            continue
+        out.append((B, Hkv * G, Hkv, n_q, n_kv, d, causal, ind, outd))
+    return out
+
+
+def _paged_cases(n):
+    out = []
+    while len(out) < n:
+        d = _pick([64, 128, 256])
+        G = _pick([1, 2, 4, 8])
+        Hkv = _pick([1, 2])
+        B = int(_rng.randint(1, 6))
+        bs = _pick([16, 32, 64])
+        causal = bool(_rng.randint(2))
+        n_q = int(_rng.randint(1, 300))
+        lens = [n_q + int(_rng.randint(0, 1500)) for _ in range(B)]
+        ind = _pick(["bf16", "f16"])
+        if sum(lens) * Hkv * G * n_q * d > _MAX_WORK:
+            continue
+        out.append((B, Hkv * G, Hkv, n_q, d, lens, bs, causal, ind))
+    return out
+
+
+def _decode_cases(n):
+    out = []
+    while len(out) < n:
+        d = _pick([64, 128, 256])
+        G = _pick([1, 2, 3, 4, 5, 8, 16])
+        Hkv = _pick([1, 2, 4])
+        S = int(_rng.randint(1, 9))
+        T = _pick([1, 1, 2, 3, 4, 8])
+        if G * T > 64:
+            continue
+        bs = _pick([16, 32, 64])
+        lens = [max(T, int(_rng.randint(1, 3000))) for _ in range(S)]
+        kv = _pick(["bf16", "f16"])
+        out.append((S, Hkv * G, Hkv, T, d, lens, bs, kv))
+    return out
+
+
+DENSE = _dense_cases(24)
+PAGED = _paged_cases(16)
+DECODE = _decode_cases(24)
+
+
+@pytest.mark.parametrize("i", range(len(DENSE)), ids=[f"r{i}" for i in range(len(DENSE))])
+def test_random_prefill(i):
+    B, Hq, Hkv, n_q, n_kv, d, causal, ind, outd = DENSE[i]
+    spec = W.PrefillSpec(B, Hq, Hkv, n_q, n_kv, d, causal, ind, outd)
+    t = W.make_prefill(spec, seed=100 + i)
+    O, lse = attn.prefill(t["Q"].cuda(), t["K"].cuda(), t["V"].cuda(), causal,
+                          out_dtype=DT[outd])
+    assert attn.last_error() == attn.OK
+    O_ref, lse_ref = oracle.sdpa(t["Q"], t["K"], t["V"], causal)
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("i", range(len(PAGED)), ids=[f"r{i}" for i in range(len(PAGED))])
+def test_random_prefill_paged(i):
+    B, Hq, Hkv, n_q, d, lens, bs, causal, ind = PAGED[i]
+    spec = W.PagedPrefillSpec(B, Hq, Hkv, n_q, d, 1, max(lens), bs, causal, ind, "f32")
+    t = W.make_paged_prefill(spec, seed=200 + i, lens=lens)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    O, lse = attn.prefill_paged(g["Q"], g["Kc"], g["Vc"], g["block_table"], g["seq_lens"],
+                                max_seq_len=max(lens), causal=causal, out_dtype=torch.float32)
+    assert attn.last_error() == attn.OK
+    O_ref, lse_ref = oracle.prefill_paged(t["Q"], t["Kc"], t["Vc"], t["block_table"],
+                                          t["seq_lens"], causal)
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("i", range(len(DECODE)), ids=[f"r{i}" for i in range(len(DECODE))])
+def test_random_decode(i):
+    S, Hq, Hkv, T, d, lens, bs, kv = DECODE[i]
+    g_out = DT[kv]
+    if T == 1:
+        spec = W.DecodeSpec(S, Hq, Hkv, d, 1, max(lens), bs, kv, kv, kv)
+        t = W.make_decode(spec, seed=300 + i, lens=lens)
+        g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+        O, lse = attn.decode(g["q"], g["Kc"], g["Vc"], g["block_table"], g["seq_lens"],
+                             max_seq_len=max(lens), out_dtype=g_out)
+        O_ref, lse_ref = oracle.decode_paged(t["q"], t["Kc"], t["Vc"], t["block_table"],
+                                             t["seq_lens"])
+    else:
+        spec = W.PagedPrefillSpec(S, Hq, Hkv, T, d, 1, max(lens), bs, True, kv, kv)
+        t = W.make_paged_prefill(spec, seed=300 + i, lens=lens)
+        g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+        O, lse = attn.decode_tokens(g["Q"], g["Kc"], g["Vc"], g["block_table"], g["seq_lens"],
+                                    max_seq_len=max(lens), out_dtype=g_out)
+        O_ref, lse_ref = oracle.prefill_paged(t["Q"], t["Kc"], t["Vc"], t["block_table"],
+                                              t["seq_lens"], True)
+    assert attn.last_error() == attn.OK
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
