@@ -1053,9 +1053,11 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
 // inputs keep 64-key blocks (with ten warps a 128-score row would not fit
 // the registers) and two stages.
 //   warp 4      TMA producer: lane 0 Q once and the K stages, lane 1 the V
-//               stages, each waiting only for its own stage
+//               stages, each waiting only for its own stage (paged calls:
+//               Q and K panels 0-1)
 //   warp 5      MMA issuer (one thread)
 //   warps 6-9   (E4M3 inputs only) widen each V tile to f16, a quarter each
+//   warps 6-7   (paged calls only) K panels 2-3; V
 //   warps 0-3   softmax, one thread per row; the epilogue
 // Tensor memory: S_0 [0,BN), S_1 [BN,2BN), O [2BN, 2BN+256).  A block that moves
 // the reference max rescales O only after the previous block's P V product

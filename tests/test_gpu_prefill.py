@@ -32,7 +32,7 @@ SMALL = [
     (1, 2, 1, 129, 129, 128, True, "bf16", "f32"),     # one row past a tile
     (3, 3, 3, 257, 511, 128, False, "bf16", "bf16"),   # tile 1 holds one row
     (1, 16, 1, 256, 256, 64, True, "f16", "bf16"),     # G = 16
-    # head size 256 (one query tile per CTA, 64-key blocks)
+    # head size 256 (one query tile per CTA; 128-key blocks for 16-bit inputs)
     (1, 1, 1, 64, 64, 256, False, "f16", "f32"),
     (1, 2, 1, 300, 300, 256, True, "bf16", "f32"),
     (1, 4, 2, 200, 700, 256, True, "f16", "bf16"),     # n_q < n_kv, bottom-right mask
