@@ -1,9 +1,10 @@
-"""Seeded random configurations against the fp64 oracle: dense prefill,
-paged prefill, decode and multi-token decode over head sizes, group sizes,
-lengths, block sizes, masking and dtypes drawn together, so that
-combinations the hand-picked cases do not list are exercised too.  The
-draws are fixed (one generator, one seed); sizes are capped so that the
-oracle finishes each case in a second or two."""
+"""Seeded random configurations against the fp64 oracle: dense prefill
+(16-bit and E4M3 inputs), paged prefill, decode (16-bit and E4M3 caches)
+and multi-token decode over head sizes, group sizes, lengths, block sizes,
+masking and dtypes drawn together, so that combinations the hand-picked
+cases do not list are exercised too.  The draws are fixed (one generator,
+one seed); sizes are capped so that the oracle finishes each case in a
+second or two."""
 import numpy as np
 import pytest
 import torch
@@ -130,5 +131,74 @@ def test_random_decode(i):
         O_ref, lse_ref = oracle.prefill_paged(t["Q"], t["Kc"], t["Vc"], t["block_table"],
                                               t["seq_lens"], True)
     assert attn.last_error() == attn.OK
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
+def _e4m3_prefill_cases(n):
+    out = []
+    while len(out) < n:
+        d = _pick([64, 128, 256])
+        G = _pick([1, 2, 4, 8])
+        Hkv = _pick([1, 2])
+        causal = bool(_rng.randint(2))
+        n_q = int(_rng.randint(1, 500))
+        n_kv = n_q + int(_rng.randint(0, 700)) if causal else int(_rng.randint(1, 1000))
+        if Hkv * G * n_q * n_kv * d > _MAX_WORK:
+            continue
+        out.append((1, Hkv * G, Hkv, n_q, n_kv, d, causal, _pick(["f32", "bf16", "f16"])))
+    return out
+
+
+def _e4m3_decode_cases(n):
+    out = []
+    while len(out) < n:
+        d = _pick([64, 128, 256])
+        G = _pick([1, 2, 4, 8, 16, 32])
+        Hkv = _pick([1, 2])
+        S = int(_rng.randint(1, 7))
+        bs = _pick([16, 32, 64])
+        lens = [int(_rng.randint(1, 3000)) for _ in range(S)]
+        out.append((S, Hkv * G, Hkv, d, lens, bs))
+    return out
+
+
+E4M3_PREFILL = _e4m3_prefill_cases(12)
+E4M3_DECODE = _e4m3_decode_cases(12)
+
+
+@pytest.mark.parametrize("i", range(len(E4M3_PREFILL)),
+                         ids=[f"r{i}" for i in range(len(E4M3_PREFILL))])
+def test_random_prefill_e4m3(i):
+    # against the oracle fed the dequantised inputs (code * per-head scale),
+    # under the 16-bit rules
+    B, Hq, Hkv, n_q, n_kv, d, causal, outd = E4M3_PREFILL[i]
+    spec = W.PrefillSpec(B, Hq, Hkv, n_q, n_kv, d, causal, "bf16", outd)
+    t = W.make_prefill(spec, seed=400 + i)
+    qz = W.quantize_prefill_e4m3(t)
+    g = {k: v.cuda() for k, v in qz.items()}
+    O, lse = attn.prefill(g["Q"], g["K"], g["V"], causal, out_dtype=DT[outd],
+                          q_scale=g["q_scale"], k_scale=g["k_scale"], v_scale=g["v_scale"])
+    assert attn.last_error() == attn.OK
+    deq = {n: oracle.dequantize_e4m3(qz[n], qz[n.lower() + "_scale"], 1) for n in "QKV"}
+    O_ref, lse_ref = oracle.sdpa(deq["Q"], deq["K"], deq["V"], causal)
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("i", range(len(E4M3_DECODE)),
+                         ids=[f"r{i}" for i in range(len(E4M3_DECODE))])
+def test_random_decode_e4m3(i):
+    S, Hq, Hkv, d, lens, bs = E4M3_DECODE[i]
+    spec = W.DecodeSpec(S, Hq, Hkv, d, 1, max(lens), bs, "bf16", "e4m3", "bf16")
+    t = W.make_decode(spec, seed=500 + i, lens=lens)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    O, lse = attn.decode(g["q"], g["Kc"], g["Vc"], g["block_table"], g["seq_lens"],
+                         max_seq_len=max(lens), k_scale=g["k_scale"], v_scale=g["v_scale"],
+                         out_dtype=torch.float32)
+    assert attn.last_error() == attn.OK
+    O_ref, lse_ref = oracle.decode_paged(t["q"], t["Kc"], t["Vc"], t["block_table"],
+                                         t["seq_lens"], k_scale=t["k_scale"],
+                                         v_scale=t["v_scale"])
     assert_out(O, O_ref)
     assert_lse(lse, lse_ref)
