@@ -1,10 +1,10 @@
 """Seeded random configurations against the fp64 oracle: dense prefill
-(16-bit and E4M3 inputs), paged prefill, decode (16-bit and E4M3 caches)
-and multi-token decode over head sizes, group sizes, lengths, block sizes,
-masking and dtypes drawn together, so that combinations the hand-picked
-cases do not list are exercised too.  The draws are fixed (one generator,
-one seed); sizes are capped so that the oracle finishes each case in a
-second or two."""
+(16-bit and E4M3 inputs), paged prefill, decode (16-bit and E4M3 caches),
+multi-token decode and the backward, over head sizes, group sizes, lengths,
+block sizes, masking and dtypes drawn together, so that combinations the
+hand-picked cases do not list are exercised too.  The draws are fixed (one
+generator, one seed); sizes are capped so that the oracle finishes each
+case in a second or two."""
 import numpy as np
 import pytest
 import torch
@@ -202,3 +202,30 @@ def test_random_decode_e4m3(i):
                                          v_scale=t["v_scale"])
     assert_out(O, O_ref)
     assert_lse(lse, lse_ref)
+
+
+def _backward_cases(n):
+    out = []
+    while len(out) < n:
+        d = _pick([64, 128])
+        G = _pick([1, 2, 4])
+        Hkv = _pick([1, 2])
+        B = _pick([1, 2])
+        causal = bool(_rng.randint(2))
+        n_q = int(_rng.randint(1, 400))
+        n_kv = n_q + int(_rng.randint(0, 300)) if causal else int(_rng.randint(1, 500))
+        ind = _pick(["bf16", "f16"])
+        outd = _pick(["f32", ind])
+        out.append((B, Hkv * G, Hkv, n_q, n_kv, d, causal, ind, outd))
+    return out
+
+
+BACKWARD = _backward_cases(10)
+
+
+@pytest.mark.parametrize("i", range(len(BACKWARD)), ids=[f"r{i}" for i in range(len(BACKWARD))])
+def test_random_backward(i):
+    # the backward tests' own check (fp32 and 16-bit O, gated per element by
+    # the bound derived from the 16-bit rounding of P and dS)
+    from tests import test_gpu_backward as bw
+    bw.test_backward_matches_oracle(BACKWARD[i])
