@@ -771,10 +771,13 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                     // 3070 -> 2930).  At d = 64 the softmax is the bound and
                     // the fused form measured slower, so it waits in turn.
                     constexpr bool kFused = D == 128;
+                    // E4M3 inputs (softmax-bound) wait for K(j+1) only where
+                    // tile 0's next S product needs it, behind its P.V issue
+                    constexpr bool kLateK = kFused && F8;
                     const bool waited =
                         kFused ? mbar_wait3(b_vfull(vs), (j / C::NV) & 1, true, b_kfull(ks),
-                                            (kn / C::NK) & 1, need_k, b_pfull(0), j & 1,
-                                            j < nb[0], abort_flag, err)
+                                            (kn / C::NK) & 1, need_k && !kLateK, b_pfull(0),
+                                            j & 1, j < nb[0], abort_flag, err)
                                : (mbar_wait(b_vfull(vs), (j / C::NV) & 1, abort_flag, err) &&
                                   (!need_k || mbar_wait(b_kfull(ks), (kn / C::NK) & 1,
                                                         abort_flag, err)));
@@ -792,10 +795,25 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                             tc_fence_after();
                         }
                         issue_pv(0, vs, j == 0);
+                        if constexpr (kLateK) {
+                            if (need_k &&
+                                !mbar_wait(b_kfull(ks), (kn / C::NK) & 1, abort_flag, err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
                         if (kn < nb[0]) {
                             issue_qk(0, ks);
                             tc_commit(b_sfull(0));
                         }
+                    } else if constexpr (kLateK) {
+                        if (need_k &&
+                            !mbar_wait(b_kfull(ks), (kn / C::NK) & 1, abort_flag, err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                     }
                     if (j < nb[1]) {
                         if (!mbar_wait(b_pfull(1), j & 1, abort_flag, err)) {
