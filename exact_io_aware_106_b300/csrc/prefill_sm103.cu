@@ -42,11 +42,14 @@
 // the same swizzled f16 layout that 16-bit inputs arrive in.  The scales
 // fold into the score factor (q_scale * k_scale) and the epilogue (v_scale).
 //
-// Scores are in the log2 domain (c = scale * log2 e).  The reference max
-// m is only moved when a block's max exceeds it by more than 8, so p stays
-// <= 2^8.  u / l does not depend on which reference value is subtracted
-// (the max-subtraction invariance of §8); keeping a slightly stale one
-// avoids most O rescales.
+// Scores are in the log2 domain (c = scale * log2 e).  u / l does not depend
+// on which reference value is subtracted (the max-subtraction invariance of
+// §8), so the reference max m is kept stale: a block's P is computed
+// against it at once and kept while no row's sum of p exceeds 2^15 (then no
+// p does, and P stays inside the f16 range) -- the row max is formed only
+// for a row's first block and when that test fails, and then m moves only
+// if the block's max exceeds it by more than 8.  This spares the row max on
+// almost every block and most O rescales.
 #include <atomic>
 
 #include "common.cuh"
@@ -65,6 +68,10 @@ constexpr int kConvWarp = 10;
 constexpr int kSplitKeys = 512; // rows seeing fewer keys carry the P residual
 
 constexpr float kRescaleThreshold = 8.0f;
+// a block computed against the reference max is kept while no row's sum of
+// p exceeds this (so no p does: every p is at most its row's sum), which
+// keeps each p inside the f16 range of the P operand
+constexpr float kSumLimit = 32768.0f;
 // Registers per thread: 384 threads launch with 168 each (the most that three
 // warps per SM sub-partition allow); the producer / MMA / converter
 // warpgroup (warps 8-11) hands most of its share to the two softmax
@@ -873,7 +880,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
         const float *ksc = F8 ? sc.k + static_cast<size_t>(bkv) * sc.kh : nullptr;
         float k_next = (F8 && live) ? ksc[0] : 1.0f;
         float m = -INFINITY, l = 0.f;
-        bool ok = true;
+        bool ok = true, ref_all = false;
 
         // The tile whose S product is the last to read each K stage (tile
         // 1, which has at least tile 0's blocks, unless it lies past n_q)
@@ -919,29 +926,42 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                     if (k > lim)
                         s[k] = -INFINITY;
             }
-            // row max as a tree of three-input maxima: eight independent
-            // chains taking two scores per step, then 8 -> 1
-            float mx8[8];
+            // Once every row of the warp has a reference max, P is computed
+            // against it straight away: p >= 0, so the block's sum bounds
+            // every p, and while no row's sum exceeds kSumLimit the
+            // reference stands and the row max is never formed.  Otherwise
+            // (a score far above the reference, or a non-finite one) the
+            // block is redone from its row max, as for the first block.
+            float sum = 0.f, alpha = 1.0f, m_use = m;
+            bool kept = false;
+            if (ref_all && !split) {
+                sum = exp_pack_store<BN, PB, false>(s, c, -m, tS);
+                kept = __all_sync(0xffffffffu, sum <= kSumLimit);
+            }
+            if (!kept) {
+                // row max as a tree of three-input maxima: eight independent
+                // chains taking two scores per step, then 8 -> 1
+                float mx8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                mx8[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+                for (int i = 0; i < 8; ++i)
+                    mx8[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-            for (int k = 16; k < BN; k += 2)
-                mx8[(k >> 1) & 7] = max3(mx8[(k >> 1) & 7], s[k], s[k + 1]);
-            const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
-                                   fmaxf(max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_blk = mx * c;
-            float m_use = m;
-            if (m_blk > m + kRescaleThreshold || m == -INFINITY)
-                m_use = fmaxf(m_blk, m);
-            const float alpha =
-                (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
-            const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
-            const float sum = split ? exp_pack_store<BN, PB, true>(s, c, neg, tS)
-                                    : exp_pack_store<BN, PB, false>(s, c, neg, tS);
+                for (int k = 16; k < BN; k += 2)
+                    mx8[(k >> 1) & 7] = max3(mx8[(k >> 1) & 7], s[k], s[k + 1]);
+                const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                                       fmaxf(max3(mx8[3], mx8[4], mx8[5]),
+                                             fmaxf(mx8[6], mx8[7])));
+                const float m_blk = mx * c;
+                if (m_blk > m + kRescaleThreshold || m == -INFINITY)
+                    m_use = fmaxf(m_blk, m);
+                alpha = (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
+                const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
+                sum = split ? exp_pack_store<BN, PB, true>(s, c, neg, tS)
+                            : exp_pack_store<BN, PB, false>(s, c, neg, tS);
+            }
             // O_t holds the sum over earlier blocks (their MMAs completed
             // before S_t of this block was produced); rescale it in place.
-            if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
+            if (!kept && __any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t u[32];
@@ -965,6 +985,7 @@ __global__ void __launch_bounds__(Cfg<D, F8>::THREADS, 1)
                 mbar_arrive(b_pfull(t));
             l = l * alpha + sum;
             m = m_use;
+            ref_all = __all_sync(0xffffffffu, m != -INFINITY);
         }
         if (ok && nb[t] > 0)
             ok = mbar_wait_warp(b_ofull, 0, abort_flag, err);
@@ -1439,7 +1460,7 @@ __global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
         const float *ksc = F8 ? sc.k + static_cast<size_t>(bkv) * sc.kh : nullptr;
         float k_next = (F8 && nb > 0) ? ksc[0] : 1.0f;
         float m = -INFINITY, l = 0.f;
-        bool ok = true;
+        bool ok = true, ref_all = false;
         for (int j = 0; j < nb; ++j) {
             const float c = F8 ? cq * k_next : cq;
             if constexpr (F8)
@@ -1472,41 +1493,51 @@ __global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
                     if (k > lim)
                         s[k] = -INFINITY;
             }
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                mx8[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-            for (int k = 16; k < BN; k += 2)
-                mx8[(k >> 1) & 7] = max3(mx8[(k >> 1) & 7], s[k], s[k + 1]);
-            const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
-                                   fmaxf(max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_blk = mx * c;
-            float m_use = m;
-            if (m_blk > m + pf::kRescaleThreshold || m == -INFINITY)
-                m_use = fmaxf(m_blk, m);
-            const float alpha =
-                (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
-            const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
-            if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
-                // O must hold exactly the blocks before j: wait for P_(j-1) V_(j-1)
-                if (!mbar_wait_warp(b_odone, (j - 1) & 1, abort_flag, err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll 1
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t u[32];
-                    tmem_ld32(tO + ch * 32, u);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-                    tmem_st32(tO + ch * 32, u);
-                }
+            // P against the reference max first, kept while no row's sum
+            // exceeds the limit; else redone from the row max, as in the
+            // d <= 128 kernel
+            float sum = 0.f, alpha = 1.0f, m_use = m;
+            bool kept = false;
+            if (ref_all && !split) {
+                sum = pf::exp_pack_store<BN, PB, false>(s, c, -m, tS);
+                kept = __all_sync(0xffffffffu, sum <= pf::kSumLimit);
             }
-            const float sum = split ? pf::exp_pack_store<BN, PB, true>(s, c, neg, tS)
-                                    : pf::exp_pack_store<BN, PB, false>(s, c, neg, tS);
+            if (!kept) {
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    mx8[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+                for (int k = 16; k < BN; k += 2)
+                    mx8[(k >> 1) & 7] = max3(mx8[(k >> 1) & 7], s[k], s[k + 1]);
+                const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                                       fmaxf(max3(mx8[3], mx8[4], mx8[5]),
+                                             fmaxf(mx8[6], mx8[7])));
+                const float m_blk = mx * c;
+                if (m_blk > m + pf::kRescaleThreshold || m == -INFINITY)
+                    m_use = fmaxf(m_blk, m);
+                alpha = (m_use == m) ? 1.0f : ((m == -INFINITY) ? 0.f : ex2(m - m_use));
+                const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
+                if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
+                    // O must hold exactly the blocks before j: wait for P_(j-1) V_(j-1)
+                    if (!mbar_wait_warp(b_odone, (j - 1) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t u[32];
+                        tmem_ld32(tO + ch * 32, u);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                        tmem_st32(tO + ch * 32, u);
+                    }
+                }
+                sum = split ? pf::exp_pack_store<BN, PB, true>(s, c, neg, tS)
+                            : pf::exp_pack_store<BN, PB, false>(s, c, neg, tS);
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -1514,6 +1545,7 @@ __global__ void __launch_bounds__(threads<F8, PAGED>(), 1)
                 mbar_arrive(b_pfull(buf));
             l = l * alpha + sum;
             m = m_use;
+            ref_all = __all_sync(0xffffffffu, m != -INFINITY);
         }
         if (ok && nb > 0)
             ok = mbar_wait_warp(b_ofull, 0, abort_flag, err);

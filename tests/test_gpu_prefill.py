@@ -92,6 +92,53 @@ def test_prefill_large_scores_do_not_overflow():
     assert_lse(lse, lse_ref)
 
 
+def _rising_inputs(n, d, seed, rise=40.0, noise=0.1):
+    """Scores that climb across the key blocks: every query component is
+    about 1 and key j's components about r_j, r_j rising linearly so that
+    the log2-domain score climbs by `rise` over the sequence (about 5 per
+    128-key block at n = 1024), so each row's reference max goes stale
+    block after block.  The rows' weights stay spread over a few dozen
+    keys: far more peaked rows would let the 16-bit rounding of P alone
+    approach the 2e-3 gate, whatever the reference."""
+    g = torch.Generator().manual_seed(seed)
+    r_max = rise / (1.4426950408889634 * d ** 0.5)
+    Q = 1.0 + noise * torch.randn(1, 2, n, d, generator=g)
+    ramp = torch.linspace(0.0, r_max, n).view(1, 1, n, 1)
+    K = ramp + noise * torch.randn(1, 1, n, d, generator=g)
+    V = torch.randn(1, 1, n, d, generator=g)
+    return Q, K, V
+
+
+@pytest.mark.parametrize("d,ind,causal", [(64, "bf16", False), (64, "f16", True),
+                                          (128, "bf16", True), (128, "f16", False),
+                                          (256, "bf16", True), (256, "f16", False)])
+def test_prefill_rising_scores_move_the_reference(d, ind, causal):
+    """A block is computed against the row's current reference max and kept
+    while its sum of p stays under the kernel's limit; scores that keep
+    climbing exercise both the kept blocks (p far above 1) and the blocks
+    redone from a new row max."""
+    Q, K, V = (x.to(DT[ind]) for x in _rising_inputs(1024, d, seed=d))
+    O_ref, lse_ref = oracle.sdpa(Q, K, V, causal)
+    O, lse = attn.prefill(Q.cuda(), K.cuda(), V.cuda(), causal, out_dtype=torch.float32)
+    assert attn.last_error() == attn.OK
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_prefill_e4m3_rising_scores_move_the_reference(d):
+    Q, K, V = (x.to(torch.bfloat16) for x in _rising_inputs(1024, d, seed=10 + d))
+    qz = W.quantize_prefill_e4m3({"Q": Q, "K": K, "V": V})
+    g = {k: v.cuda() for k, v in qz.items()}
+    O, lse = attn.prefill(g["Q"], g["K"], g["V"], True, out_dtype=torch.float32,
+                          q_scale=g["q_scale"], k_scale=g["k_scale"], v_scale=g["v_scale"])
+    assert attn.last_error() == attn.OK
+    deq = {n: oracle.dequantize_e4m3(qz[n], qz[n.lower() + "_scale"], 1) for n in "QKV"}
+    O_ref, lse_ref = oracle.sdpa(deq["Q"], deq["K"], deq["V"], True)
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
 def _sample_rows(n_q, rng, k=6):
     base = [0, 1, 127, 128, 255, 256, n_q - 1, n_q - 2]
     base += [int(x) for x in rng.integers(0, n_q, size=k)]
