@@ -36,9 +36,12 @@
 // up owning 4 consecutive output columns.  The per-head scales fold into the
 // score scale (k) and the partial (v).
 //
-// Scores are in the log2 domain (c = scale * log2 e); the reference max is
-// moved only when a unit's max exceeds it by more than 8, so p <= 2^8; u / l
-// does not depend on the reference (the max-subtraction invariance of §8).
+// Scores are in the log2 domain (c = scale * log2 e).  u / l does not depend
+// on the reference max subtracted (the max-subtraction invariance of §8), so
+// it is kept stale: it moves only when a unit's max exceeds it by more than
+// 8.  With E4M3 caches a unit's p is first taken against it and kept while
+// no lane's partial row sum exceeds 2^15 (so no p does), and the row max is
+// formed only for a row's first unit and when that test fails.
 #include <type_traits>
 
 #include "common.cuh"
@@ -109,6 +112,7 @@ constexpr int kThreads = (kNC + 1) * 32;
 constexpr int kMaxUnits = 256;  // units per CTA (tps <= 4096)
 constexpr int kSplitKeys = 512; // sequences shorter than this carry the P residual
 constexpr float kRescaleThreshold = 8.0f;
+constexpr float kSumLimit = 32768.0f; // keeps every kept p inside the f16 range
 
 // resident CTAs per SM.  A CTA serves NRT x NG 16-row tiles: its kNC
 // consumer warps form NG groups of kNC / NG, each group takes NRT tiles and
@@ -429,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT, NG>::MIN_CTAS)
         m[rt][0] = m[rt][1] = -INFINITY;
         l[rt][0] = l[rt][1] = 0.f;
     }
-    bool ok = true;
+    bool ok = true, ref_all = false;
 
     for (int u = wl; u < nunits; u += GW) {
         const int st = u % Ly::NST;
@@ -531,30 +535,54 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT, NG>::MIN_CTAS)
                         sc[4 + i] = -INFINITY;
                 }
             }
-            float mx[2] = {max4(sc[0], sc[1], sc[2], sc[3]), max4(sc[4], sc[5], sc[6], sc[7])};
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-            }
-            float alpha[2], neg[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                float mu = m[rt][r];
-                if (mx[r] > m[rt][r] + kRescaleThreshold || m[rt][r] == -INFINITY)
-                    mu = fmaxf(mx[r], m[rt][r]);
-                alpha[r] = (mu == m[rt][r]) ? 1.0f
-                                            : ((m[rt][r] == -INFINITY) ? 0.f : ex2(m[rt][r] - mu));
-                neg[r] = (mu == -INFINITY) ? 0.f : -mu;
-                m[rt][r] = mu;
-            }
+            // E4M3 caches (bound by the consumers' instruction issue): once
+            // every row of the warp has a reference max, p is taken against
+            // it at once and kept while no lane's partial row sum exceeds
+            // kSumLimit (each p is at most its lane's partial sum);
+            // otherwise the unit is redone from the row max.  (16-bit caches,
+            // near the copy bandwidth, measured no gain from it.)
             float p[8];
+            float alpha[2] = {1.0f, 1.0f};
+            bool kept = false;
+            if (KV8 && ref_all) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                p[i] = ex2(sc[i] + neg[i >> 2]);
-            l[rt][0] = l[rt][0] * alpha[0] + ((p[0] + p[1]) + (p[2] + p[3]));
-            l[rt][1] = l[rt][1] * alpha[1] + ((p[4] + p[5]) + (p[6] + p[7]));
-            if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+                for (int i = 0; i < 8; ++i)
+                    p[i] = ex2(sc[i] - m[rt][i >> 2]);
+                const float ps0 = (p[0] + p[1]) + (p[2] + p[3]);
+                const float ps1 = (p[4] + p[5]) + (p[6] + p[7]);
+                kept = __all_sync(0xffffffffu, ps0 <= kSumLimit && ps1 <= kSumLimit);
+                if (kept) {
+                    l[rt][0] += ps0;
+                    l[rt][1] += ps1;
+                }
+            }
+            if (!kept) {
+                float mx[2] = {max4(sc[0], sc[1], sc[2], sc[3]),
+                               max4(sc[4], sc[5], sc[6], sc[7])};
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                }
+                float neg[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    float mu = m[rt][r];
+                    if (mx[r] > m[rt][r] + kRescaleThreshold || m[rt][r] == -INFINITY)
+                        mu = fmaxf(mx[r], m[rt][r]);
+                    alpha[r] = (mu == m[rt][r])
+                                   ? 1.0f
+                                   : ((m[rt][r] == -INFINITY) ? 0.f : ex2(m[rt][r] - mu));
+                    neg[r] = (mu == -INFINITY) ? 0.f : -mu;
+                    m[rt][r] = mu;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    p[i] = ex2(sc[i] + neg[i >> 2]);
+                l[rt][0] = l[rt][0] * alpha[0] + ((p[0] + p[1]) + (p[2] + p[3]));
+                l[rt][1] = l[rt][1] * alpha[1] + ((p[4] + p[5]) + (p[6] + p[7]));
+            }
+            if (!kept && __any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
                 for (int n = 0; n < D / 8; ++n) {
                     o[rt][n][0] *= alpha[0];
@@ -632,6 +660,13 @@ __global__ void __launch_bounds__(kThreads, Lay<D, KV8, NRT, NG>::MIN_CTAS)
             fence_proxy_async_smem(); // the zeroing stores precede the next copy into this stage
         if (lane == 0)
             mbar_arrive(b_empty(st));
+        if constexpr (KV8) {
+            bool fin = true;
+#pragma unroll
+            for (int rt = 0; rt < NRT; ++rt)
+                fin = fin && m[rt][0] != -INFINITY && m[rt][1] != -INFINITY;
+            ref_all = __all_sync(0xffffffffu, fin);
+        }
     }
     // the four lanes of a quad hold partial row sums of the same rows
 #pragma unroll

@@ -77,6 +77,51 @@ def test_decode_e4m3(d, G):
     assert_out(O[long_rows], O_src[long_rows], atol=ATOL_FP8)
 
 
+def _rising_cache(t, spec, rise=40.0, noise=0.1, seed=0):
+    """Rewrite a decode case so that the scores climb along each sequence:
+    q components about 1, the key of logical token p about r_p (r rising
+    linearly to a log2-domain score of `rise` at the longest sequence's
+    end).  Each row's reference max then goes stale unit after unit."""
+    g = torch.Generator().manual_seed(seed)
+    S, d, bs = spec.num_seqs, spec.d, spec.block_size
+    t["q"] = (1.0 + noise * torch.randn(S, spec.Hq, d, generator=g)).to(t["q"].dtype)
+    r_max = rise / (1.4426950408889634 * d ** 0.5)
+    K = noise * torch.randn(t["Vc"].shape, generator=g)
+    lens = t["seq_lens"].tolist()
+    for s_i, n in enumerate(lens):
+        for b in range((n + bs - 1) // bs):
+            pos = torch.arange(b * bs, b * bs + bs, dtype=torch.float32)
+            K[int(t["block_table"][s_i, b])] += (r_max * pos / max(lens)).view(1, bs, 1)
+    return K
+
+
+@pytest.mark.parametrize("kv,d,G", [("e4m3", 64, 4), ("e4m3", 64, 32), ("e4m3", 128, 8),
+                                    ("e4m3", 256, 16), ("bf16", 128, 4)])
+def test_decode_rising_scores_move_the_reference(kv, d, G):
+    """Units are computed against each row's current reference max and kept
+    while no partial row sum of p exceeds the kernel's limit; climbing
+    scores exercise kept units (p far above 1) and units redone from a new
+    row max."""
+    lens = [2000, 1500, 600, 37]
+    spec = W.DecodeSpec(len(lens), 2 * G, 2, d, 1, max(lens), 16, "bf16", kv, "bf16")
+    t = W.make_decode(spec, seed=5, lens=lens)
+    K = _rising_cache(t, spec, seed=d + G)
+    if kv == "e4m3":
+        t["Kc"], t["k_scale"] = W.quantize_e4m3_per_head(K.to(torch.bfloat16), 1)
+    else:
+        t["Kc"] = K.to(torch.bfloat16)
+    g = _dev(t)
+    O, lse = attn.decode(g["q"], g["Kc"], g["Vc"], g["block_table"], g["seq_lens"],
+                         max_seq_len=max(lens), k_scale=g["k_scale"], v_scale=g["v_scale"],
+                         out_dtype=torch.float32)
+    assert attn.last_error() == attn.OK
+    O_ref, lse_ref = oracle.decode_paged(t["q"], t["Kc"], t["Vc"], t["block_table"],
+                                         t["seq_lens"], k_scale=t["k_scale"],
+                                         v_scale=t["v_scale"])
+    assert_out(O, O_ref)
+    assert_lse(lse, lse_ref)
+
+
 def test_decode_empty_and_boundary_lengths():
     lens = [0, 16, 32, 1, 0]
     spec = W.DecodeSpec(5, 4, 2, 128, 1, 32, 16, "bf16", "bf16", "bf16")
