@@ -61,9 +61,13 @@ struct Cfg {
     static constexpr int OFF_Y = OFF_X + NX * TILE;
     static constexpr int OFF_ROW = OFF_Y + NY * TILE; // -lse2 / -D of 128 rows, 2 buffers
     static constexpr int OFF_BAR = OFF_ROW + 2 * 2 * BT * 4;
+    // the dK/dV kernel releases a step's X and Y stages together, on one
+    // barrier per step modulo NU (a common multiple of the ring depths)
+    static constexpr int NU = D == 128 ? 6 : 4;
+    static_assert(NU % NX == 0 && NU % NY == 0, "NU must be a multiple of both ring depths");
     // afull, xfull/xempty[NX], yfull/yempty[NY], sready, dpready, sfree,
-    // pready[2], done, drain
-    static constexpr int NBAR = 1 + 2 * NX + 2 * NY + 3 + 2 + 2;
+    // pready[2], done, drain, used[NU]
+    static constexpr int NBAR = 1 + 2 * NX + 2 * NY + 3 + 2 + 2 + NU;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_MISC + 64;  // from the 1024-aligned base
     // room to align the base; at d = 128 the rings leave less than 1024
@@ -262,16 +266,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *s_row = reinterpret_cast<float *>(base + C::OFF_ROW);
     const uint32_t bar0 = base_s + C::OFF_BAR;
     const uint32_t b_afull = bar0;
+    // (the slots of the per-ring empty barriers, which the dQ kernel uses,
+    // stay unused here: b_used below releases both rings)
     auto b_xfull = [&](int i) { return bar0 + 8u * (1 + i); };
-    auto b_xempty = [&](int i) { return bar0 + 8u * (1 + C::NX + i); };
     auto b_yfull = [&](int i) { return bar0 + 8u * (1 + 2 * C::NX + i); };
-    auto b_yempty = [&](int i) { return bar0 + 8u * (1 + 2 * C::NX + C::NY + i); };
     const uint32_t b_s = bar0 + 8u * (1 + 2 * C::NX + 2 * C::NY); // scores ready
     const uint32_t b_dp = b_s + 8u;                   // second product ready
     const uint32_t b_sfree = b_s + 16u;               // scores loaded by the softmax warps
     auto b_pready = [&](int e) { return b_s + 8u * (3 + e); }; // half e packed
     const uint32_t b_done = b_s + 40u;
     const uint32_t b_drain = b_done + 8u;
+    // step u's Q and dO stages consumed (one commit releases both rings)
+    auto b_used = [&](int u) { return b_drain + 8u * (1 + u % C::NU); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);
 
@@ -292,14 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(b_afull, 1);
-        for (int i = 0; i < C::NX; ++i) {
+        for (int i = 0; i < C::NX; ++i)
             mbar_init(b_xfull(i), 1);
-            mbar_init(b_xempty(i), 1);
-        }
-        for (int i = 0; i < C::NY; ++i) {
+        for (int i = 0; i < C::NY; ++i)
             mbar_init(b_yfull(i), 1);
-            mbar_init(b_yempty(i), 1);
-        }
         mbar_init(b_s, 1);
         mbar_init(b_dp, 1);
         mbar_init(b_sfree, kSoftmaxWarps);
@@ -307,6 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_pready(e), kSoftmaxWarps);
         mbar_init(b_done, 1);
         mbar_init(b_drain, 1);
+        for (int i = 0; i < C::NU; ++i)
+            mbar_init(b_used(i), 1);
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -332,8 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             for (int t = 0; t < nsteps; ++t) {
                 const int st = t % n;
-                if (t >= n && !mbar_wait(is_x ? b_xempty(st) : b_yempty(st), ((t / n) - 1) & 1,
-                                         abort_flag, err))
+                // stage st was last read by step t - n.  A waiter is never
+                // two phases behind on b_used: step t - n + NU cannot be
+                // consumed before this ring has refilled its stage, which
+                // needs this very wait
+                if (t >= n && !mbar_wait(b_used(t - n), ((t - n) / C::NU) & 1, abort_flag, err))
                     break;
                 const int h = hk * sh.G + t / nq_steps;
                 const int qb = qb0 + t % nq_steps;
@@ -406,8 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    false);
                 mma_tmem_a_half<D>(tmem + C::ACC1, tmem + C::DP_COL + 80, sQ(xt), 1, idesc_acc,
                                    false);
-                tc_commit(b_xempty(xt)); // step t's Q and dO consumed
-                tc_commit(b_yempty(yt));
+                tc_commit(b_used(t)); // step t's Q and dO consumed
                 if (next) {
                     tc_fence_after();
                     // after half 1's products, which read these columns (the
